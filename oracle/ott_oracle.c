@@ -1,0 +1,607 @@
+/*
+ * ott_oracle.c -- plain CPU oracle for Outlier Tokens Tracing (OTT) KV-cache
+ * quantization: the every-G flush and the three-store decode attention.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark load this file. It shares no code, header,
+ * table or helper with the CUDA library and is written to be read against
+ * the sources, not to be fast. It never calls into the CUDA library.
+ *
+ * Sources (page title / section):
+ *  [blog]  "Accurate KV Cache Quantization with Outlier Tokens Tracing"
+ *          (zijie-tian.site): sec. 3.1 (quantize the latest group every G
+ *          tokens; rank candidates by the key norm), sec. 3.2 (outlier pool
+ *          of capacity P, new tokens compete with pool tokens, a displaced
+ *          token is written back to the main cache), sec. 3.3 (decode: the
+ *          query meets quantized, residual-window and pool keys; concat,
+ *          softmax, times the matching values), the flowchart.
+ *  [ss]    "Accurate KV Cache Quantization with Outlier Tokens Tracing"
+ *          (sciencestack.ai, arXiv 2505.10938): TL;DR (three KV caches, pool
+ *          filled by key magnitude, group quantization every G tokens),
+ *          Abstract (keys quantized per channel, values per token),
+ *          Fig. 1(c) (keep the tokens whose keys have the smallest
+ *          magnitude), Fig. 2 (decoding and quantization stages).
+ *  [kivi]  the KIVI reference listed on the mlsanity.com page ("asymmetric
+ *          2bit"): min/max asymmetric quantization.
+ *
+ * Readings taken where the pages are silent (each is restated where used):
+ *  R1  The R newest tokens stay fp16; once G+R tokens wait unquantized, the
+ *      G oldest of them form the group that is flushed (ring holds < G+R).
+ *  R2  A prefill of L tokens is L appends, in token order.
+ *  R3  The outlier score is the squared L2 norm of the fp16 key, summed in
+ *      fp32 in channel order 0..d-1 (same ranking as the L2 norm).
+ *  R4  Candidates at a flush are the pool plus the whole group; the P
+ *      smallest (norm, token index) pairs stay, ties go to the lower index.
+ *  R5  Evicted pool tokens and the group's non-outliers together form the
+ *      new quantized block, stored in ascending token order; a block is
+ *      made at every flush, even when it holds no token.
+ *  R6  Keys: one (scale, zero) per channel over the block's tokens. Values:
+ *      one (scale, zero) per token per 32 consecutive channels. Both fp16.
+ *  R7  mn, mx over the valid values (as fp32; -0 orders below +0);
+ *      s = fp16_rn((mx - mn) / 3) in fp32 with IEEE division; z = mn;
+ *      code = 0 if s == 0, else clamp(rint((x - z) / s), 0, 3) with fp32
+ *      subtraction and division and round-half-to-even.
+ *  R8  Pool and residual tokens keep their fp16 values ("full precision").
+ *  R9  Decode attends over every token seen, with scale 1/sqrt(d); query
+ *      head h reads kv head h / (Hq / Hkv).
+ *
+ * Floating point: decisions that yield integers or stored bits (norms,
+ * scales, zeros, codes) are taken in fp32 exactly as the library takes them.
+ * The attention output is computed in double. Build with -ffp-contract=off.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 <-> binary32, written from the format's definition.    */
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.        */
+/* ------------------------------------------------------------------------ */
+
+float orc_h2f(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)m, -24);                   /* zero / subnormal */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(m | 0x400), e - 25);      /* (1024+m) * 2^(e-25) */
+    return sign ? -v : v;
+}
+
+/* Round |f| to the binary16 grid with ties to even, then encode. */
+uint16_t orc_f2h(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7e00u);
+    double a = fabs((double)f);
+    if (isinf(f))
+        return (uint16_t)(sign | 0x7c00u);
+    if (a == 0.0)
+        return sign;
+    /* grid spacing at a: 2^-24 below 2^-14 (subnormals), else 2^(E-10) */
+    int E;
+    frexp(a, &E);                 /* a = frac * 2^E, frac in [0.5, 1) */
+    E -= 1;                       /* a in [2^E, 2^(E+1)) */
+    int qexp = (E < -14) ? -24 : E - 10;
+    double y = ldexp(a, -qexp);   /* exact: a has 24 significant bits */
+    double r = floor(y);
+    double frac = y - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    double rounded = ldexp(r, qexp);
+    if (rounded >= 65536.0)
+        return (uint16_t)(sign | 0x7c00u);           /* overflow to inf */
+    if (rounded < ldexp(1.0, -14))                    /* subnormal (or 0) */
+        return (uint16_t)(sign | (uint16_t)(rounded / ldexp(1.0, -24)));
+    int E2;
+    frexp(rounded, &E2);
+    E2 -= 1;
+    int mant = (int)(ldexp(rounded, 10 - E2)) - 1024;
+    return (uint16_t)(sign | (uint16_t)((E2 + 15) << 10) | (uint16_t)mant);
+}
+
+void orc_f2h_array(const float *x, uint16_t *out, long long n)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = orc_f2h(x[i]);
+}
+
+void orc_h2f_array(const uint16_t *x, float *out, long long n)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = orc_h2f(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Outlier score (R3): squared L2 norm of an fp16 key, fp32, channel order. */
+/* ------------------------------------------------------------------------ */
+
+float orc_norm(const uint16_t *k, int d)
+{
+    float s = 0.0f;
+    for (int c = 0; c < d; ++c) {
+        float kc = orc_h2f(k[c]);
+        s = s + kc * kc;
+    }
+    return s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Asymmetric 2-bit quantization of n values x[0], x[stride], ... (R7).     */
+/* Writes the fp16 bits of scale and zero, and one code per value.           */
+/* ------------------------------------------------------------------------ */
+
+static int below(float a, float b)  /* a < b, with -0 ordered below +0 */
+{
+    return a < b || (a == b && signbit(a) && !signbit(b));
+}
+
+void orc_quant_group(const uint16_t *x, int n, int stride, uint16_t *s_out,
+                     uint16_t *z_out, uint8_t *code, int code_stride)
+{
+    if (n <= 0) {
+        *s_out = 0;
+        *z_out = 0;
+        return;
+    }
+    float mn = orc_h2f(x[0]), mx = mn;
+    for (int i = 1; i < n; ++i) {
+        float v = orc_h2f(x[(long)i * stride]);
+        if (below(v, mn))
+            mn = v;
+        if (below(mx, v))
+            mx = v;
+    }
+    uint16_t s16 = orc_f2h((mx - mn) / 3.0f);
+    uint16_t z16 = orc_f2h(mn);                       /* exact: mn is fp16 */
+    float s = orc_h2f(s16), z = orc_h2f(z16);
+    for (int i = 0; i < n; ++i) {
+        int q = 0;
+        if (s != 0.0f) {
+            float v = orc_h2f(x[(long)i * stride]);
+            q = (int)rintf((v - z) / s);
+            if (q < 0)
+                q = 0;
+            if (q > 3)
+                q = 3;
+        }
+        code[(long)i * code_stride] = (uint8_t)q;
+    }
+    *s_out = s16;
+    *z_out = z16;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache state, one unit per (sequence b, kv head).                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int c;              /* valid tokens in the block */
+    int32_t *idx;       /* [c] token indices, ascending */
+    uint8_t *kcode;     /* [c][d] key codes 0..3 */
+    uint16_t *ks, *kz;  /* [d] per-channel key scale/zero (fp16 bits) */
+    uint8_t *vcode;     /* [c][d] value codes 0..3 */
+    uint16_t *vs, *vz;  /* [c][d/32] per-token value scale/zero (fp16 bits) */
+} orc_block;
+
+typedef struct {
+    /* unquantized residual tokens, oldest first */
+    int tail_n, tail_cap;
+    int32_t *tail_idx;
+    uint16_t *tail_k, *tail_v;   /* [tail_cap][d] */
+    /* outlier pool, kept sorted by (norm, idx) ascending */
+    int pool_n;
+    int32_t *pool_idx;           /* [P] */
+    float *pool_norm;            /* [P] */
+    uint16_t *pool_k, *pool_v;   /* [P][d] */
+    /* quantized blocks, one per flush */
+    int nb, nb_cap;
+    orc_block *blk;
+} orc_unit;
+
+typedef struct {
+    int B, Hq, Hkv, d, G, R, P;
+    long long T;
+    orc_unit *u;        /* [B*Hkv] */
+} orc_cache;
+
+typedef struct {
+    float norm;
+    int32_t idx;
+    const uint16_t *k, *v;
+} orc_cand;
+
+static int cand_cmp_norm(const void *a, const void *b)
+{
+    const orc_cand *x = (const orc_cand *)a, *y = (const orc_cand *)b;
+    if (x->norm < y->norm) return -1;
+    if (x->norm > y->norm) return 1;
+    return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
+}
+
+static int cand_cmp_idx(const void *a, const void *b)
+{
+    const orc_cand *x = (const orc_cand *)a, *y = (const orc_cand *)b;
+    return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
+}
+
+void orc_destroy(void *hp)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (!h)
+        return;
+    for (int i = 0; i < h->B * h->Hkv; ++i) {
+        orc_unit *u = &h->u[i];
+        free(u->tail_idx); free(u->tail_k); free(u->tail_v);
+        free(u->pool_idx); free(u->pool_norm); free(u->pool_k); free(u->pool_v);
+        for (int j = 0; j < u->nb; ++j) {
+            orc_block *b = &u->blk[j];
+            free(b->idx); free(b->kcode); free(b->ks); free(b->kz);
+            free(b->vcode); free(b->vs); free(b->vz);
+        }
+        free(u->blk);
+    }
+    free(h->u);
+    free(h);
+}
+
+void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
+{
+    if (B < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || d < 32 || d % 32 ||
+        G < 1 || R < 0 || P < 0)
+        return NULL;
+    orc_cache *h = (orc_cache *)calloc(1, sizeof(orc_cache));
+    h->B = B; h->Hq = Hq; h->Hkv = Hkv; h->d = d; h->G = G; h->R = R; h->P = P;
+    h->u = (orc_unit *)calloc((size_t)B * Hkv, sizeof(orc_unit));
+    for (int i = 0; i < B * Hkv; ++i) {
+        orc_unit *u = &h->u[i];
+        u->tail_cap = G + R;
+        u->tail_idx = (int32_t *)calloc(u->tail_cap, sizeof(int32_t));
+        u->tail_k = (uint16_t *)calloc((size_t)u->tail_cap * d, 2);
+        u->tail_v = (uint16_t *)calloc((size_t)u->tail_cap * d, 2);
+        u->pool_idx = (int32_t *)calloc(P + 1, sizeof(int32_t));
+        u->pool_norm = (float *)calloc(P + 1, sizeof(float));
+        u->pool_k = (uint16_t *)calloc((size_t)(P + 1) * d, 2);
+        u->pool_v = (uint16_t *)calloc((size_t)(P + 1) * d, 2);
+    }
+    return h;
+}
+
+/* The flush (R1, R3-R7): the oldest G residual tokens meet the pool. */
+static void flush_unit(orc_cache *h, orc_unit *u)
+{
+    const int d = h->d, G = h->G, P = h->P, ng = d / 32;
+    const int ncand = u->pool_n + G;
+    orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * ncand);
+    for (int i = 0; i < u->pool_n; ++i) {
+        cand[i].norm = u->pool_norm[i];
+        cand[i].idx = u->pool_idx[i];
+        cand[i].k = u->pool_k + (size_t)i * d;
+        cand[i].v = u->pool_v + (size_t)i * d;
+    }
+    for (int i = 0; i < G; ++i) {
+        orc_cand *c = &cand[u->pool_n + i];
+        c->k = u->tail_k + (size_t)i * d;
+        c->v = u->tail_v + (size_t)i * d;
+        c->idx = u->tail_idx[i];
+        c->norm = orc_norm(c->k, d);
+    }
+    /* R4: order by (norm, index); the first P stay in the pool. */
+    qsort(cand, ncand, sizeof(orc_cand), cand_cmp_norm);
+    const int keep = ncand < P ? ncand : P;
+    const int c = ncand - keep;
+    /* R5: the rest, in token order, become the new block. */
+    qsort(cand + keep, c, sizeof(orc_cand), cand_cmp_idx);
+
+    if (u->nb == u->nb_cap) {
+        u->nb_cap = u->nb_cap ? 2 * u->nb_cap : 16;
+        u->blk = (orc_block *)realloc(u->blk, sizeof(orc_block) * u->nb_cap);
+    }
+    orc_block *b = &u->blk[u->nb++];
+    b->c = c;
+    b->idx = (int32_t *)malloc(sizeof(int32_t) * (c + 1));
+    b->kcode = (uint8_t *)calloc((size_t)c * d + 1, 1);
+    b->vcode = (uint8_t *)calloc((size_t)c * d + 1, 1);
+    b->ks = (uint16_t *)calloc(d, 2);
+    b->kz = (uint16_t *)calloc(d, 2);
+    b->vs = (uint16_t *)calloc((size_t)c * ng + 1, 2);
+    b->vz = (uint16_t *)calloc((size_t)c * ng + 1, 2);
+    uint16_t *bk = (uint16_t *)malloc((size_t)(c + 1) * d * 2);
+    uint16_t *bv = (uint16_t *)malloc((size_t)(c + 1) * d * 2);
+    for (int t = 0; t < c; ++t) {
+        b->idx[t] = cand[keep + t].idx;
+        memcpy(bk + (size_t)t * d, cand[keep + t].k, (size_t)d * 2);
+        memcpy(bv + (size_t)t * d, cand[keep + t].v, (size_t)d * 2);
+    }
+    /* R6/R7: keys per channel over the block's tokens ... */
+    for (int ch = 0; ch < d; ++ch)
+        orc_quant_group(bk + ch, c, d, &b->ks[ch], &b->kz[ch], b->kcode + ch, d);
+    /* ... values per token per 32 channels. */
+    for (int t = 0; t < c; ++t)
+        for (int g = 0; g < ng; ++g)
+            orc_quant_group(bv + (size_t)t * d + 32 * g, 32, 1,
+                            &b->vs[(size_t)t * ng + g], &b->vz[(size_t)t * ng + g],
+                            b->vcode + (size_t)t * d + 32 * g, 1);
+
+    /* new pool: the first `keep` candidates (copy out before overwriting) */
+    uint16_t *nk = (uint16_t *)malloc((size_t)(keep + 1) * d * 2);
+    uint16_t *nv = (uint16_t *)malloc((size_t)(keep + 1) * d * 2);
+    int32_t *ni = (int32_t *)malloc(sizeof(int32_t) * (keep + 1));
+    float *nn = (float *)malloc(sizeof(float) * (keep + 1));
+    for (int i = 0; i < keep; ++i) {
+        memcpy(nk + (size_t)i * d, cand[i].k, (size_t)d * 2);
+        memcpy(nv + (size_t)i * d, cand[i].v, (size_t)d * 2);
+        ni[i] = cand[i].idx;
+        nn[i] = cand[i].norm;
+    }
+    memcpy(u->pool_k, nk, (size_t)keep * d * 2);
+    memcpy(u->pool_v, nv, (size_t)keep * d * 2);
+    memcpy(u->pool_idx, ni, sizeof(int32_t) * keep);
+    memcpy(u->pool_norm, nn, sizeof(float) * keep);
+    u->pool_n = keep;
+
+    /* drop the group from the residual list */
+    u->tail_n -= G;
+    memmove(u->tail_idx, u->tail_idx + G, sizeof(int32_t) * u->tail_n);
+    memmove(u->tail_k, u->tail_k + (size_t)G * d, (size_t)u->tail_n * d * 2);
+    memmove(u->tail_v, u->tail_v + (size_t)G * d, (size_t)u->tail_n * d * 2);
+
+    free(nk); free(nv); free(ni); free(nn);
+    free(bk); free(bv);
+    free(cand);
+}
+
+/* Append one token to unit u (R1): store it fp16, flush when G+R wait. */
+static void append_unit(orc_cache *h, orc_unit *u, long long t,
+                        const uint16_t *k, const uint16_t *v)
+{
+    const int d = h->d;
+    u->tail_idx[u->tail_n] = (int32_t)t;
+    memcpy(u->tail_k + (size_t)u->tail_n * d, k, (size_t)d * 2);
+    memcpy(u->tail_v + (size_t)u->tail_n * d, v, (size_t)d * 2);
+    u->tail_n += 1;
+    if (u->tail_n >= h->G + h->R)
+        flush_unit(h, u);
+}
+
+/* k, v: fp16 bits [B][Hkv][d]. */
+int orc_append(void *hp, const uint16_t *k, const uint16_t *v)
+{
+    orc_cache *h = (orc_cache *)hp;
+    const int U = h->B * h->Hkv;
+    for (int i = 0; i < U; ++i)
+        append_unit(h, &h->u[i], h->T, k + (size_t)i * h->d, v + (size_t)i * h->d);
+    h->T += 1;
+    return 0;
+}
+
+/* R2. K, V: fp16 bits [B][Hkv][L][d]; only on an empty cache. */
+int orc_prefill(void *hp, const uint16_t *K, const uint16_t *V, int L)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (h->T != 0 || L < 0)
+        return -2;
+    const int U = h->B * h->Hkv, d = h->d;
+    for (int i = 0; i < U; ++i)
+        for (int t = 0; t < L; ++t)
+            append_unit(h, &h->u[i], t, K + ((size_t)i * L + t) * d,
+                        V + ((size_t)i * L + t) * d);
+    h->T = L;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention for one query head (R8, R9), in double:                  */
+/* scores against every quantized, residual and pool key; one softmax over   */
+/* the concatenation; the weights times the matching (dequantized) values.   */
+/* ------------------------------------------------------------------------ */
+
+int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (h->T < 1 || b < 0 || b >= h->B || hq < 0 || hq >= h->Hq)
+        return -2;
+    const int d = h->d, ng = d / 32;
+    const orc_unit *u = &h->u[b * h->Hkv + hq / (h->Hq / h->Hkv)];
+    const double sigma = 1.0 / sqrt((double)d);
+    const long long n = h->T;
+    double *score = (double *)malloc(sizeof(double) * n);
+    double *q = (double *)malloc(sizeof(double) * d);
+    for (int c = 0; c < d; ++c)
+        q[c] = orc_h2f(qv[c]);
+
+    /* scores, segment by segment: quantized blocks, residual, pool */
+    long long m = 0;
+    for (int j = 0; j < u->nb; ++j) {
+        const orc_block *bl = &u->blk[j];
+        for (int t = 0; t < bl->c; ++t) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double kh = bl->kcode[(size_t)t * d + c] * (double)orc_h2f(bl->ks[c]) +
+                            (double)orc_h2f(bl->kz[c]);
+                acc += q[c] * kh;
+            }
+            score[m++] = sigma * acc;
+        }
+    }
+    for (int t = 0; t < u->tail_n; ++t) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += q[c] * orc_h2f(u->tail_k[(size_t)t * d + c]);
+        score[m++] = sigma * acc;
+    }
+    for (int t = 0; t < u->pool_n; ++t) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += q[c] * orc_h2f(u->pool_k[(size_t)t * d + c]);
+        score[m++] = sigma * acc;
+    }
+
+    /* softmax over the concatenated scores */
+    double mx = -INFINITY;
+    for (long long i = 0; i < m; ++i)
+        if (score[i] > mx)
+            mx = score[i];
+    double sum = 0.0;
+    for (long long i = 0; i < m; ++i) {
+        score[i] = exp(score[i] - mx);
+        sum += score[i];
+    }
+
+    /* weights times values, same segment order */
+    for (int c = 0; c < d; ++c)
+        out[c] = 0.0;
+    m = 0;
+    for (int j = 0; j < u->nb; ++j) {
+        const orc_block *bl = &u->blk[j];
+        for (int t = 0; t < bl->c; ++t) {
+            double p = score[m++];
+            for (int c = 0; c < d; ++c) {
+                size_t sg = (size_t)t * ng + c / 32;
+                double vh = bl->vcode[(size_t)t * d + c] * (double)orc_h2f(bl->vs[sg]) +
+                            (double)orc_h2f(bl->vz[sg]);
+                out[c] += p * vh;
+            }
+        }
+    }
+    for (int t = 0; t < u->tail_n; ++t) {
+        double p = score[m++];
+        for (int c = 0; c < d; ++c)
+            out[c] += p * orc_h2f(u->tail_v[(size_t)t * d + c]);
+    }
+    for (int t = 0; t < u->pool_n; ++t) {
+        double p = score[m++];
+        for (int c = 0; c < d; ++c)
+            out[c] += p * orc_h2f(u->pool_v[(size_t)t * d + c]);
+    }
+    for (int c = 0; c < d; ++c)
+        out[c] /= sum;
+    free(score);
+    free(q);
+    return 0;
+}
+
+/* q: fp16 bits [B][Hq][d]; out: double [B][Hq][d]. */
+int orc_decode(void *hp, const uint16_t *q, double *out)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (h->T < 1)
+        return -2;
+    for (int b = 0; b < h->B; ++b)
+        for (int hq = 0; hq < h->Hq; ++hq) {
+            size_t o = ((size_t)b * h->Hq + hq) * h->d;
+            orc_decode_head(h, b, hq, q + o, out + o);
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Introspection and canonical export.                                       */
+/* ------------------------------------------------------------------------ */
+
+void orc_counts(void *hp, int u, long long *T, int *nf, int *tail, int *npool)
+{
+    orc_cache *h = (orc_cache *)hp;
+    *T = h->T;
+    *nf = h->u[u].nb;
+    *tail = h->u[u].tail_n;
+    *npool = h->u[u].pool_n;
+}
+
+int orc_block_count(void *hp, int u, int j)
+{
+    orc_cache *h = (orc_cache *)hp;
+    return (j >= 0 && j < h->u[u].nb) ? h->u[u].blk[j].c : -1;
+}
+
+/*
+ * Canonical export of unit u. Any pointer may be NULL (skipped). Shapes, with
+ * nf blocks, residual length nt and d channels:
+ *   bcount [nf] int32             block token counts
+ *   bidx   [nf][G] int32          token indices ascending, -1 padded
+ *   kcode  [nf][G][d/4] uint8     packed: code of channel c at bits 2(c%4)
+ *   ks, kz [nf][d] uint16         of byte c/4; padding rows are zero
+ *   vcode  [nf][G][d/4] uint8     same packing
+ *   vs, vz [nf][G][d/32] uint16   zero padded
+ *   tidx   [nt] int32, tk, tv [nt][d] uint16   residual tokens, oldest first
+ *   pidx   [P] int32 ascending (-1 pad), pnorm [P] fp32 bits,
+ *   pk, pv [P][d] uint16          pool tokens in ascending index order
+ */
+int orc_export_unit(void *hp, int ui, int32_t *bcount, int32_t *bidx, uint8_t *kcode,
+                    uint16_t *ks, uint16_t *kz, uint8_t *vcode, uint16_t *vs, uint16_t *vz,
+                    int32_t *tidx, uint16_t *tk, uint16_t *tv, int32_t *pidx,
+                    uint32_t *pnorm, uint16_t *pk, uint16_t *pv)
+{
+    orc_cache *h = (orc_cache *)hp;
+    const orc_unit *u = &h->u[ui];
+    const int d = h->d, G = h->G, P = h->P, ng = d / 32, rb = d / 4;
+    for (int j = 0; j < u->nb; ++j) {
+        const orc_block *bl = &u->blk[j];
+        if (bcount) bcount[j] = bl->c;
+        for (int t = 0; t < G; ++t) {
+            int valid = t < bl->c;
+            if (bidx) bidx[(size_t)j * G + t] = valid ? bl->idx[t] : -1;
+            for (int by = 0; by < rb; ++by) {
+                uint8_t kb = 0, vb = 0;
+                if (valid)
+                    for (int e = 0; e < 4; ++e) {
+                        kb |= (uint8_t)(bl->kcode[(size_t)t * d + 4 * by + e] << (2 * e));
+                        vb |= (uint8_t)(bl->vcode[(size_t)t * d + 4 * by + e] << (2 * e));
+                    }
+                if (kcode) kcode[((size_t)j * G + t) * rb + by] = kb;
+                if (vcode) vcode[((size_t)j * G + t) * rb + by] = vb;
+            }
+            for (int g = 0; g < ng; ++g) {
+                size_t o = ((size_t)j * G + t) * ng + g;
+                if (vs) vs[o] = valid ? bl->vs[(size_t)t * ng + g] : 0;
+                if (vz) vz[o] = valid ? bl->vz[(size_t)t * ng + g] : 0;
+            }
+        }
+        for (int c = 0; c < d; ++c) {
+            if (ks) ks[(size_t)j * d + c] = bl->ks[c];
+            if (kz) kz[(size_t)j * d + c] = bl->kz[c];
+        }
+    }
+    for (int t = 0; t < u->tail_n; ++t) {
+        if (tidx) tidx[t] = u->tail_idx[t];
+        if (tk) memcpy(tk + (size_t)t * d, u->tail_k + (size_t)t * d, (size_t)d * 2);
+        if (tv) memcpy(tv + (size_t)t * d, u->tail_v + (size_t)t * d, (size_t)d * 2);
+    }
+    /* pool in ascending token order */
+    int *ord = (int *)malloc(sizeof(int) * (P + 1));
+    for (int i = 0; i < u->pool_n; ++i)
+        ord[i] = i;
+    for (int i = 1; i < u->pool_n; ++i)          /* insertion sort by index */
+        for (int j = i; j > 0 && u->pool_idx[ord[j - 1]] > u->pool_idx[ord[j]]; --j) {
+            int tmp = ord[j]; ord[j] = ord[j - 1]; ord[j - 1] = tmp;
+        }
+    for (int i = 0; i < P; ++i) {
+        int valid = i < u->pool_n;
+        int s = valid ? ord[i] : 0;
+        if (pidx) pidx[i] = valid ? u->pool_idx[s] : -1;
+        if (pnorm) {
+            uint32_t nb = 0;
+            if (valid) memcpy(&nb, &u->pool_norm[s], 4);
+            pnorm[i] = nb;
+        }
+        if (pk) {
+            if (valid) memcpy(pk + (size_t)i * d, u->pool_k + (size_t)s * d, (size_t)d * 2);
+            else memset(pk + (size_t)i * d, 0, (size_t)d * 2);
+        }
+        if (pv) {
+            if (valid) memcpy(pv + (size_t)i * d, u->pool_v + (size_t)s * d, (size_t)d * 2);
+            else memset(pv + (size_t)i * d, 0, (size_t)d * 2);
+        }
+    }
+    free(ord);
+    return 0;
+}
