@@ -1,0 +1,368 @@
+"""Benchmark: OTT decode-step attention on one GB300 (or N, one process each).
+
+A step is one pass of the whole hot path for one new token of every sequence:
+ott_append (the token enters the fp16 ring; every G tokens the flush packs a
+group into 2-bit blocks) followed by ott_decode_attn (split-K attention over
+blocks, ring and pool, plus the combine). The default workload is the
+Llama-2-7B-shaped layer at batch 32 with a 4096-token prefill, G=128, R=32,
+P=32. `value` is decode tokens/s (batch x steps / time); the JSON line also
+carries the decode kernel's achieved GB/s against the measured HBM peak.
+
+Multi-GPU (torchrun): every rank runs an independent shard of a larger batch
+(weak scaling); no collective touches the data path, only the barrier and
+the max-over-ranks of the timing.
+
+    python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_ott_gb300 import metrics, synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "OTT decode-attn GB/s (% of HBM peak) and decode tokens/s at B=32, 4K ctx"
+DECODE_SRC = os.path.join(ROOT, "bit_kv_cache_ott_gb300", "csrc", "ott_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_src_hash() -> str:
+    with open(DECODE_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per decode launch from a committed ncu capture, if it was
+    taken on the current decode kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("decode_src_sha256_16") != decode_src_hash():
+        return None
+    return t.get("per_launch_bytes", {}).get(workload)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_rate(w, steps: int, warmup: int, units_sample: int):
+    """The CPU oracle (single thread) on a sample of the workload's units:
+    prefill, then `warmup` untimed and `steps` timed decode steps (append +
+    decode of every query head of the sampled units). Returns decode tokens/s
+    scaled to the full workload, and a description of the sample."""
+    from oracle.oracle import OracleCache
+    Bs = max(1, min(w.B, units_sample // w.Hkv))
+    ws = w.with_(B=Bs)
+    orc = OracleCache(ws.B, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P)
+    K, V = synth.prefill_kv(ws)
+    orc.prefill(K, V)
+    del K, V
+    inputs = [synth.step_kvq(ws, s) for s in range(warmup + steps)]
+    for s in range(warmup):
+        k, v, q = inputs[s]
+        orc.append(k, v)
+        orc.decode(q)
+    t0 = time.perf_counter()
+    for s in range(warmup, warmup + steps):
+        k, v, q = inputs[s]
+        orc.append(k, v)
+        orc.decode(q)
+    dt = time.perf_counter() - t0
+    frac = (Bs * ws.Hkv) / (w.B * w.Hkv)
+    per_step_full = dt / steps / frac
+    rate = w.B * w.layers / (per_step_full * w.layers)   # tokens/s (every layer decodes each token)
+    sample = (f"{Bs} of {w.B} sequences ({Bs * w.Hkv} of {w.B * w.Hkv} (sequence, kv head) units), "
+              f"{steps} timed decode steps after {warmup} warm-up, T={w.L}+; one layer; scaled by units")
+    return rate, dt, sample
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    rate, dt, sample = oracle_rate(w, args.steps, args.warmup, args.oracle_units)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.B / rate,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
+                   "G": w.G, "R": w.R, "P": w.P, "layers": w.layers},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w):
+    import bit_kv_cache_ott_gb300 as ott
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ott.load()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    # weak scaling: rank r holds its own shard of B sequences
+    wr = w.with_(seed=w.seed + 7919 * rank) if ws > 1 else w
+    K_steps, W_steps, E_steps = args.steps, args.warmup, args.e2e_steps
+    total_steps = W_steps + K_steps + E_steps
+    caches = []
+    for layer in range(w.layers):
+        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps)
+        K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
+        c.prefill(K, V)
+        del K, V
+        caches.append(c)
+    torch.cuda.synchronize()
+
+    # step inputs (drawn on the host with the CPU generator, staged on the device)
+    n_distinct = min(total_steps, 64)
+    host = [synth.step_kvq(wr, s) for s in range(n_distinct)]
+    dev_in = [tuple(t.to(dev) for t in x) for x in host]
+    stream = torch.cuda.current_stream()
+    out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float16, device=dev)
+
+    def step(s, ev=None):
+        k, v, q = dev_in[s % n_distinct]
+        for c in caches:
+            c.append(k, v, stream)
+            if ev is not None:
+                ev[0].record(stream)
+            c.decode_attn(q, out, stream)
+            if ev is not None:
+                ev[1].record(stream)
+
+    for s in range(W_steps):
+        step(s)
+    torch.cuda.synchronize()
+
+    # timed region: K steps, decode kernels bracketed by events on the same stream
+    launches = 0
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K_steps * w.layers)]
+    dec_bytes = 0
+    flushes = 0
+    T0 = caches[0].counts()[0]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for s in range(K_steps):
+            k, v, q = dev_in[(W_steps + s) % n_distinct]
+            for li, c in enumerate(caches):
+                nf_before = c.counts()[1]
+                c.append(k, v, stream)
+                T, nf_after, _, _ = c.counts()
+                flushes += nf_after - nf_before
+                ev = dec_events[s * w.layers + li]
+                ev[0].record(stream)
+                c.decode_attn(q, out, stream)
+                ev[1].record(stream)
+                dec_bytes += metrics.decode_bytes(T, w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = e0.elapsed_time(e1)
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_events)
+    launches = K_steps * w.layers * 3 + flushes   # append + decode + combine, plus flushes
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    for c in caches:
+        c.check_device()
+
+    tokens = w.B * K_steps * ws
+    value = tokens / (ms * 1e-3)
+    n_launch = K_steps * w.layers
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # k, v, q host->device, append, decode, out device->host
+    e2e = None
+    if E_steps > 0:
+        pin = [tuple(t.pin_memory() for t in x) for x in host]
+        dk = torch.empty_like(dev_in[0][0]); dv = torch.empty_like(dev_in[0][1]); dq = torch.empty_like(dev_in[0][2])
+        out_h = torch.empty(w.B, w.Hq, w.d, dtype=torch.float16).pin_memory()
+        torch.cuda.synchronize()
+        barrier()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for s in range(E_steps):
+            hk, hv, hq = pin[(W_steps + K_steps + s) % n_distinct]
+            dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True); dq.copy_(hq, non_blocking=True)
+            for c in caches:
+                c.append(dk, dv, stream)
+                c.decode_attn(dq, out, stream)
+            out_h.copy_(out, non_blocking=True)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = x0.elapsed_time(x1)
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": w.B * E_steps * ws / (ems * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in pin[0])),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": E_steps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, dt, sample = oracle_rate(w, args.oracle_steps, 1, args.oracle_units)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+
+    if rank == 0:
+        cache_bytes = caches[0].device_bytes() * w.layers
+        fp16_bytes = metrics.fp16_cache_bytes(T0, w.B, w.Hkv, w.d) * w.layers
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K_steps,
+            "warmup": W_steps, "ms_per_step": ms / K_steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16 storage, fp32 accumulation", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
+                       "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
+                       "l2": (f"cache {cache_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"
+                              if cache_bytes > L2_BYTES else "cache fits L2: L2-resident numbers"),
+                       "parallelism": f"weak-scaled shards x{ws}" if ws > 1 else "1 GPU"},
+            "decode_gbs": achieved, "decode_pct_of_hbm_peak": 100.0 * achieved / peak,
+            "decode_us_per_launch": 1e3 * dec_ms / n_launch,
+            "flushes_in_timed_region": flushes,
+            "bytes_per_decoded_token": dec_bytes / (n_launch * w.B) * w.layers,
+            "cache_bytes": cache_bytes, "fp16_cache_bytes": fp16_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
+                         "kernel": "k_decode + k_combine (ott_decode_attn)",
+                         "algorithmic_bytes_per_launch": dec_bytes / n_launch,
+                         "traffic": recorded_traffic(w.name)},
+            "clocks": clk.summary(),
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    for c in caches:
+        c.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--oracle-units", type=int, default=64)
+    ap.add_argument("--oracle-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+"""bit_kv_cache_ott_gb300 -- Outlier Tokens Tracing (OTT) KV-cache quantization
+on one GB300 GPU.
+
+A thin ctypes binding over ``libott.so`` (C ABI in ``include/ott.h``): it only
+marshals torch tensors into device pointers and streams. Every step of the
+path (append, flush, prefill, decode attention) runs in the library's CUDA
+kernels. There is no CPU fallback: if the library is missing or cannot load,
+``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import synth  # noqa: F401  (seeded workloads)
+
+__all__ = ["OTTCache", "OTTError", "load", "status_str", "lib_path"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libott.so")
+_lib = None
+
+OTT_OK, OTT_ERR_INVALID, OTT_ERR_STATE, OTT_ERR_CAPACITY = 0, -1, -2, -3
+OTT_ERR_OOM, OTT_ERR_CUDA, OTT_ERR_DEVICE = -4, -5, -6
+
+
+class OTTError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_str(code)} ({code})")
+        self.code = code
+
+
+class StateExport(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in
+                ("bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tk", "tv", "pidx", "pnorm", "pk", "pv")]
+
+
+SYMBOLS = ("ott_create", "ott_destroy", "ott_prefill", "ott_append", "ott_decode_attn",
+           "ott_get_counts", "ott_block_count", "ott_export_state", "ott_check_device",
+           "ott_device_bytes", "ott_status_str")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libott.so (raises if it is absent or broken)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        if not build_if_missing:
+            raise RuntimeError(f"libott.so not built ({_LIB_PATH}); run __graft_entry__.build()")
+        from .build import build
+        build()
+    L = C.CDLL(_LIB_PATH)
+    P, i32, i64 = C.c_void_p, C.c_int, C.c_longlong
+    L.ott_create.argtypes = [i32] * 8 + [C.POINTER(P)]
+    L.ott_destroy.argtypes = [P]
+    L.ott_prefill.argtypes = [P, P, P, i32, P]
+    L.ott_append.argtypes = [P, P, P, P]
+    L.ott_decode_attn.argtypes = [P, P, P, P]
+    L.ott_get_counts.argtypes = [P, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
+    L.ott_block_count.argtypes = [P, i32]
+    L.ott_export_state.argtypes = [P, i32, i32, C.POINTER(StateExport)]
+    L.ott_check_device.argtypes = [P]
+    L.ott_device_bytes.argtypes = [P]
+    L.ott_device_bytes.restype = i64
+    L.ott_status_str.argtypes = [i32]
+    L.ott_status_str.restype = C.c_char_p
+    _lib = L
+    return L
+
+
+def status_str(code: int) -> str:
+    return load().ott_status_str(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OTT_OK:
+        raise OTTError(rc, what)
+
+
+def _dev_ptr(t: torch.Tensor, shape, name) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float16:
+        raise TypeError(f"{name}: expected a CUDA float16 tensor")
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class OTTCache:
+    """One OTT cache (one attention layer): ``create/prefill/append/decode_attn/destroy``."""
+
+    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192):
+        L = load()
+        self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
+        self.max_tokens = max_tokens
+        h = C.c_void_p()
+        _check(L.ott_create(B, Hq, Hkv, d, G, R, P, max_tokens, C.byref(h)), "ott_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            load().ott_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    def prefill(self, K: torch.Tensor, V: torch.Tensor, stream=None):
+        Lq = K.shape[2] if K.dim() == 4 else -1
+        shp = (self.B, self.Hkv, Lq, self.d)
+        _check(load().ott_prefill(self._h, _dev_ptr(K, shp, "K"), _dev_ptr(V, shp, "V"), Lq,
+                                  _stream(stream)), "ott_prefill")
+
+    def append(self, k: torch.Tensor, v: torch.Tensor, stream=None):
+        shp = (self.B, self.Hkv, self.d)
+        _check(load().ott_append(self._h, _dev_ptr(k, shp, "k"), _dev_ptr(v, shp, "v"),
+                                 _stream(stream)), "ott_append")
+
+    def decode_attn(self, q: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        shp = (self.B, self.Hq, self.d)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float16, device=q.device)
+        _check(load().ott_decode_attn(self._h, _dev_ptr(q, shp, "q"), _dev_ptr(out, shp, "out"),
+                                      _stream(stream)), "ott_decode_attn")
+        return out
+
+    def counts(self):
+        T, nf, tail, npool = C.c_longlong(), C.c_int(), C.c_int(), C.c_int()
+        _check(load().ott_get_counts(self._h, C.byref(T), C.byref(nf), C.byref(tail), C.byref(npool)),
+               "ott_get_counts")
+        return T.value, nf.value, tail.value, npool.value
+
+    def block_count(self, j: int) -> int:
+        rc = load().ott_block_count(self._h, j)
+        if rc < 0:
+            raise OTTError(rc, "ott_block_count")
+        return rc
+
+    def device_bytes(self) -> int:
+        return int(load().ott_device_bytes(self._h))
+
+    def check_device(self):
+        _check(load().ott_check_device(self._h), "ott_check_device")
+
+    def export_state(self, u0: int = 0, nu: int | None = None) -> dict:
+        """Canonical host arrays of units [u0, u0+nu) (numpy)."""
+        import numpy as np
+        nu = self.B * self.Hkv - u0 if nu is None else nu
+        T, nf, nt, npool = self.counts()
+        G, P, d = self.G, self.P, self.d
+        e = dict(
+            bidx=np.zeros((nu, nf, G), np.int32),
+            kcode=np.zeros((nu, nf, G, d // 4), np.uint8),
+            ks=np.zeros((nu, nf, d), np.uint16), kz=np.zeros((nu, nf, d), np.uint16),
+            vcode=np.zeros((nu, nf, G, d // 4), np.uint8),
+            vs=np.zeros((nu, nf, G, d // 32), np.uint16), vz=np.zeros((nu, nf, G, d // 32), np.uint16),
+            tk=np.zeros((nu, nt, d), np.uint16), tv=np.zeros((nu, nt, d), np.uint16),
+            pidx=np.zeros((nu, P), np.int32), pnorm=np.zeros((nu, P), np.uint32),
+            pk=np.zeros((nu, P, d), np.uint16), pv=np.zeros((nu, P, d), np.uint16),
+        )
+        st = StateExport(**{k: (v.ctypes.data if v.size else None) for k, v in e.items()})
+        _check(load().ott_export_state(self._h, u0, nu, C.byref(st)), "ott_export_state")
+        e["bcount"] = np.array([self.block_count(j) for j in range(nf)], np.int32)
+        e.update(T=T, nf=nf, tail=nt, npool=npool)
+        return e

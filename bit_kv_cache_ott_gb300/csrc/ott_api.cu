@@ -1,0 +1,324 @@
+// ott_api.cu -- the C ABI: argument and state checks, device memory, the
+// host-side mirror of the counts (T, nf) and the flush schedule.
+//
+// The host knows T for every call, so whether an append triggers a flush
+// ("every G tokens", zijie-tian.site sec. 3.1; the R newest tokens stay fp16,
+// sec. 3.3) is decided here, with no device round trip on the decode path.
+#include <algorithm>
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ott_internal.cuh"
+
+using namespace ott;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fail_cuda(ott_cache *c, cudaError_t e) {
+    if (e == cudaSuccess) return OTT_OK;
+    if (c) c->poisoned = 1;
+    return OTT_ERR_CUDA;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Flush needed after T tokens with nf flushes done?
+bool flush_due(const ott_cache *c) { return c->T - (long long)c->nf * c->G >= (long long)c->G + c->R; }
+
+}  // namespace
+
+extern "C" {
+
+const char *ott_status_str(int code) {
+    switch (code) {
+        case OTT_OK: return "ok";
+        case OTT_ERR_INVALID: return "invalid argument";
+        case OTT_ERR_STATE: return "call not allowed in the current cache state";
+        case OTT_ERR_CAPACITY: return "capacity (max_tokens) exceeded";
+        case OTT_ERR_OOM: return "device allocation failed";
+        case OTT_ERR_CUDA: return "CUDA error (handle poisoned)";
+        case OTT_ERR_DEVICE: return "a kernel timed out on a bounded wait";
+        default: return "unknown status";
+    }
+}
+
+int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
+    if (!out) return OTT_ERR_INVALID;
+    *out = nullptr;
+    if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
+        return OTT_ERR_INVALID;
+    const int gq = Hq / Hkv;
+    if (!decode_supported(d, gq)) return OTT_ERR_INVALID;
+    if ((long long)B * Hkv > INT_MAX / 64 || (long long)G + R + P > (1 << 20)) return OTT_ERR_INVALID;
+
+    int dev = 0, sms = 0, smem_optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return OTT_ERR_CUDA;
+    const int fsmem = flush_smem_bytes(d, G, P);
+    if (fsmem > smem_optin || decode_smem_bytes(d, gq) > smem_optin) return OTT_ERR_INVALID;
+
+    ott_cache *c = new (std::nothrow) ott_cache();
+    if (!c) return OTT_ERR_OOM;
+    c->B = B; c->Hq = Hq; c->Hkv = Hkv; c->d = d; c->G = G; c->R = R; c->P = P;
+    c->max_tokens = max_tokens;
+    c->U = B * Hkv;
+    c->gq = gq;
+    c->ring = G + R;
+    c->NB = max_tokens >= G + R ? (max_tokens - R) / G : 0;
+    c->ntile = ntiles_of(G);
+    c->blk_bytes = block_bytes_of(d, G);
+    c->device = dev;
+    c->sm_count = sms;
+    c->flush_smem = fsmem;
+    // split capacity per unit: one split per block plus the fp16 chunks
+    c->su_max = c->NB + (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + 1;
+
+    const size_t U = (size_t)c->U;
+    const size_t sz_blk = U * c->NB * (size_t)c->blk_bytes;
+    const size_t sz_bidx = U * c->NB * (size_t)G * 4;
+    const size_t sz_ring = U * c->ring * (size_t)d * 2;
+    const size_t sz_pool = U * (size_t)P * d * 2;
+    const size_t sz_pn = U * (size_t)P * 4;
+    const size_t sz_part = U * (size_t)c->su_max * gq * (d + 2) * 4;
+    size_t off = 0;
+    const size_t o_blk = off; off = round_up(off + sz_blk, 256);
+    const size_t o_bidx = off; off = round_up(off + sz_bidx, 256);
+    const size_t o_rk = off; off = round_up(off + sz_ring, 256);
+    const size_t o_rv = off; off = round_up(off + sz_ring, 256);
+    const size_t o_pk = off; off = round_up(off + sz_pool, 256);
+    const size_t o_pv = off; off = round_up(off + sz_pool, 256);
+    const size_t o_pn = off; off = round_up(off + sz_pn, 256);
+    const size_t o_pi = off; off = round_up(off + sz_pn, 256);
+    const size_t o_part = off; off = round_up(off + sz_part, 256);
+    const size_t o_ctl = off; off = round_up(off + 64, 256);
+    c->mem_bytes = off;
+
+    // Host-side fault injection for tests: OTT_FAULT=alloc makes the device
+    // allocation report failure (exercises the cleanup path without a GPU fault).
+    const char *fault = std::getenv("OTT_FAULT");
+    if (fault && std::strcmp(fault, "alloc") == 0) {
+        delete c;
+        return OTT_ERR_OOM;
+    }
+    void *mem = nullptr;
+    e = cudaMalloc(&mem, c->mem_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return OTT_ERR_OOM;
+    }
+    c->mem = mem;
+    uint8_t *base = static_cast<uint8_t *>(mem);
+    c->blk = base + o_blk;
+    c->bidx = reinterpret_cast<int32_t *>(base + o_bidx);
+    c->rk = reinterpret_cast<__half *>(base + o_rk);
+    c->rv = reinterpret_cast<__half *>(base + o_rv);
+    c->pk = reinterpret_cast<__half *>(base + o_pk);
+    c->pv = reinterpret_cast<__half *>(base + o_pv);
+    c->pnorm = reinterpret_cast<float *>(base + o_pn);
+    c->pidx = reinterpret_cast<int32_t *>(base + o_pi);
+    c->part = reinterpret_cast<float *>(base + o_part);
+    c->ctl = reinterpret_cast<int *>(base + o_ctl);
+    e = cudaMemset(mem, 0, c->mem_bytes);
+    if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(mem);
+        delete c;
+        return OTT_ERR_CUDA;
+    }
+    *out = c;
+    return OTT_OK;
+}
+
+int ott_destroy(ott_cache *c) {
+    if (!c) return OTT_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (c->mem) {
+        cudaError_t e2 = cudaFree(c->mem);
+        if (e == cudaSuccess) e = e2;
+    }
+    delete c;
+    return e == cudaSuccess ? OTT_OK : OTT_ERR_CUDA;
+}
+
+int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || c->T != 0) return OTT_ERR_STATE;
+    if (L < 0) return OTT_ERR_INVALID;
+    if (L > c->max_tokens) return OTT_ERR_CAPACITY;
+    if (L == 0) return OTT_OK;
+    if (!K || !V || !aligned16(K) || !aligned16(V)) return OTT_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
+    const int nf = L >= c->G + c->R ? (L - c->R) / c->G : 0;
+    for (int j = 0; j < nf; ++j) {
+        cudaError_t e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
+    cudaError_t e = launch_copy_tail(c, Kh, Vh, L, (long long)nf * c->G, s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    c->T = L;
+    c->nf = nf;
+    return OTT_OK;
+}
+
+int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned) return OTT_ERR_STATE;
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
+    if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_append(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    c->T += 1;
+    if (flush_due(c)) {
+        e = launch_flush(c, c->rk, c->rv, (long long)c->ring * c->d, c->ring, (long long)c->nf * c->G, c->nf, s);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+        c->nf += 1;
+    }
+    return OTT_OK;
+}
+
+int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || c->T < 1) return OTT_ERR_STATE;
+    if (!q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
+    cudaError_t e = launch_decode(c, static_cast<const __half *>(q), static_cast<__half *>(out),
+                                  static_cast<cudaStream_t>(stream));
+    return fail_cuda(c, e);
+}
+
+int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_pool) {
+    if (!c) return OTT_ERR_INVALID;
+    if (T) *T = c->T;
+    if (nf) *nf = c->nf;
+    if (tail) *tail = (int)(c->T - (long long)c->nf * c->G);
+    if (n_pool) *n_pool = pool_after(c->P, c->G, c->nf);
+    return OTT_OK;
+}
+
+int ott_block_count(const ott_cache *c, int j) {
+    if (!c || j < 0 || j >= c->nf) return OTT_ERR_INVALID;
+    return block_count(c->P, c->G, j);
+}
+
+long long ott_device_bytes(const ott_cache *c) { return c ? (long long)c->mem_bytes : 0; }
+
+int ott_check_device(ott_cache *c) {
+    if (!c) return OTT_ERR_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    int flag = 0;
+    e = cudaMemcpy(&flag, c->ctl + 1, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    return flag ? OTT_ERR_DEVICE : OTT_OK;
+}
+
+int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst) {
+    if (!c || !dst) return OTT_ERR_INVALID;
+    if (c->poisoned) return OTT_ERR_STATE;
+    if (u0 < 0 || nu < 0 || u0 + nu > c->U) return OTT_ERR_INVALID;
+    if (nu == 0) return OTT_OK;
+    const int d = c->d, G = c->G, P = c->P, nf = c->nf;
+    const int nt = (int)(c->T - (long long)nf * G);
+    const int np = pool_after(P, G, nf);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(c, e);
+
+    // blocks: canonical codes and scales through a staging buffer
+    if (nf > 0 && (dst->kcode || dst->vcode || dst->ks || dst->kz || dst->vs || dst->vz)) {
+        const size_t sb = export_stage_bytes(c, nu);
+        uint8_t *stage = nullptr;
+        e = cudaMalloc(&stage, sb);
+        if (e != cudaSuccess) { cudaGetLastError(); return OTT_ERR_OOM; }
+        e = launch_export(c, u0, nu, stage, 0);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        const size_t nblk = (size_t)nu * nf;
+        const size_t n_code = nblk * G * (d / 4), n_ksz = nblk * d, n_vsz = nblk * G * (d / 32);
+        uint8_t *p = stage;
+        if (e == cudaSuccess && dst->kcode) e = cudaMemcpy(dst->kcode, p, n_code, cudaMemcpyDeviceToHost);
+        p += n_code;
+        if (e == cudaSuccess && dst->vcode) e = cudaMemcpy(dst->vcode, p, n_code, cudaMemcpyDeviceToHost);
+        p += n_code;
+        if (e == cudaSuccess && dst->ks) e = cudaMemcpy(dst->ks, p, n_ksz * 2, cudaMemcpyDeviceToHost);
+        p += n_ksz * 2;
+        if (e == cudaSuccess && dst->kz) e = cudaMemcpy(dst->kz, p, n_ksz * 2, cudaMemcpyDeviceToHost);
+        p += n_ksz * 2;
+        if (e == cudaSuccess && dst->vs) e = cudaMemcpy(dst->vs, p, n_vsz * 2, cudaMemcpyDeviceToHost);
+        p += n_vsz * 2;
+        if (e == cudaSuccess && dst->vz) e = cudaMemcpy(dst->vz, p, n_vsz * 2, cudaMemcpyDeviceToHost);
+        cudaError_t e2 = cudaFree(stage);
+        if (e == cudaSuccess) e = e2;
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
+    if (nf > 0 && dst->bidx) {
+        for (int uu = 0; uu < nu; ++uu) {
+            e = cudaMemcpy(dst->bidx + (size_t)uu * nf * G, c->bidx + (size_t)(u0 + uu) * c->NB * G,
+                           (size_t)nf * G * 4, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return fail_cuda(c, e);
+        }
+    }
+    // residual tokens nf*G .. T-1, oldest first
+    if (nt > 0 && (dst->tk || dst->tv)) {
+        std::vector<uint16_t> rk((size_t)nu * c->ring * d), rv(rk.size());
+        e = cudaMemcpy(rk.data(), c->rk + (size_t)u0 * c->ring * d, rk.size() * 2, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(rv.data(), c->rv + (size_t)u0 * c->ring * d, rv.size() * 2, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+        for (int uu = 0; uu < nu; ++uu)
+            for (int x = 0; x < nt; ++x) {
+                const long long t = (long long)nf * G + x;
+                const size_t src = ((size_t)uu * c->ring + (size_t)(t % c->ring)) * d;
+                const size_t o = ((size_t)uu * nt + x) * d;
+                if (dst->tk) std::memcpy(dst->tk + o, rk.data() + src, (size_t)d * 2);
+                if (dst->tv) std::memcpy(dst->tv + o, rv.data() + src, (size_t)d * 2);
+            }
+    }
+    // pool in ascending token order
+    if (P > 0 && (dst->pidx || dst->pnorm || dst->pk || dst->pv)) {
+        const size_t n = (size_t)nu * P;
+        std::vector<int32_t> pi(n);
+        std::vector<float> pn(n);
+        std::vector<uint16_t> pk(n * d), pv(n * d);
+        e = cudaMemcpy(pi.data(), c->pidx + (size_t)u0 * P, n * 4, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(pn.data(), c->pnorm + (size_t)u0 * P, n * 4, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(pk.data(), c->pk + (size_t)u0 * P * d, n * d * 2, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(pv.data(), c->pv + (size_t)u0 * P * d, n * d * 2, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+        std::vector<int> ord(P);
+        for (int uu = 0; uu < nu; ++uu) {
+            for (int x = 0; x < np; ++x) ord[x] = x;
+            const int32_t *ip = pi.data() + (size_t)uu * P;
+            std::sort(ord.begin(), ord.begin() + np, [&](int a, int b) { return ip[a] < ip[b]; });
+            for (int x = 0; x < P; ++x) {
+                const bool valid = x < np;
+                const size_t so = (size_t)uu * P + (valid ? ord[x] : 0), o = (size_t)uu * P + x;
+                if (dst->pidx) dst->pidx[o] = valid ? pi[so] : -1;
+                if (dst->pnorm) {
+                    uint32_t bits = 0;
+                    if (valid) std::memcpy(&bits, &pn[so], 4);
+                    dst->pnorm[o] = bits;
+                }
+                if (dst->pk) {
+                    if (valid) std::memcpy(dst->pk + o * d, pk.data() + so * d, (size_t)d * 2);
+                    else std::memset(dst->pk + o * d, 0, (size_t)d * 2);
+                }
+                if (dst->pv) {
+                    if (valid) std::memcpy(dst->pv + o * d, pv.data() + so * d, (size_t)d * 2);
+                    else std::memset(dst->pv + o * d, 0, (size_t)d * 2);
+                }
+            }
+        }
+    }
+    return OTT_OK;
+}
+
+}  // extern "C"

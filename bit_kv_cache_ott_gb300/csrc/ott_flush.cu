@@ -1,0 +1,416 @@
+// ott_flush.cu -- append, flush (norm, top-P pool merge, 2-bit quantization,
+// packing), prefill tail copy and the canonical state export.
+//
+// The flush follows "Accurate KV Cache Quantization with Outlier Tokens
+// Tracing": zijie-tian.site sec. 3.1 (every G tokens the oldest group is
+// quantized; candidates are ranked by the key norm) and sec. 3.2 (an outlier
+// pool of capacity P; new tokens compete with the pool; a displaced token is
+// written back to the quantized cache); sciencestack.ai Abstract (keys per
+// channel, values per token) and Fig. 1(c) (keep the smallest-magnitude keys).
+//
+// One CTA per unit (sequence, kv head). The candidates (pool + group) are
+// staged in shared memory; the squared norm of each group key is summed in
+// fp32 in channel order; every candidate's rank under (norm, token index) is
+// counted; the P best stay (pool slot = rank), the rest form the block in
+// ascending token order. Keys are quantized per channel, values per token per
+// 32 channels, with IEEE fp32 steps (__fsub_rn/__fdiv_rn, round-half-even
+// __float2int_rn) and fp16 round-to-nearest for scale and zero.
+#include "ott_internal.cuh"
+
+namespace ott {
+namespace {
+
+constexpr int FLUSH_THREADS = 256;
+
+// a < b with -0 ordered below +0 (makes min/max independent of order)
+__device__ __forceinline__ bool below(float a, float b) {
+    return a < b || (a == b && signbit(a) && !signbit(b));
+}
+
+__device__ __forceinline__ uint32_t qcode(float x, float s, float z) {
+    if (s == 0.0f) return 0u;
+    int q = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
+    return (uint32_t)min(max(q, 0), 3);
+}
+
+__device__ __forceinline__ uint32_t half2_bits(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+struct FlushArgs {
+    uint8_t *blk;
+    int32_t *bidx;
+    __half *pk, *pv;
+    float *pnorm;
+    int32_t *pidx;
+    const __half *srcK, *srcV;
+    long long src_unit_stride;   // elements between units in the source
+    long long src_mod;           // slot = token mod src_mod
+    long long t0;                // first token of the group
+    long long blk_bytes;
+    int G, P, NB, ntile, j, np0;
+};
+
+template <int D>
+__global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int RS = D + 8;          // padded row stride (halves): 16B-aligned rows
+    constexpr int VPR = D / 8;         // 16-byte vectors per row
+    constexpr int NG = D / 32;         // value groups
+    constexpr int NKT = D / 16;
+    constexpr int NW = D / 32;
+    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
+    const int G = a.G, P = a.P, np0 = a.np0, nc = np0 + G;
+
+    __half *ck = reinterpret_cast<__half *>(smem);
+    __half *cv = ck + (size_t)nc * RS;
+    uint64_t *key = reinterpret_cast<uint64_t *>(cv + (size_t)nc * RS);
+    int *rank = reinterpret_cast<int *>(key + nc);
+    int *bmap = rank + nc;
+    float *ks = reinterpret_cast<float *>(bmap + G);
+    float *kz = ks + D;
+    float *vs = kz + D;
+    float *vz = vs + G * NG;
+
+    // 1. stage the candidates: old pool rows, then the group's rows
+    for (int e = tid; e < nc * VPR; e += nth) {
+        const int row = e / VPR, v8 = e % VPR;
+        const __half *sk, *sv;
+        if (row < np0) {
+            const size_t off = ((size_t)u * P + row) * D;
+            sk = a.pk + off;
+            sv = a.pv + off;
+        } else {
+            const long long t = a.t0 + (row - np0);
+            const size_t off = (size_t)u * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
+            sk = a.srcK + off;
+            sv = a.srcV + off;
+        }
+        reinterpret_cast<uint4 *>(ck + (size_t)row * RS)[v8] = reinterpret_cast<const uint4 *>(sk)[v8];
+        reinterpret_cast<uint4 *>(cv + (size_t)row * RS)[v8] = reinterpret_cast<const uint4 *>(sv)[v8];
+    }
+    __syncthreads();
+
+    // 2. keys: (fp32 squared norm bits, token index); norms >= +0 order as bits
+    for (int row = tid; row < nc; row += nth) {
+        float nrm;
+        int idx;
+        if (row < np0) {
+            nrm = a.pnorm[(size_t)u * P + row];
+            idx = a.pidx[(size_t)u * P + row];
+        } else {
+            const __half *kr = ck + (size_t)row * RS;
+            float s = 0.0f;
+            for (int ch = 0; ch < D; ++ch) {
+                const float x = __half2float(kr[ch]);
+                s = __fadd_rn(s, __fmul_rn(x, x));
+            }
+            nrm = s;
+            idx = (int)(a.t0 + (row - np0));
+        }
+        key[row] = ((uint64_t)__float_as_uint(nrm) << 32) | (uint32_t)idx;
+    }
+    __syncthreads();
+
+    // 3. rank of every candidate under (norm, index); keys are distinct
+    for (int r = tid; r < nc; r += nth) {
+        const uint64_t kr = key[r];
+        int rk = 0;
+        for (int q = 0; q < nc; ++q) rk += key[q] < kr;
+        rank[r] = rk;
+    }
+    __syncthreads();
+    const int keep = min(P, nc), cnt = nc - keep;
+
+    // 4. block slot of every leaving candidate: rank by token index
+    for (int r = tid; r < nc; r += nth) {
+        if (rank[r] >= keep) {
+            const uint32_t ir = (uint32_t)key[r];
+            int pos = 0;
+            for (int q = 0; q < nc; ++q) pos += (rank[q] >= keep) && ((uint32_t)key[q] < ir);
+            bmap[pos] = r;
+        }
+    }
+    // 5. the new pool (old pool rows are already staged in shared memory)
+    for (int e = tid; e < nc * VPR; e += nth) {
+        const int row = e / VPR, v8 = e % VPR, rk = rank[row];
+        if (rk < keep) {
+            const size_t off = ((size_t)u * P + rk) * D;
+            reinterpret_cast<uint4 *>(a.pk + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[v8];
+            reinterpret_cast<uint4 *>(a.pv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[v8];
+        }
+    }
+    for (int row = tid; row < nc; row += nth) {
+        const int rk = rank[row];
+        if (rk < keep) {
+            a.pnorm[(size_t)u * P + rk] = __uint_as_float((uint32_t)(key[row] >> 32));
+            a.pidx[(size_t)u * P + rk] = (int32_t)(uint32_t)key[row];
+        }
+    }
+    __syncthreads();
+
+    uint8_t *bb = a.blk + ((size_t)u * a.NB + a.j) * a.blk_bytes;
+    uint8_t *tiles = bb + ksz_bytes(D);
+    for (int t = tid; t < G; t += nth)
+        a.bidx[((size_t)u * a.NB + a.j) * G + t] = t < cnt ? (int32_t)(uint32_t)key[bmap[t]] : -1;
+
+    // 6. keys: one (scale, zero) per channel over the block's tokens
+    for (int ch = tid; ch < D; ch += nth) {
+        __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
+        if (cnt > 0) {
+            float mn = __half2float(ck[(size_t)bmap[0] * RS + ch]), mx = mn;
+            for (int t = 1; t < cnt; ++t) {
+                const float v = __half2float(ck[(size_t)bmap[t] * RS + ch]);
+                if (below(v, mn)) mn = v;
+                if (below(mx, v)) mx = v;
+            }
+            s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            z16 = __float2half_rn(mn);
+        }
+        ks[ch] = __half2float(s16);
+        kz[ch] = __half2float(z16);
+        reinterpret_cast<uint32_t *>(bb)[ch] = half2_bits(s16, z16);
+    }
+    // 7. values: one (scale, zero) per token per 32 channels
+    for (int e = tid; e < a.ntile * TILE * NG; e += nth) {
+        const int t = e / NG, gm = e % NG;
+        __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
+        if (t < cnt) {
+            const __half *row = cv + (size_t)bmap[t] * RS + 32 * gm;
+            float mn = __half2float(row[0]), mx = mn;
+            for (int k = 1; k < 32; ++k) {
+                const float v = __half2float(row[k]);
+                if (below(v, mn)) mn = v;
+                if (below(mx, v)) mx = v;
+            }
+            s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            z16 = __float2half_rn(mn);
+            vs[t * NG + gm] = __half2float(s16);
+            vz[t * NG + gm] = __half2float(z16);
+        }
+        uint8_t *tb = tiles + (size_t)(t / TILE) * tile_bytes(D) + tile_sz_off(D);
+        reinterpret_cast<uint32_t *>(tb)[vsz_index(t, gm)] = half2_bits(s16, z16);
+    }
+    __syncthreads();
+
+    // 8. pack the codes into the mma.sync word format (see ott_internal.cuh)
+    const int nwords = a.ntile * 32 * NW;
+    for (int e = tid; e < nwords; e += nth) {
+        const int tau = e / (32 * NW), rem = e % (32 * NW), lane = rem / NW, w = rem % NW;
+        const int r = lane >> 2, i = lane & 3, wp = w >> 1, hi = w & 1;
+        uint32_t kw = 0, vw = 0;
+        const int tk = TILE * tau + r + 8 * hi;   // K: token slot of this word
+        const __half *krow = tk < cnt ? ck + (size_t)bmap[tk] * RS : nullptr;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int q = 8 * wp + p;
+            // K word: channels 16kt + 2i + 8o (+1) of token tk
+            const int o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
+            if (krow) {
+                kw |= qcode(__half2float(krow[ch]), ks[ch], kz[ch]) << (2 * p);
+                kw |= qcode(__half2float(krow[ch + 1]), ks[ch + 1], kz[ch + 1]) << (16 + 2 * p);
+            }
+            // V word: channel 16mt + r + 8rowhalf of token slots 16tau + 2i + 8hi (+1)
+            const int rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int tv = TILE * tau + 2 * i + 8 * hi + h;
+                if (tv < cnt) {
+                    const int gi = tv * NG + vch / 32;
+                    vw |= qcode(__half2float(cv[(size_t)bmap[tv] * RS + vch]), vs[gi], vz[gi]) << (16 * h + 2 * p);
+                }
+            }
+        }
+        uint8_t *tb = tiles + (size_t)tau * tile_bytes(D);
+        reinterpret_cast<uint32_t *>(tb + tile_k_off(D))[lane * NW + w] = kw;
+        reinterpret_cast<uint32_t *>(tb + tile_v_off(D))[lane * NW + w] = vw;
+    }
+}
+
+// k, v [U][d] -> ring slot `slot` of every unit
+__global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
+                         __half *rv, int U, int d, int ring, int slot) {
+    const int vpr = d / 8;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
+        const int u = e / vpr, x = e % vpr;
+        const size_t off = ((size_t)u * ring + slot) * d;
+        reinterpret_cast<uint4 *>(rk + off)[x] = k[e];
+        reinterpret_cast<uint4 *>(rv + off)[x] = v[e];
+    }
+}
+
+// tokens [t_begin, L) of K, V [U][L][d] -> their ring slots
+__global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half *rv, int U, int d,
+                            int ring, int L, long long t_begin) {
+    const int vpr = d / 8;
+    const long long ntok = L - t_begin;
+    const long long total = (long long)U * ntok * vpr;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int x = (int)(e % vpr);
+        const long long tt = (e / vpr) % ntok;
+        const int u = (int)(e / vpr / ntok);
+        const long long t = t_begin + tt;
+        const size_t src = ((size_t)u * L + t) * d;
+        const size_t dst = ((size_t)u * ring + (size_t)(t % ring)) * d;
+        reinterpret_cast<uint4 *>(rk + dst)[x] = reinterpret_cast<const uint4 *>(K + src)[x];
+        reinterpret_cast<uint4 *>(rv + dst)[x] = reinterpret_cast<const uint4 *>(V + src)[x];
+    }
+}
+
+// Canonical export of the quantized blocks of units [u0, u0+nu):
+//   kcode/vcode [nu][nf][G][d/4] bytes, ks/kz [nu][nf][d], vs/vz [nu][nf][G][d/32]
+struct ExportArgs {
+    const uint8_t *blk;
+    long long blk_bytes;
+    int NB, nf, G, d, u0, nu;
+    uint8_t *kcode, *vcode;
+    uint16_t *ks, *kz, *vs, *vz;
+};
+
+__global__ void k_export(ExportArgs a) {
+    const int d = a.d, rb = d / 4, NG = d / 32;
+    const long long nblk = (long long)a.nu * a.nf;
+    const long long n_code = nblk * a.G * rb;
+    const long long n_ksz = nblk * d;
+    const long long n_vsz = nblk * a.G * NG;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n_code; e += stride) {
+        const int by = (int)(e % rb);
+        const int t = (int)((e / rb) % a.G);
+        const long long bj = e / rb / a.G;
+        const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
+        const uint8_t *tb = a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes + ksz_bytes(d) +
+                            (size_t)(t / TILE) * tile_bytes(d);
+        const uint32_t *kw = reinterpret_cast<const uint32_t *>(tb + tile_k_off(d));
+        const uint32_t *vw = reinterpret_cast<const uint32_t *>(tb + tile_v_off(d));
+        uint32_t kb = 0, vb = 0;
+        for (int x = 0; x < 4; ++x) {
+            const int ch = 4 * by + x;
+            int w, bit;
+            k_loc(t, ch, d, w, bit);
+            kb |= ((kw[w] >> bit) & 3u) << (2 * x);
+            v_loc(t, ch, d, w, bit);
+            vb |= ((vw[w] >> bit) & 3u) << (2 * x);
+        }
+        a.kcode[e] = (uint8_t)kb;
+        a.vcode[e] = (uint8_t)vb;
+    }
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n_ksz; e += stride) {
+        const int ch = (int)(e % d);
+        const long long bj = e / d;
+        const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
+        const uint32_t sz = reinterpret_cast<const uint32_t *>(
+            a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes)[ch];
+        a.ks[e] = (uint16_t)(sz & 0xffffu);
+        a.kz[e] = (uint16_t)(sz >> 16);
+    }
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n_vsz; e += stride) {
+        const int gm = (int)(e % NG);
+        const int t = (int)((e / NG) % a.G);
+        const long long bj = e / NG / a.G;
+        const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
+        const uint8_t *tb = a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes + ksz_bytes(d) +
+                            (size_t)(t / TILE) * tile_bytes(d);
+        const uint32_t sz = reinterpret_cast<const uint32_t *>(tb + tile_sz_off(d))[vsz_index(t, gm)];
+        a.vs[e] = (uint16_t)(sz & 0xffffu);
+        a.vz[e] = (uint16_t)(sz >> 16);
+    }
+}
+
+}  // namespace
+
+int flush_smem_bytes(int d, int G, int P) {
+    const long long nc = (long long)P + G;
+    const long long b = nc * (d + 8) * 2 * 2   // staged K and V rows
+                        + nc * 8               // keys
+                        + nc * 4 + (long long)G * 4           // ranks, block map
+                        + 2LL * d * 4                         // key scale/zero
+                        + 2LL * ntiles_of(G) * TILE * (d / 32) * 4;  // value scale/zero
+    return b > (1LL << 30) ? (1 << 30) : (int)b;
+}
+
+cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+    const int slot = (int)(c->T % c->ring);
+    const int n = c->U * c->d / 8;
+    const int th = 256, bl = (n + th - 1) / th;
+    k_append<<<bl, th, 0, s>>>(reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
+                               c->rk, c->rv, c->U, c->d, c->ring, slot);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
+                         long long src_unit_stride, long long src_mod, long long t0, int j,
+                         cudaStream_t s) {
+    FlushArgs a;
+    a.blk = c->blk;
+    a.bidx = c->bidx;
+    a.pk = c->pk;
+    a.pv = c->pv;
+    a.pnorm = c->pnorm;
+    a.pidx = c->pidx;
+    a.srcK = srcK;
+    a.srcV = srcV;
+    a.src_unit_stride = src_unit_stride;
+    a.src_mod = src_mod;
+    a.t0 = t0;
+    a.blk_bytes = c->blk_bytes;
+    a.G = c->G;
+    a.P = c->P;
+    a.NB = c->NB;
+    a.ntile = c->ntile;
+    a.j = j;
+    a.np0 = pool_after(c->P, c->G, j);
+    const int smem = flush_smem_bytes(c->d, c->G, c->P);
+    if (c->d == 128)
+        k_flush<128><<<c->U, FLUSH_THREADS, smem, s>>>(a);
+    else
+        k_flush<64><<<c->U, FLUSH_THREADS, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *V, int L,
+                             long long t_begin, cudaStream_t s) {
+    if (t_begin >= L) return cudaSuccess;
+    const long long total = (long long)c->U * (L - t_begin) * (c->d / 8);
+    const int th = 256;
+    const long long bl = (total + th - 1) / th;
+    k_copy_tail<<<(int)(bl < 65535 ? bl : 65535), th, 0, s>>>(K, V, c->rk, c->rv, c->U, c->d, c->ring,
+                                                               L, t_begin);
+    return cudaGetLastError();
+}
+
+size_t export_stage_bytes(const ott_cache *c, int nu) {
+    const size_t nblk = (size_t)nu * c->nf;
+    return nblk * c->G * (c->d / 4) * 2 + nblk * c->d * 2 * 2 + nblk * c->G * (c->d / 32) * 2 * 2 + 64;
+}
+
+cudaError_t launch_export(const ott_cache *c, int u0, int nu, uint8_t *stage, cudaStream_t s) {
+    const size_t nblk = (size_t)nu * c->nf;
+    ExportArgs a;
+    a.blk = c->blk;
+    a.blk_bytes = c->blk_bytes;
+    a.NB = c->NB;
+    a.nf = c->nf;
+    a.G = c->G;
+    a.d = c->d;
+    a.u0 = u0;
+    a.nu = nu;
+    uint8_t *p = stage;
+    a.kcode = p; p += nblk * c->G * (c->d / 4);
+    a.vcode = p; p += nblk * c->G * (c->d / 4);
+    a.ks = reinterpret_cast<uint16_t *>(p); p += nblk * c->d * 2;
+    a.kz = reinterpret_cast<uint16_t *>(p); p += nblk * c->d * 2;
+    a.vs = reinterpret_cast<uint16_t *>(p); p += nblk * c->G * (c->d / 32) * 2;
+    a.vz = reinterpret_cast<uint16_t *>(p);
+    if (nblk == 0) return cudaSuccess;
+    k_export<<<4 * c->sm_count, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t set_flush_attributes(int d, int smem) {
+    if (d == 128) return cudaFuncSetAttribute(k_flush<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return cudaFuncSetAttribute(k_flush<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace ott

@@ -1,0 +1,142 @@
+// ott_internal.cuh -- device layout of the OTT cache and the launcher
+// interface shared by the library's translation units.
+//
+// Packed cache layout (one unit = one (sequence, kv head)):
+//
+//   block j of unit u, at blk + (u*NB + j) * block_bytes:
+//     [0, 4d)                 K scale/zero, half2 (s, z) per channel
+//     then ntile = ceil(G/16) tiles of 16 token slots, 10d bytes each:
+//       [0, 4d)    K codes : 32 lanes x d/32 words, lane-major
+//       [4d, 8d)   V codes : same
+//       [8d, 10d)  V scale/zero half2, index ((gamma*4 + i)*4 + k)
+//   A block holds c_j <= G valid tokens in slots 0..c_j-1 (ascending token
+//   index); padding slots carry code 0 and scale/zero 0.
+//
+// Word format. A 32-bit word carries 16 two-bit codes: eight in the low
+// half at bits 2p (p = 0..7) and eight in the high half at bits 16+2p.
+// Masking position p < 5 leaves the code at bits 2p of each 16-bit half,
+// which as an IEEE fp16 number is the subnormal code * 2^(2p-24); positions
+// p = 5..7 do the same after a right shift by 10 (class p-5). So one AND
+// (plus one shift per word) turns two codes into an exact fp16x2 operand of
+// mma.sync, at a power-of-two "class" scale that the other operand or the
+// epilogue removes. Which (token, channel) sits at (lane, word, p, half) is
+// fixed by the mma.sync m16n8k16 fragment layouts:
+//
+//   K (A operand of the score MMA, rows = tokens, k = channels):
+//     lane = 4r + i, word w = 2*wp + th, slot q = 8*wp + p,
+//     o = q / (d/16), kt = q % (d/16):
+//       token slot 16*tile + r + 8*th, channel 16*kt + 2i + 8o + half
+//   V (A operand of the PV MMA, rows = channels, k = tokens):
+//     lane = 4r + i, word w = 2*wp + tp, slot q = 8*wp + p,
+//     rowhalf = q / (d/16), mt = q % (d/16):
+//       channel 16*mt + r + 8*rowhalf, token slot 16*tile + 2i + 8*tp + half
+//   V scale/zero: (gamma, i, k) holds token slot 16*tile + 2i + (k&1) + 8*(k>>1)
+//
+// Residual ring: rk, rv [U][G+R][d], token t in slot t mod (G+R).
+// Outlier pool:  pk, pv [U][P][d], pnorm [U][P], pidx [U][P], kept sorted by
+// (norm, token index) ascending; n_pool = min(P, nf*G) for every unit.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ott.h"
+
+namespace ott {
+
+constexpr int TILE = 16;          // token slots per tile
+constexpr int CHUNK_TILES = 4;    // tiles per staged chunk in the decode kernel
+constexpr int DEC_WARPS = 16;     // warps per decode CTA
+constexpr int FP16_CHUNK = 32;    // fp16 tokens per decode split (one per lane)
+
+__host__ __device__ constexpr int ksz_bytes(int d) { return 4 * d; }
+__host__ __device__ constexpr int tile_bytes(int d) { return 10 * d; }
+__host__ __device__ constexpr int tile_k_off(int) { return 0; }
+__host__ __device__ constexpr int tile_v_off(int d) { return 4 * d; }
+__host__ __device__ constexpr int tile_sz_off(int d) { return 8 * d; }
+__host__ __device__ constexpr int stage_bytes(int d) { return ksz_bytes(d) + CHUNK_TILES * tile_bytes(d); }
+__host__ __device__ inline int ntiles_of(int G) { return (G + TILE - 1) / TILE; }
+__host__ __device__ inline long long block_bytes_of(int d, int G) {
+    return ksz_bytes(d) + (long long)ntiles_of(G) * tile_bytes(d);
+}
+__host__ __device__ constexpr int cls_of_pos(int p) { return p < 5 ? p : p - 5; }
+
+// Pool size after nf flushes and valid tokens of block j (same for all units).
+__host__ __device__ inline int pool_after(int P, int G, long long nf) {
+    long long x = nf * (long long)G;
+    return (int)(x < P ? x : P);
+}
+__host__ __device__ inline int block_count(int P, int G, int j) {
+    return pool_after(P, G, j) + G - pool_after(P, G, j + 1);
+}
+
+// (token slot t, channel ch) -> (word index lane*(d/32)+w within the tile's
+// K region, bit offset). Inverse of the K mapping above.
+__host__ __device__ inline void k_loc(int t, int ch, int d, int &word, int &bit) {
+    const int nkt = d / 16, nw = d / 32;
+    const int tin = t & 15, r = tin & 7, th = tin >> 3;
+    const int kt = ch >> 4, rem = ch & 15, o = rem >> 3, i = (rem & 7) >> 1, half = rem & 1;
+    const int q = o * nkt + kt, wp = q >> 3, p = q & 7;
+    word = (4 * r + i) * nw + 2 * wp + th;
+    bit = 16 * half + 2 * p;
+}
+
+__host__ __device__ inline void v_loc(int t, int ch, int d, int &word, int &bit) {
+    const int nkt = d / 16, nw = d / 32;
+    const int tin = t & 15, tp = tin >> 3, i = (tin & 7) >> 1, half = tin & 1;
+    const int mt = ch >> 4, rem = ch & 15, rowhalf = rem >> 3, r = rem & 7;
+    const int q = rowhalf * nkt + mt, wp = q >> 3, p = q & 7;
+    word = (4 * r + i) * nw + 2 * wp + tp;
+    bit = 16 * half + 2 * p;
+}
+
+__host__ __device__ inline int vsz_index(int t, int gamma) {
+    const int tin = t & 15, i = (tin & 7) >> 1, k = (tin & 1) + 2 * (tin >> 3);
+    return (gamma * 4 + i) * 4 + k;
+}
+
+}  // namespace ott
+
+struct ott_cache {
+    int B, Hq, Hkv, d, G, R, P, max_tokens;
+    int U, gq, ring, NB, ntile;
+    long long blk_bytes;
+    long long T;
+    int nf;
+    int poisoned;
+    int device;
+    int sm_count;
+    int flush_smem;
+    int su_max;             // split capacity per unit
+    // device memory (one allocation)
+    void *mem;
+    size_t mem_bytes;
+    uint8_t *blk;           // [U][NB][blk_bytes]
+    int32_t *bidx;          // [U][NB][G]
+    __half *rk, *rv;        // [U][ring][d]
+    __half *pk, *pv;        // [U][P][d]
+    float *pnorm;           // [U][P]
+    int32_t *pidx;          // [U][P]
+    float *part;            // [U][su_max][gq][d+2] split-K partials
+    int *ctl;               // [0] split counter, [1] status flag
+};
+
+namespace ott {
+
+cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s);
+cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
+                         long long src_unit_stride, long long src_mod, long long t0, int j,
+                         cudaStream_t s);
+cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *V, int L,
+                             long long t_begin, cudaStream_t s);
+cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
+cudaError_t launch_export(const ott_cache *c, int u0, int nu, uint8_t *stage, cudaStream_t s);
+size_t export_stage_bytes(const ott_cache *c, int nu);
+int flush_smem_bytes(int d, int G, int P);
+int decode_smem_bytes(int d, int gq);
+cudaError_t set_kernel_attributes(int d, int gq, int smem_max);
+cudaError_t set_flush_attributes(int d, int smem);
+bool decode_supported(int d, int gq);
+
+}  // namespace ott

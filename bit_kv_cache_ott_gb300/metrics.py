@@ -1,0 +1,47 @@
+"""Counting rules for the measurements (no timing here).
+
+Algorithmic bytes of one decode-attention call, per (sequence, kv head),
+counting only what the method must read or write once:
+
+    K codes   n_q * d/4          V codes   n_q * d/4
+    K scale/zero  (non-empty blocks) * d * 4
+    V scale/zero  n_q * (d/32) * 4
+    fp16 residual + pool tokens   (tail + n_pool) * d * 4   (K and V)
+    queries in and outputs out    g * d * 4
+
+with n_q = nf*G - n_pool quantized tokens. Padding slots, split-K partials,
+token indices, norms and block counts are not credited. At d = 128 this is
+84 bytes per quantized token and 512 bytes per fp16 token.
+"""
+from __future__ import annotations
+
+
+def flush_count(T: int, G: int, R: int) -> int:
+    return (T - R) // G if T >= G + R else 0
+
+
+def pool_size(T: int, G: int, R: int, P: int) -> int:
+    return min(P, flush_count(T, G, R) * G)
+
+
+def block_count(j: int, G: int, P: int) -> int:
+    return min(P, j * G) + G - min(P, (j + 1) * G)
+
+
+def decode_bytes_per_unit(T: int, d: int, g: int, G: int, R: int, P: int) -> int:
+    nf = flush_count(T, G, R)
+    npool = pool_size(T, G, R, P)
+    nq = nf * G - npool
+    tail = T - nf * G
+    nonempty = sum(1 for j in range(nf) if block_count(j, G, P) > 0)
+    return (2 * nq * d // 4 + nonempty * d * 4 + nq * (d // 32) * 4
+            + (tail + npool) * d * 4 + g * d * 4)
+
+
+def decode_bytes(T: int, B: int, Hq: int, Hkv: int, d: int, G: int, R: int, P: int) -> int:
+    return B * Hkv * decode_bytes_per_unit(T, d, Hq // Hkv, G, R, P)
+
+
+def fp16_cache_bytes(T: int, B: int, Hkv: int, d: int) -> int:
+    """The same cache held entirely in fp16 (K and V)."""
+    return B * Hkv * T * d * 4

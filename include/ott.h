@@ -1,0 +1,164 @@
+/*
+ * ott.h -- C ABI of libott: Outlier Tokens Tracing (OTT) KV-cache
+ * quantization on one GB300 (sm_103a): the every-G flush that packs tokens
+ * into 2-bit blocks, and the decode-step attention over the three stores.
+ *
+ * The method: "Accurate KV Cache Quantization with Outlier Tokens Tracing".
+ *   zijie-tian.site, sec. 3.1 -- every G tokens the latest group is
+ *       quantized to 2 bits; candidates are scored by the key norm.
+ *   zijie-tian.site, sec. 3.2 -- an outlier pool of capacity P keeps
+ *       full-precision K/V; new tokens compete with pool tokens and a
+ *       displaced token is written back to the quantized cache.
+ *   zijie-tian.site, sec. 3.3 and flowchart -- decoding multiplies the query
+ *       by quantized, residual-window (latest R tokens, fp16) and outlier
+ *       keys, softmaxes the concatenated scores and sums the matching values.
+ *   sciencestack.ai (arXiv 2505.10938), TL;DR and Abstract -- three KV
+ *       caches; keys quantized per channel, values per token; Fig. 1(c) --
+ *       keep the tokens whose keys have the smallest magnitude; Fig. 2 --
+ *       the decoding and quantization stages.
+ *
+ * Exact rules this library implements (and the CPU oracle in the test suite
+ * implements independently):
+ *   - A flush runs when G+R tokens wait unquantized; it takes the G oldest.
+ *   - Outlier score: squared L2 norm of the fp16 key, fp32, summed in channel
+ *     order. Candidates = pool + group; the P smallest (norm, token index)
+ *     stay in the pool (ties to the lower index); all others form the new
+ *     block in ascending token order (a block is made at every flush).
+ *   - Keys: one fp16 (scale, zero) per channel over the block's tokens.
+ *     Values: one fp16 (scale, zero) per token per 32 channels.
+ *     mn/mx in fp32 (-0 below +0); s = fp16_rn((mx-mn)/3); z = mn;
+ *     code = 0 if s == 0, else clamp(rint((x-z)/s), 0, 3), IEEE fp32 ops.
+ *   - Decode attends to every token seen, scale 1/sqrt(d); query head h
+ *     reads kv head h / (Hq/Hkv). Output fp16 (round to nearest).
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses of fp16 data (IEEE binary16),
+ *     contiguous, 16-byte aligned. The caller owns them and keeps them alive
+ *     until the work queued on `stream` completes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream). All
+ *     work is queued on it; no call synchronizes except ott_export_state and
+ *     ott_check_device.
+ *   - Arguments and state are checked before anything is queued: a call that
+ *     returns an error other than OTT_ERR_CUDA leaves the cache unchanged.
+ *     A CUDA error poisons the handle: later calls return OTT_ERR_STATE.
+ *   - A handle is not thread-safe. Distinct handles are independent.
+ *   - Every sequence of the batch has the same length T.
+ */
+#ifndef OTT_H
+#define OTT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ott_cache ott_cache;
+
+enum {
+    OTT_OK = 0,
+    OTT_ERR_INVALID = -1,   /* bad argument: NULL, misaligned, unsupported shape */
+    OTT_ERR_STATE = -2,     /* not allowed now: prefill on a non-empty cache,
+                               decode on an empty one, poisoned handle */
+    OTT_ERR_CAPACITY = -3,  /* would exceed max_tokens */
+    OTT_ERR_OOM = -4,       /* device allocation failed in ott_create */
+    OTT_ERR_CUDA = -5,      /* a CUDA call or kernel failed; handle poisoned */
+    OTT_ERR_DEVICE = -6     /* a kernel reported a bounded wait that timed out */
+};
+
+/*
+ * Create an empty cache for B sequences, Hq query heads, Hkv kv heads, head
+ * dim d, group G, residual window R, pool capacity P (the pages' defaults are
+ * G=128, R=32, P=32). max_tokens bounds T; all device memory is allocated
+ * here (blocks, residual ring, pool, split-K scratch) and nothing is
+ * allocated by the other calls except ott_export_state's staging buffer.
+ * Supported: d in {64, 128}; Hq % Hkv == 0 with Hq/Hkv in {1, 2, 4};
+ * G >= 1; R >= 0; P >= 0; (P + G) * (d + 8) * 4 bytes of flush staging must
+ * fit in one CTA's shared memory. Uses the current CUDA device.
+ * Returns OTT_OK and *out, or an error with *out = NULL.
+ */
+int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P,
+               int max_tokens, ott_cache **out);
+
+/* Free everything. NULL-safe. Waits for the device to finish. */
+int ott_destroy(ott_cache *c);
+
+/*
+ * Prefill L tokens into an EMPTY cache. K, V: device fp16 [B][Hkv][L][d].
+ * Equivalent to L appends in token order (the flush runs for every group of
+ * G that leaves the residual window). L may be 0. Errors: OTT_ERR_STATE if
+ * T > 0, OTT_ERR_CAPACITY if L > max_tokens.
+ */
+int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream);
+
+/*
+ * Append one token to every sequence. k, v: device fp16 [B][Hkv][d]. The
+ * token goes to the fp16 residual ring; when G+R tokens wait, the flush
+ * kernel runs on the same stream (the decision is taken on the host from T,
+ * without a device round trip).
+ */
+int ott_append(ott_cache *c, const void *k, const void *v, void *stream);
+
+/*
+ * Decode-step attention for one query token per sequence.
+ * q: device fp16 [B][Hq][d]; out: device fp16 [B][Hq][d] (may not alias q).
+ * out = softmax(q . K^T / sqrt(d)) V over all T tokens: dequantized blocks,
+ * residual ring and outlier pool. Requires T >= 1 (else OTT_ERR_STATE).
+ * Uses the split-K scratch allocated at create; queues two kernels.
+ */
+int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
+
+/* Counts (same for every sequence and kv head): tokens seen, blocks (flushes),
+ * residual tokens, pool tokens. Host-side, no device access. */
+int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_pool);
+
+/* Valid tokens of block j (0 <= j < nf). Host-side. Returns the count or
+ * OTT_ERR_INVALID. */
+int ott_block_count(const ott_cache *c, int j);
+
+/*
+ * Canonical host copy of the state of units [u0, u0+nu), unit = b*Hkv + hkv.
+ * Every pointer is a HOST pointer and may be NULL (that array is skipped).
+ * Shapes, with nf blocks and nt residual tokens:
+ *   bidx  [nu][nf][G]      int32  token indices ascending, -1 padded
+ *   kcode [nu][nf][G][d/4] uint8  code of channel c at bits 2(c%4) of byte c/4
+ *   ks,kz [nu][nf][d]      fp16 bits: per-channel key scale / zero
+ *   vcode [nu][nf][G][d/4] uint8  same packing
+ *   vs,vz [nu][nf][G][d/32] fp16 bits: per-token value scale / zero
+ *   tk,tv [nu][nt][d]      fp16 bits: residual tokens nf*G .. T-1 in order
+ *   pidx  [nu][P] int32 ascending (-1 pad); pnorm [nu][P] fp32 bits;
+ *   pk,pv [nu][P][d]       pool tokens in ascending token order (0 padded)
+ * Padding slots are zero. Synchronizes the device; allocates a temporary
+ * device staging buffer. Errors: OTT_ERR_INVALID for a bad unit range.
+ */
+typedef struct {
+    int32_t *bidx;
+    uint8_t *kcode;
+    uint16_t *ks, *kz;
+    uint8_t *vcode;
+    uint16_t *vs, *vz;
+    uint16_t *tk, *tv;
+    int32_t *pidx;
+    uint32_t *pnorm;
+    uint16_t *pk, *pv;
+} ott_state_export;
+
+int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst);
+
+/*
+ * Wait for the device and read the cache's device status word: OTT_OK, or
+ * OTT_ERR_DEVICE if a kernel gave up a bounded wait, or OTT_ERR_CUDA.
+ */
+int ott_check_device(ott_cache *c);
+
+/* Bytes of device memory the cache holds. Host-side. */
+long long ott_device_bytes(const ott_cache *c);
+
+/* Static text for a status code. */
+const char *ott_status_str(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OTT_H */

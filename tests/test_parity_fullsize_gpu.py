@@ -1,0 +1,77 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times: the whole quantized state bit-exact against the oracle at
+every flush boundary the run crosses, and the attention output of a sample of
+(sequence, query head) pairs against the oracle's one-head decode.
+
+The Llama-3.1-8B-shaped workload has 32 layers with identical shapes; each
+layer's cache is independent, so one layer is checked here.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_ott_gb300 import synth
+from tests.parity_util import compare_out, compare_state
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_heads(w, n, seed):
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (w.B - 1, w.Hq - 1)}
+    while len(pairs) < min(n, w.B * w.Hq):
+        pairs.add((int(rng.integers(w.B)), int(rng.integers(w.Hq))))
+    return sorted(pairs)
+
+
+def _units_to_check(w, limit):
+    U = w.B * w.Hkv
+    if U <= limit:
+        return range(U)
+    rng = np.random.default_rng(7)
+    return sorted({0, U - 1, *rng.choice(U, limit - 2, replace=False).tolist()})
+
+
+def run_fullsize(oracle_mod, ott, name, steps, decode_steps, heads=8, unit_limit=64):
+    w = synth.WORKLOADS[name]
+    K, V = synth.prefill_kv(w)
+    orc = oracle_mod.OracleCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+    orc.prefill(K, V)
+    pairs = _sample_heads(w, heads, 1)
+    with ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + steps) as c:
+        c.prefill(K.cuda(), V.cuda())
+        del K, V
+        nf_prev = c.counts()[1]
+        units = _units_to_check(w, unit_limit)
+        compare_state(c.export_state(), orc)   # every unit after the prefill
+        for s in range(steps):
+            k, v, q = synth.step_kvq(w, s)
+            c.append(k.cuda(), v.cuda())
+            orc.append(k, v)
+            nf = c.counts()[1]
+            if nf != nf_prev:
+                compare_state(c.export_state(), orc, units)
+                nf_prev = nf
+            if s in decode_steps:
+                out = c.decode_attn(q.cuda()).float().cpu().numpy()
+                ref = np.stack([orc.decode_head(b, h, q[b, h]) for b, h in pairs])
+                got = torch.from_numpy(np.stack([out[b, h] for b, h in pairs]))
+                compare_out(got, ref, f"{name} step {s}")
+        c.check_device()
+
+
+def test_llama2_7b_layer(oracle_mod, ott):
+    run_fullsize(oracle_mod, ott, "llama2_7b_layer", 256, {0, 31, 32, 100, 255}, heads=12)
+
+
+def test_batch_b32_headline(oracle_mod, ott):
+    run_fullsize(oracle_mod, ott, "batch_b32", 300, {0, 31, 32, 160, 299}, heads=12, unit_limit=48)
+
+
+@pytest.mark.parametrize("name", ["mistral_gqa_g128", "mistral_gqa_g256"])
+def test_mistral_gqa(oracle_mod, ott, name):
+    run_fullsize(oracle_mod, ott, name, 256, {0, 63, 64, 200, 255}, heads=10)
+
+
+def test_llama31_8b_131k_one_layer(oracle_mod, ott):
+    run_fullsize(oracle_mod, ott, "llama31_8b_131k", 128, {0, 31, 32, 127}, heads=8)
