@@ -77,8 +77,10 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_token
     c->device = dev;
     c->sm_count = sms;
     c->flush_smem = fsmem;
-    // split capacity per unit: one split per block plus the fp16 chunks
-    c->su_max = c->NB + (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + 1;
+    // the decode grid's warps split the work items evenly; a warp's range
+    // (at most W/NW + 1 items) touches at most U/NW + 2 units
+    const int nwarps = sms * DEC_WARPS;
+    c->maxu = (int)((long long)B * Hkv / nwarps) + 2;
 
     const size_t U = (size_t)c->U;
     const size_t sz_blk = U * c->NB * (size_t)c->blk_bytes;
@@ -86,7 +88,7 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_token
     const size_t sz_ring = U * c->ring * (size_t)d * 2;
     const size_t sz_pool = U * (size_t)P * d * 2;
     const size_t sz_pn = U * (size_t)P * 4;
-    const size_t sz_part = U * (size_t)c->su_max * gq * (d + 2) * 4;
+    const size_t sz_part = (size_t)nwarps * c->maxu * 2 * gq * (d + 2) * 4;
     size_t off = 0;
     const size_t o_blk = off; off = round_up(off + sz_blk, 256);
     const size_t o_bidx = off; off = round_up(off + sz_bidx, 256);

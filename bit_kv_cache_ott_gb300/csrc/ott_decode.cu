@@ -7,15 +7,17 @@
 // sciencestack.ai Fig. 2 (decoding stage).
 //
 // Split-K (flash-decoding) design for one GB300:
-//   * A persistent grid (one CTA of 8 warps per SM) pulls splits from an
-//     atomic counter. A split is a run of quantized blocks of one unit, or
-//     32 fp16 tokens (residual ring + pool) of one unit. Every split keeps
-//     its own online-softmax state and writes (m, l, acc[d]) per query head;
-//     k_combine merges the splits with a log-sum-exp weighting.
-//   * Quantized splits: each warp streams its blocks into a private
+//   * Work items, unit by unit (unit = (sequence, kv head)): first the fp16
+//     tokens (residual ring, then pool) in chunks of 32, then the quantized
+//     blocks. A persistent grid (one CTA of 16 warps per SM) gives every warp
+//     an equal contiguous range of items (stream-K partition): no atomics, no
+//     tail, and one partial (m, l, acc[d]) per query head for each (unit,
+//     item type) segment a warp touches. k_combine finds a unit's partials
+//     arithmetically and merges them with log-sum-exp weights.
+//   * Quantized segments: each warp streams its blocks into a private
 //     two-stage shared-memory ring with 1-D TMA bulk copies
-//     (cp.async.bulk + mbarrier complete_tx), one copy per chunk of up to 8
-//     tiles. Waits are bounded; a timeout sets the cache's status word.
+//     (cp.async.bulk + mbarrier complete_tx), one copy per chunk of up to
+//     4 tiles of 16 tokens. Waits are bounded; a timeout sets the status word.
 //   * Dequantization is folded into the products: q.k_hat =
 //     sum_c (q_c s_c) code_c + sum_c q_c z_c and
 //     p.v_hat = sum_t (p_t s_t) code_t + sum_t p_t z_t.
@@ -25,8 +27,8 @@
 //     Scores: A = K codes [16 tokens x 16 channels], B = q*s [16 x (head,
 //     hi/lo)]. PV: A = V codes [16 channels x 16 tokens], B = p*s [16 tokens
 //     x (head, group, hi/lo)]. All query heads of a kv head share the codes.
-//   * fp16 splits: one lane per token for the scores, one lane per d/32
-//     channels for P.V, fp32 accumulation.
+//   * fp16 segments: one lane per token for the scores, one lane per d/32
+//     channels for P.V, fp32 accumulation, online softmax across chunks.
 #include <math_constants.h>
 
 #include <type_traits>
@@ -115,12 +117,15 @@ struct DecodeArgs {
     float *part;
     int *ctl;
     int Hq, Hkv, G;
-    int nf;
-    long long tail_start;
-    int ring_start;   // tail_start mod ring
+    int nf, jfull;      // blocks; blocks j >= jfull hold G tokens
+    int ring_start;     // first residual token's ring slot
     int ntail, npool;
-    int Sq, ipsq, Sf, S_u, total;
-    float sl2;   // softmax scale 1/sqrt(d) times log2(e)
+    int Sf;             // fp16 chunks per unit
+    int Iu;             // work items per unit: Sf + nf
+    long long W;        // U * Iu
+    int NWp;            // warps in the grid
+    int MAXU;           // units a warp's range can touch
+    float sl2;          // softmax scale 1/sqrt(d) times log2(e)
 };
 
 template <int D, int GQ>
@@ -132,7 +137,26 @@ struct Cfg {
     static constexpr int NV = (NG + GPV - 1) / GPV;  // PV B variants
     static constexpr int CPL = D / 32;             // channels per lane, fp16 path
     static constexpr int STAGE = stage_bytes(D);
+    static constexpr bool COOP = GQ <= 2;          // per-block constants computed cooperatively
+    static constexpr int QHL = COOP ? GQ * 2 * (D + 8) * 2 : 0;   // hi/lo staging bytes
+    static constexpr int WARP_SMEM = 2 * STAGE + 16 + GQ * D * 4 + QHL;
 };
+
+__device__ __forceinline__ int block_cnt(const DecodeArgs &a, int j) {
+    return j >= a.jfull ? a.G : block_count(a.P, a.G, j);
+}
+
+// First item of warp w's range (items are split as evenly as integers allow).
+__device__ __forceinline__ long long range_start(long long W, int NWp, long long w) { return w * W / NWp; }
+
+// The warp whose range holds item x.
+__device__ __forceinline__ int warp_of(long long W, int NWp, long long x) {
+    return (int)(((x + 1) * NWp + W - 1) / W - 1);
+}
+
+__device__ __forceinline__ size_t part_slot(const DecodeArgs &a, int w, int unit_off, int type) {
+    return ((size_t)w * a.MAXU + unit_off) * 2 + type;
+}
 
 template <int NW>
 __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[NW]) {
@@ -145,39 +169,36 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[NW]) {
     }
 }
 
-// ---------------------------------------------------------------- quantized split
 template <int D, int GQ>
-__device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, uint8_t *stg0,
-                            uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
+__device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
+    const int b = u / a.Hkv, hkv = u % a.Hkv;
+    const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + hkv * GQ) * D);
+    for (int e = lane; e < GQ * D / 2; e += 32) {
+        const float2 f = __half22float2(qp[e]);
+        qsm[2 * e] = f.x;
+        qsm[2 * e + 1] = f.y;
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------- quantized segment
+// Blocks [j0, j1) of unit u; the partial goes to part[slot].
+template <int D, int GQ>
+__device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
+                              uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
+                              int lane) {
     using C = Cfg<D, GQ>;
     constexpr int NKT = C::NKT, NW = C::NW, NG = C::NG, GPV = C::GPV, NV = C::NV;
     constexpr int KSZ = ksz_bytes(D), TB = tile_bytes(D);
     const int r = lane >> 2, i = lane & 3;
-    const int b = u / a.Hkv, hkv = u % a.Hkv;
-    const int G = a.G, P = a.P;
 
-    float acc[NKT][4];
-#pragma unroll
-    for (int mt = 0; mt < NKT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-    float zs[NV];
-#pragma unroll
-    for (int v = 0; v < NV; ++v) zs[v] = 0.0f;
-    float m_run = -CUDART_INF_F, l_run = 0.0f;   // head i
-    uint32_t Bk[NKT][2];
-    float c1 = 0.0f, c0 = 0.0f;
-
-    // PV B column of this lane: head hV, value-group offset glow, piece
-    const int hV = (r >> 1) / GPV, glow = (r >> 1) % GPV;
-    const int src0 = 4 * (2 * i) + hV, src1 = 4 * (2 * i + 1) + hV;
-
-    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < block_count(P, G, j); };
+    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < block_cnt(a, j); };
     int lj = j0, lk = 0;
     while (lj < j1 && !active(lj, lk)) { ++lj; lk = 0; }
     int cj_ = lj, ck_ = lk;   // next chunk to consume
-
     auto issue = [&](int j, int k, int st) {
         if (lane == 0) {
-            const int cj = block_count(P, G, j), vt = (cj + TILE - 1) / TILE;
+            const int vt = (block_cnt(a, j) + TILE - 1) / TILE;
             const int t0 = k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
             const uint8_t *bsrc = a.blk + ((size_t)u * a.NB + j) * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
@@ -191,27 +212,31 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
         ++k;
         while (j < j1 && !active(j, k)) { ++j; k = 0; }
     };
-
+    // start the copies first, then stage the queries while they fly
     int st_issue = 0;
     for (int n = 0; n < 2 && lj < j1; ++n) {
         issue(lj, lk, st_issue);
         st_issue ^= 1;
         next(lj, lk);
     }
-    // the query heads of this kv head, as fp32 in this warp's shared memory
+    load_queries<D, GQ>(a, u, qsm, lane);
+
+    float acc[NKT][4];
+#pragma unroll
+    for (int mt = 0; mt < NKT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+    float zs[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) zs[v] = 0.0f;
+    float m_run = -CUDART_INF_F, l_run = 0.0f;   // head i
+    uint32_t Bk[NKT][2];
+    float c1 = 0.0f, c0 = 0.0f;
+
     const int hB = r >> 1;               // score-MMA B column of this lane: head r/2,
     const bool piece = (r & 1) != 0;     // piece r&1 (hi or lo)
-    {
-        const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + hkv * GQ) * D);
-        for (int e = lane; e < GQ * D / 2; e += 32) {
-            const float2 f = __half22float2(qp[e]);
-            qsm[2 * e] = f.x;
-            qsm[2 * e + 1] = f.y;
-        }
-        __syncwarp();
-    }
-    const float qon = hB < GQ ? 1.0f : 0.0f;
-    const float *qrow = qsm + (hB < GQ ? hB : 0) * D;
+    const float pm = piece ? 1.0f : 0.0f;
+    // PV B column of this lane: head hV, value-group offset glow, piece
+    const int hV = (r >> 1) / GPV, glow = (r >> 1) % GPV;
+    const int src0 = 4 * (2 * i) + hV, src1 = 4 * (2 * i + 1) + hV;
 
     int st = 0;
     while (cj_ < j1) {
@@ -223,83 +248,140 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
             return false;
         }
         phase ^= 1u << st;
-        const int cj = block_count(P, G, cj_), vt = (cj + TILE - 1) / TILE;
+        const int cj = block_cnt(a, cj_), vt = (cj + TILE - 1) / TILE;
         const int t0 = ck_ * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
 
         if (ck_ == 0) {
-            // per-block constants: B = q*s split in hi/lo at a class scale
+            // per-block constants: B = q*s split in hi/lo at a per-block
+            // exponent E and a per-channel class scale; qz = q.z
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(stage);
-            float qs[NKT][2][2];
-            float amax = 0.0f, qz = 0.0f;
+            int Eh[GQ];
+            float qzh[GQ];
+            if constexpr (C::COOP) {
+                // each lane: channels lane + 32m of every head, staged as hi/lo rows
+                float xs[GQ][D / 32];
 #pragma unroll
-            for (int kt = 0; kt < NKT; ++kt)
+                for (int h = 0; h < GQ; ++h) {
+                    float amax = 0.0f, qz = 0.0f;
 #pragma unroll
-                for (int o = 0; o < 2; ++o) {
-                    const uint2 sz = *reinterpret_cast<const uint2 *>(ksz + 16 * kt + 2 * i + 8 * o);
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                    float2 qq = *reinterpret_cast<const float2 *>(qrow + 16 * kt + 2 * i + 8 * o);
-                    qq.x *= qon;
-                    qq.y *= qon;
-                    qs[kt][o][0] = qq.x * f0.x;
-                    qs[kt][o][1] = qq.y * f1.x;
-                    qz = fmaf(qq.x, f0.y, qz);
-                    qz = fmaf(qq.y, f1.y, qz);
-                    amax = fmaxf(amax, fmaxf(fabsf(qs[kt][o][0]), fabsf(qs[kt][o][1])));
+                    for (int m = 0; m < D / 32; ++m) {
+                        const int ch = lane + 32 * m;
+                        const float2 sz = __half22float2(*reinterpret_cast<const __half2 *>(ksz + ch));
+                        const float qv = qsm[h * D + ch];
+                        xs[h][m] = qv * sz.x;
+                        qz = fmaf(qv, sz.y, qz);
+                        amax = fmaxf(amax, fabsf(xs[h][m]));
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                        qz += __shfl_xor_sync(0xffffffffu, qz, o);
+                    }
+                    const int E = amax > 0.0f ? min(max(14 - (((__float_as_int(amax) >> 23) & 0xff) - 127), -100), 100) : 0;
+                    Eh[h] = E;
+                    qzh[h] = qz;
+#pragma unroll
+                    for (int m = 0; m < D / 32; ++m) {
+                        const int ch = lane + 32 * m;
+                        const int slotq = ((ch >> 3) & 1) * NKT + (ch >> 4);
+                        const float x = xs[h][m] * pow2i(E - 2 * cls_of_pos(slotq & 7));
+                        const __half hi = __float2half_rn(x);
+                        const __half lo = __float2half_rn(x - __half2float(hi));
+                        qhl[(h * 2 + 0) * (D + 8) + ch] = hi;
+                        qhl[(h * 2 + 1) * (D + 8) + ch] = lo;
+                    }
                 }
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            qz += __shfl_xor_sync(0xffffffffu, qz, 1);
-            qz += __shfl_xor_sync(0xffffffffu, qz, 2);
-            int E = amax > 0.0f ? 14 - (((__float_as_int(amax) >> 23) & 0xff) - 127) : 0;
-            E = min(max(E, -100), 100);
-            const float pm = piece ? 1.0f : 0.0f;
+                __syncwarp();
+                const __half *row = qhl + ((hB < GQ ? hB : 0) * 2 + (piece ? 1 : 0)) * (D + 8);
 #pragma unroll
-            for (int kt = 0; kt < NKT; ++kt)
+                for (int kt = 0; kt < NKT; ++kt)
 #pragma unroll
-                for (int o = 0; o < 2; ++o) {
-                    const int cls = cls_of_pos((o * NKT + kt) & 7);
-                    const float sc = pow2i(E - 2 * cls);
-                    const float x0 = qs[kt][o][0] * sc, x1 = qs[kt][o][1] * sc;
-                    const __half2 hh = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(hh);
-                    Bk[kt][o] = h2bits(__floats2half2_rn(x0 - pm * hf.x, x1 - pm * hf.y));
+                    for (int o = 0; o < 2; ++o) {
+                        const uint32_t v = *reinterpret_cast<const uint32_t *>(row + 16 * kt + 2 * i + 8 * o);
+                        Bk[kt][o] = hB < GQ ? v : 0u;
+                    }
+                __syncwarp();
+            } else {
+                // every lane computes its own 32 values (all columns are live)
+                const float *qrow = qsm + hB * D;
+                float qs[NKT][2][2];
+                float amax = 0.0f, qz = 0.0f;
+#pragma unroll
+                for (int kt = 0; kt < NKT; ++kt)
+#pragma unroll
+                    for (int o = 0; o < 2; ++o) {
+                        const uint2 sz = *reinterpret_cast<const uint2 *>(ksz + 16 * kt + 2 * i + 8 * o);
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
+                        const float2 qq = *reinterpret_cast<const float2 *>(qrow + 16 * kt + 2 * i + 8 * o);
+                        qs[kt][o][0] = qq.x * f0.x;
+                        qs[kt][o][1] = qq.y * f1.x;
+                        qz = fmaf(qq.x, f0.y, qz);
+                        qz = fmaf(qq.y, f1.y, qz);
+                        amax = fmaxf(amax, fmaxf(fabsf(qs[kt][o][0]), fabsf(qs[kt][o][1])));
+                    }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                qz += __shfl_xor_sync(0xffffffffu, qz, 1);
+                qz += __shfl_xor_sync(0xffffffffu, qz, 2);
+                const int E = amax > 0.0f ? min(max(14 - (((__float_as_int(amax) >> 23) & 0xff) - 127), -100), 100) : 0;
+#pragma unroll
+                for (int kt = 0; kt < NKT; ++kt)
+#pragma unroll
+                    for (int o = 0; o < 2; ++o) {
+                        const float sc = pow2i(E - 2 * cls_of_pos((o * NKT + kt) & 7));
+                        const float x0 = qs[kt][o][0] * sc, x1 = qs[kt][o][1] * sc;
+                        const __half2 hh = __floats2half2_rn(x0, x1);
+                        const float2 hf = __half22float2(hh);
+                        Bk[kt][o] = h2bits(__floats2half2_rn(x0 - pm * hf.x, x1 - pm * hf.y));
+                    }
+                // lane 8h holds head h (piece 0)
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) {
+                    Eh[h] = __shfl_sync(0xffffffffu, E, 8 * h);
+                    qzh[h] = __shfl_sync(0xffffffffu, qz, 8 * h);
                 }
-            // score constants of head i (lane 8i holds head i, piece 0)
-            const float Ei = __shfl_sync(0xffffffffu, (float)E, 8 * i);
-            const float qzi = __shfl_sync(0xffffffffu, qz, 8 * i);
-            c1 = pow2i(24 - (int)Ei) * a.sl2;
+            }
+            // score constants of head i
+            int Ei = Eh[0];
+            float qzi = qzh[0];
+#pragma unroll
+            for (int h = 1; h < GQ; ++h)
+                if (i == h) { Ei = Eh[h]; qzi = qzh[h]; }
+            c1 = pow2i(24 - Ei) * a.sl2;
             c0 = qzi * a.sl2;
         }
 
         const bool partial = 16 * (t0 + nt) > cj;   // chunk reaches past the valid tokens
-        // phase 1: scores of every tile of the chunk (head i, tokens r and r+8)
+        // phase 1: scores of every tile of the chunk (head i, tokens r and r+8);
+        // all tiles' key words are read first so their unpacking and MMAs interleave
         float lg[CHUNK_TILES][2];
+        uint32_t kw[CHUNK_TILES][NW];
+#pragma unroll
+        for (int tau = 0; tau < CHUNK_TILES; ++tau)
+            if (tau < nt) lds_words<NW>(stage + KSZ + tau * TB + tile_k_off(D) + lane * NW * 4, kw[tau]);
 #pragma unroll
         for (int tau = 0; tau < CHUNK_TILES; ++tau) {
             lg[tau][0] = lg[tau][1] = -CUDART_INF_F;
             if (tau < nt) {
-                const uint8_t *tb = stage + KSZ + tau * TB;
-                uint32_t kw[NW], k10[NW];
-                lds_words<NW>(tb + tile_k_off(D) + lane * NW * 4, kw);
+                uint32_t k10[NW];
 #pragma unroll
-                for (int w = 0; w < NW; ++w) k10[w] = kw[w] >> 10;
+                for (int w = 0; w < NW; ++w) k10[w] = kw[tau][w] >> 10;
                 float da[4] = {0.0f, 0.0f, 0.0f, 0.0f}, db[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int kt = 0; kt < NKT; ++kt) {
                     const int q0 = kt, q1 = NKT + kt;
                     const int w0 = 2 * (q0 >> 3), p0 = q0 & 7, w1 = 2 * (q1 >> 3), p1 = q1 & 7;
-                    mma16816((kt & 1) ? db : da, ext_rt(kw[w0], k10[w0], p0), ext_rt(kw[w0 + 1], k10[w0 + 1], p0),
-                             ext_rt(kw[w1], k10[w1], p1), ext_rt(kw[w1 + 1], k10[w1 + 1], p1), Bk[kt][0],
-                             Bk[kt][1]);
+                    mma16816((kt & 1) ? db : da, ext_rt(kw[tau][w0], k10[w0], p0),
+                             ext_rt(kw[tau][w0 + 1], k10[w0 + 1], p0), ext_rt(kw[tau][w1], k10[w1], p1),
+                             ext_rt(kw[tau][w1 + 1], k10[w1 + 1], p1), Bk[kt][0], Bk[kt][1]);
                 }
-                const float dsc[4] = {da[0] + db[0], da[1] + db[1], da[2] + db[2], da[3] + db[3]};
-                lg[tau][0] = fmaf(dsc[0] + dsc[1], c1, c0);
-                lg[tau][1] = fmaf(dsc[2] + dsc[3], c1, c0);
+                lg[tau][0] = fmaf((da[0] + db[0]) + (da[1] + db[1]), c1, c0);
+                lg[tau][1] = fmaf((da[2] + db[2]) + (da[3] + db[3]), c1, c0);
                 if (partial) {
-                    const int slot = 16 * (t0 + tau) + r;
-                    if (slot >= cj) lg[tau][0] = -CUDART_INF_F;
-                    if (slot + 8 >= cj) lg[tau][1] = -CUDART_INF_F;
+                    const int slotk = 16 * (t0 + tau) + r;
+                    if (slotk >= cj) lg[tau][0] = -CUDART_INF_F;
+                    if (slotk + 8 >= cj) lg[tau][1] = -CUDART_INF_F;
                 }
                 if (i >= GQ) lg[tau][0] = lg[tau][1] = -CUDART_INF_F;
             }
@@ -328,10 +410,12 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
         }
         const float m_use = m_run == -CUDART_INF_F ? 0.0f : m_run;
 
-        // phase 3: weights, P' = p*s (hi/lo) and the PV products
-        const float pm = piece ? 1.0f : 0.0f;
+        // phase 3a: weights and P' = p*s (hi/lo) for every tile of the chunk
+        uint32_t bv[CHUNK_TILES][NV][2];
 #pragma unroll
         for (int tau = 0; tau < CHUNK_TILES; ++tau) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) bv[tau][v][0] = bv[tau][v][1] = 0u;
             if (tau < nt) {
                 const uint8_t *tb = stage + KSZ + tau * TB;
                 const float p0 = ex2(lg[tau][0] - m_use), p1 = ex2(lg[tau][1] - m_use);
@@ -340,11 +424,9 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
                 const float pb = __shfl_sync(0xffffffffu, p0, src1);
                 const float pc = __shfl_sync(0xffffffffu, p1, src0);
                 const float pd = __shfl_sync(0xffffffffu, p1, src1);
-                uint32_t bv[NV][2];
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
                     const int gamma = v * GPV + glow;
-                    bv[v][0] = bv[v][1] = 0u;
                     if (gamma < NG) {
                         const uint4 sz =
                             *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
@@ -359,12 +441,18 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
                         zs[v] = fmaf(pd, e3.y, zs[v]);
                         const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
                         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                        bv[v][0] = h2bits(__floats2half2_rn(x0 - pm * f01.x, x1 - pm * f01.y));
-                        bv[v][1] = h2bits(__floats2half2_rn(x2 - pm * f23.x, x3 - pm * f23.y));
+                        bv[tau][v][0] = h2bits(__floats2half2_rn(x0 - pm * f01.x, x1 - pm * f01.y));
+                        bv[tau][v][1] = h2bits(__floats2half2_rn(x2 - pm * f23.x, x3 - pm * f23.y));
                     }
                 }
+            }
+        }
+        // phase 3b: the PV products
+#pragma unroll
+        for (int tau = 0; tau < CHUNK_TILES; ++tau) {
+            if (tau < nt) {
                 uint32_t vw[NW], v10[NW];
-                lds_words<NW>(tb + tile_v_off(D) + lane * NW * 4, vw);
+                lds_words<NW>(stage + KSZ + tau * TB + tile_v_off(D) + lane * NW * 4, vw);
 #pragma unroll
                 for (int w = 0; w < NW; ++w) v10[w] = vw[w] >> 10;
 #pragma unroll
@@ -374,7 +462,7 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
                     const int v = (mt >> 1) / GPV;
                     mma16816(acc[mt], ext_rt(vw[w0], v10[w0], p0_), ext_rt(vw[w1], v10[w1], p1_),
                              ext_rt(vw[w0 + 1], v10[w0 + 1], p0_), ext_rt(vw[w1 + 1], v10[w1 + 1], p1_),
-                             bv[v][0], bv[v][1]);
+                             bv[tau][v][0], bv[tau][v][1]);
                 }
             }
         }
@@ -400,7 +488,7 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 1);
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 2);
     }
-    float *pb = a.part + (size_t)sg * GQ * (D + 2);
+    float *pb = a.part + slot * GQ * (D + 2);
     if (r == 0 && i < GQ) {
         pb[i * (D + 2) + 0] = m_run;
         pb[i * (D + 2) + 1] = l;
@@ -421,111 +509,131 @@ __device__ bool quant_split(const DecodeArgs &a, int sg, int u, int j0, int j1, 
     return true;
 }
 
-// ---------------------------------------------------------------- fp16 split
+// ---------------------------------------------------------------- fp16 segment
+// fp16 chunks [c0, c1) of unit u (chunk c = residual-then-pool tokens
+// 32c .. 32c+31); the partial goes to part[slot].
 template <int D, int GQ>
-__device__ void fp16_split(const DecodeArgs &a, int sg, int u, int lf, float *qsm, int lane) {
+__device__ void fp16_segment(const DecodeArgs &a, size_t slot, int u, int c0, int c1, float *qsm, int lane) {
     constexpr int CPL = Cfg<D, GQ>::CPL;
-    const int b = u / a.Hkv, hkv = u % a.Hkv;
     const int nfp = a.ntail + a.npool;
-    const int f0 = lf * FP16_CHUNK, nvalid = min(FP16_CHUNK, nfp - f0);
-
-    // query heads of this kv head, as fp32 in shared memory
-    const __half *qp = a.q + ((size_t)b * a.Hq + hkv * GQ) * D;
-    for (int e = lane; e < GQ * D; e += 32) qsm[e] = __half2float(qp[e]);
-    __syncwarp();
+    load_queries<D, GQ>(a, u, qsm, lane);
 
     auto row_of = [&](int f, const __half *ringb, const __half *poolb) -> const __half * {
         if (f < a.ntail) {
-            int slot = a.ring_start + f;   // f < ntail < ring
-            if (slot >= a.ring) slot -= a.ring;
-            return ringb + ((size_t)u * a.ring + slot) * D;
+            int s = a.ring_start + f;   // f < ntail < ring
+            if (s >= a.ring) s -= a.ring;
+            return ringb + ((size_t)u * a.ring + s) * D;
         }
         return poolb + ((size_t)u * a.P + (f - a.ntail)) * D;
     };
 
-    const bool valid = lane < nvalid;
-    float dot[GQ];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
-    {
-        // the whole key row of this lane's token: all loads in flight at once
-        uint4 kv[D / 8];
-        const __half *kr = row_of(valid ? f0 + lane : f0, a.rk, a.pk);
-#pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8) kv[c8] = valid ? reinterpret_cast<const uint4 *>(kr)[c8] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8) {
-            const __half2 *kh = reinterpret_cast<const __half2 *>(&kv[c8]);
-            float kf[8];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const float2 f = __half22float2(kh[x]);
-                kf[2 * x] = f.x;
-                kf[2 * x + 1] = f.y;
-            }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float4 qa = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[0];
-                const float4 qb = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[1];
-                dot[h] = fmaf(qa.x, kf[0], dot[h]);
-                dot[h] = fmaf(qa.y, kf[1], dot[h]);
-                dot[h] = fmaf(qa.z, kf[2], dot[h]);
-                dot[h] = fmaf(qa.w, kf[3], dot[h]);
-                dot[h] = fmaf(qb.x, kf[4], dot[h]);
-                dot[h] = fmaf(qb.y, kf[5], dot[h]);
-                dot[h] = fmaf(qb.z, kf[6], dot[h]);
-                dot[h] = fmaf(qb.w, kf[7], dot[h]);
-            }
-        }
-    }
-    float m[GQ], p[GQ], acc[GQ][CPL];
+    float m_run[GQ], l_run[GQ], acc[GQ][CPL];
 #pragma unroll
     for (int h = 0; h < GQ; ++h) {
-        const float lg = valid ? dot[h] * a.sl2 : -CUDART_INF_F;
-        float mx = lg;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        m[h] = mx;
-        p[h] = ex2(lg - (mx == -CUDART_INF_F ? 0.0f : mx));
+        m_run[h] = -CUDART_INF_F;
+        l_run[h] = 0.0f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) acc[h][c] = 0.0f;
     }
-    // this lane's channels of the value rows, eight tokens' loads in flight at a time
-    using VT = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
-#pragma unroll 1
-    for (int tb = 0; tb < nvalid; tb += 8) {
-        VT vv[8];
+    for (int chk = c0; chk < c1; ++chk) {
+        // keep the query rows in shared memory (re-read per chunk) instead of
+        // letting them be hoisted into registers across chunks
+        asm volatile("" ::: "memory");
+        const int f0 = chk * FP16_CHUNK, nvalid = min(FP16_CHUNK, nfp - f0);
+        const bool valid = lane < nvalid;
+        float dot[GQ];
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-            vv[x] = (tb + x < nvalid) ? *reinterpret_cast<const VT *>(row_of(f0 + tb + x, a.rv, a.pv) + lane * CPL)
-                                      : VT{};
+        for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
+        {
+            // this lane's token's key row, half a row of loads in flight at a time
+            constexpr int KV = D / 8, KH = KV > 8 ? 8 : KV;
+            const __half *kr = row_of(valid ? f0 + lane : f0, a.rk, a.pk);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            float vf[CPL];
-            if constexpr (CPL == 4) {
-                const float2 f0_ = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].x));
-                const float2 f1_ = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].y));
-                vf[0] = f0_.x; vf[1] = f0_.y; vf[2] = f1_.x; vf[3] = f1_.y;
-            } else {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x]));
-                vf[0] = f.x; vf[1] = f.y;
+            for (int hb = 0; hb < KV; hb += KH) {
+                uint4 kv[KH];
+#pragma unroll
+                for (int x = 0; x < KH; ++x)
+                    kv[x] = valid ? reinterpret_cast<const uint4 *>(kr)[hb + x] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int x = 0; x < KH; ++x) {
+                    const int c8 = hb + x;
+                    const __half2 *kh = reinterpret_cast<const __half2 *>(&kv[x]);
+                    float kf[8];
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) {
+                        const float2 f = __half22float2(kh[y]);
+                        kf[2 * y] = f.x;
+                        kf[2 * y + 1] = f.y;
+                    }
+#pragma unroll
+                    for (int h = 0; h < GQ; ++h) {
+                        const float4 qa = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[0];
+                        const float4 qb = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[1];
+                        dot[h] = fmaf(qa.x, kf[0], dot[h]);
+                        dot[h] = fmaf(qa.y, kf[1], dot[h]);
+                        dot[h] = fmaf(qa.z, kf[2], dot[h]);
+                        dot[h] = fmaf(qa.w, kf[3], dot[h]);
+                        dot[h] = fmaf(qb.x, kf[4], dot[h]);
+                        dot[h] = fmaf(qb.y, kf[5], dot[h]);
+                        dot[h] = fmaf(qb.z, kf[6], dot[h]);
+                        dot[h] = fmaf(qb.w, kf[7], dot[h]);
+                    }
+                }
             }
+        }
+        float p[GQ];
 #pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float pt = __shfl_sync(0xffffffffu, p[h], (tb + x) & 31);
+        for (int h = 0; h < GQ; ++h) {
+            const float lg = valid ? dot[h] * a.sl2 : -CUDART_INF_F;
+            float mx = lg;
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(pt, vf[c], acc[h][c]);
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float m_new = fmaxf(m_run[h], mx);   // finite: the chunk has >= 1 token
+            const float alpha = ex2(m_run[h] - m_new);
+            l_run[h] *= alpha;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[h][c] *= alpha;
+            m_run[h] = m_new;
+            p[h] = ex2(lg - m_new);
+            l_run[h] += p[h];
+        }
+        // this lane's channels of the value rows, eight tokens' loads in flight at a time
+        using VT = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
+#pragma unroll 1
+        for (int tb = 0; tb < nvalid; tb += 8) {
+            VT vv[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                vv[x] = (tb + x < nvalid) ? *reinterpret_cast<const VT *>(row_of(f0 + tb + x, a.rv, a.pv) + lane * CPL)
+                                          : VT{};
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                float vf[CPL];
+                if constexpr (CPL == 4) {
+                    const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].x));
+                    const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].y));
+                    vf[0] = fa.x; vf[1] = fa.y; vf[2] = fb.x; vf[3] = fb.y;
+                } else {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x]));
+                    vf[0] = f.x; vf[1] = f.y;
+                }
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) {
+                    const float pt = __shfl_sync(0xffffffffu, p[h], (tb + x) & 31);
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(pt, vf[c], acc[h][c]);
+                }
             }
         }
     }
-    float *pb = a.part + (size_t)sg * GQ * (D + 2);
+    float *pb = a.part + slot * GQ * (D + 2);
 #pragma unroll
     for (int h = 0; h < GQ; ++h) {
-        float l = p[h];
+        float l = l_run[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) {
-            pb[h * (D + 2) + 0] = m[h];
+            pb[h * (D + 2) + 0] = m_run[h];
             pb[h * (D + 2) + 1] = l;
         }
 #pragma unroll
@@ -539,11 +647,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     using C = Cfg<D, GQ>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *stg0 = smem + (size_t)warp * 2 * C::STAGE;
-    uint8_t *stg1 = stg0 + C::STAGE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)DEC_WARPS * 2 * C::STAGE) + 2 * warp;
-    float *qsm = reinterpret_cast<float *>(smem + (size_t)DEC_WARPS * 2 * C::STAGE + DEC_WARPS * 16) +
-                 (size_t)warp * GQ * D;
+    uint8_t *wbase = smem + (size_t)warp * C::WARP_SMEM;
+    uint8_t *stg0 = wbase;
+    uint8_t *stg1 = wbase + C::STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wbase + 2 * C::STAGE);
+    float *qsm = reinterpret_cast<float *>(wbase + 2 * C::STAGE + 16);
+    __half *qhl = reinterpret_cast<__half *>(wbase + 2 * C::STAGE + 16 + GQ * D * 4);
     if (lane == 0) {
         mbar_init(&bars[0]);
         mbar_init(&bars[1]);
@@ -551,52 +660,64 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     }
     __syncwarp();
     uint32_t phase = 0;
-    // the next split's id is fetched one split ahead, so the atomic's round
-    // trip overlaps the current split
-    int s_next = 0;
-    if (lane == 0) s_next = atomicAdd(&a.ctl[0], 1);
-    s_next = __shfl_sync(0xffffffffu, s_next, 0);
-    while (s_next < a.total) {
-        const int s = s_next;
-        if (lane == 0) s_next = atomicAdd(&a.ctl[0], 1);
-        s_next = __shfl_sync(0xffffffffu, s_next, 0);
-        const int u = s / a.S_u, ls = s % a.S_u;
-        if (ls < a.Sq) {
-            if (!quant_split<D, GQ>(a, s, u, ls * a.ipsq, min(a.nf, (ls + 1) * a.ipsq), stg0, stg1, bars,
-                                    phase, qsm, lane))
-                break;
+    // this warp's contiguous range of work items, split into (unit, type) segments
+    const int gw = blockIdx.x * DEC_WARPS + warp;
+    long long x = range_start(a.W, a.NWp, gw);
+    const long long x1 = range_start(a.W, a.NWp, gw + 1);
+    const int u_first = (int)(x / a.Iu);
+    while (x < x1) {
+        const int u = (int)(x / a.Iu);
+        const long long ubase = (long long)u * a.Iu;
+        const int off = (int)(x - ubase);
+        if (off < a.Sf) {
+            const int end = (int)min(x1 - ubase, (long long)a.Sf);
+            fp16_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 0), u, off, end, qsm, lane);
+            x = ubase + end;
         } else {
-            fp16_split<D, GQ>(a, s, u, ls - a.Sq, qsm, lane);
+            const int end = (int)min(x1 - ubase, (long long)a.Iu);
+            if (!quant_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 1), u, off - a.Sf, end - a.Sf, stg0,
+                                      stg1, bars, phase, qsm, qhl, lane))
+                return;
+            x = ubase + end;
         }
     }
 }
 
+// One warp per (sequence, query head): find the partials of its unit (the
+// warps whose ranges overlap the unit's items) and merge them.
 template <int D, int GQ>
-__global__ void k_combine(const float *__restrict__ part, __half *__restrict__ out, int *ctl, int B, int Hq,
-                          int Hkv, int S_u) {
+__global__ void k_combine(DecodeArgs a, int B) {
     constexpr int CPL = D / 32;
-    if (blockIdx.x == 0 && threadIdx.x == 0) ctl[0] = 0;   // re-arm the split counter
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (w >= B * Hq) return;
-    const int b = w / Hq, hq = w % Hq, u = b * Hkv + hq / GQ, h = hq % GQ;
-    const size_t sstride = (size_t)GQ * (D + 2);
-    const float *base = part + ((size_t)u * S_u * GQ + h) * (D + 2);
-    float M = -CUDART_INF_F;
-    for (int s = lane; s < S_u; s += 32) M = fmaxf(M, base[s * sstride]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.0f, acc[CPL];
+    if (w >= B * a.Hq) return;
+    const int b = w / a.Hq, hq = w % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
+    const long long ub = (long long)u * a.Iu, ue = ub + a.Iu;
+    const int wa = warp_of(a.W, a.NWp, ub), wb = warp_of(a.W, a.NWp, ue - 1);
+    float M = -CUDART_INF_F, L = 0.0f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
-    for (int s = 0; s < S_u; ++s) {
-        const float *ps = base + s * sstride;
-        const float ms = ps[0];
-        const float wgt = ms == -CUDART_INF_F ? 0.0f : exp2f(ms - M);
-        L = fmaf(wgt, ps[1], L);
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int ww = wa; ww <= wb; ++ww) {
+            const long long s0 = range_start(a.W, a.NWp, ww), s1 = range_start(a.W, a.NWp, ww + 1);
+            const int uf = (int)(s0 / a.Iu);
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wgt, ps[2 + lane * CPL + c], acc[c]);
+            for (int type = 0; type < 2; ++type) {
+                const long long t0 = type ? ub + a.Sf : ub, t1 = type ? ue : ub + a.Sf;
+                if (max(s0, t0) >= min(s1, t1)) continue;   // no overlap
+                const float *ps = a.part + (part_slot(a, ww, u - uf, type) * GQ + h) * (D + 2);
+                const float ms = ps[0];
+                if (pass == 0) {
+                    M = fmaxf(M, ms);
+                } else {
+                    const float wgt = ms == -CUDART_INF_F ? 0.0f : ex2(ms - M);
+                    L = fmaf(wgt, ps[1], L);
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wgt, ps[2 + lane * CPL + c], acc[c]);
+                }
+            }
+        }
     }
-    __half *o = out + ((size_t)b * Hq + hq) * D + lane * CPL;
+    __half *o = a.out + ((size_t)b * a.Hq + hq) * D + lane * CPL;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) o[c] = __float2half_rn(acc[c] / L);
 }
@@ -621,32 +742,22 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cu
     a.Hkv = c->Hkv;
     a.G = c->G;
     a.nf = c->nf;
-    a.tail_start = (long long)c->nf * c->G;
-    a.ring_start = (int)(a.tail_start % c->ring);
-    a.ntail = (int)(c->T - a.tail_start);
+    a.jfull = (c->P + c->G - 1) / c->G;   // from this block on, the pool is full
+    const long long tail_start = (long long)c->nf * c->G;
+    a.ring_start = (int)(tail_start % c->ring);
+    a.ntail = (int)(c->T - tail_start);
     a.npool = pool_after(c->P, c->G, c->nf);
-    const int nfp = a.ntail + a.npool;
-    a.Sf = (nfp + FP16_CHUNK - 1) / FP16_CHUNK;
-    // blocks per quantized split: aim at ~8 splits per resident warp overall
-    const long long target = 8LL * c->sm_count * DEC_WARPS;
-    const long long per_unit = target / c->U > 1 ? target / c->U : 1;
-    int ipsq = c->nf > 0 ? (int)((c->nf + per_unit - 1) / per_unit) : 1;
-    ipsq = ipsq < 1 ? 1 : (ipsq > 4 ? 4 : ipsq);
-    a.Sq = (c->nf + ipsq - 1) / ipsq;
-    while (a.Sq + a.Sf > c->su_max) {   // split capacity of the scratch buffer
-        ++ipsq;
-        a.Sq = (c->nf + ipsq - 1) / ipsq;
-    }
-    a.ipsq = ipsq;
-    a.S_u = a.Sq + a.Sf;
-    a.total = c->U * a.S_u;
+    a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
+    a.Iu = a.Sf + c->nf;
+    a.W = (long long)c->U * a.Iu;
+    a.NWp = c->sm_count * DEC_WARPS;
+    a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
-    const int smem = decode_smem_bytes(D, GQ);
-    k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, smem, s>>>(a);
+    k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = c->B * c->Hq, th = 256, bl = (warps * 32 + th - 1) / th;
-    k_combine<D, GQ><<<bl, th, 0, s>>>(c->part, out, c->ctl, c->B, c->Hq, c->Hkv, a.S_u);
+    k_combine<D, GQ><<<bl, th, 0, s>>>(a, c->B);
     return cudaGetLastError();
 }
 
@@ -662,7 +773,11 @@ bool decode_supported(int d, int gq) {
 }
 
 int decode_smem_bytes(int d, int gq) {
-    return DEC_WARPS * (2 * stage_bytes(d) + 16 + gq * d * 4);
+#define OTT_SM(D_, G_) \
+    if (d == D_ && gq == G_) return Cfg<D_, G_>::WARP_SMEM * DEC_WARPS;
+    OTT_SM(128, 1) OTT_SM(128, 2) OTT_SM(128, 4) OTT_SM(64, 1) OTT_SM(64, 2) OTT_SM(64, 4)
+#undef OTT_SM
+    return 1 << 30;
 }
 
 // Both kernels may use up to smem_max bytes of dynamic shared memory (the

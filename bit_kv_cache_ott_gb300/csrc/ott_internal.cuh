@@ -108,7 +108,7 @@ struct ott_cache {
     int device;
     int sm_count;
     int flush_smem;
-    int su_max;             // split capacity per unit
+    int maxu;               // units one decode warp's item range can touch
     // device memory (one allocation)
     void *mem;
     size_t mem_bytes;
@@ -118,8 +118,8 @@ struct ott_cache {
     __half *pk, *pv;        // [U][P][d]
     float *pnorm;           // [U][P]
     int32_t *pidx;          // [U][P]
-    float *part;            // [U][su_max][gq][d+2] split-K partials
-    int *ctl;               // [0] split counter, [1] status flag
+    float *part;            // [warps][maxu][2][gq][d+2] split-K partials
+    int *ctl;               // [1] status flag set by a bounded wait that timed out
 };
 
 namespace ott {
