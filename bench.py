@@ -46,6 +46,26 @@ def dist_env():
     return ws, rank, local
 
 
+def shard(w, rank: int, world: int):
+    """Weak scaling: rank r runs its own batch of sequences (a different seed)."""
+    return w.with_(seed=w.seed + 7919 * rank) if world > 1 else w
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's time: every rank contributes, all receive the max."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(B: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank decodes B tokens per step."""
+    return B * steps * world / (ms * 1e-3)
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -154,7 +174,7 @@ def oracle_rate(w, steps: int, warmup: int, units_sample: int):
     dt = time.perf_counter() - t0
     frac = (Bs * ws.Hkv) / (w.B * w.Hkv)
     per_step_full = dt / steps / frac
-    rate = w.B * w.layers / (per_step_full * w.layers)   # tokens/s (every layer decodes each token)
+    rate = w.B / (per_step_full * w.layers)   # tokens/s: each token passes every layer
     sample = (f"{Bs} of {w.B} sequences ({Bs * w.Hkv} of {w.B * w.Hkv} (sequence, kv head) units), "
               f"{steps} timed decode steps after {warmup} warm-up, T={w.L}+; one layer; scaled by units")
     return rate, dt, sample
@@ -197,7 +217,7 @@ def run_ours(args, w):
             torch.distributed.barrier()
 
     # weak scaling: rank r holds its own shard of B sequences
-    wr = w.with_(seed=w.seed + 7919 * rank) if ws > 1 else w
+    wr = shard(w, rank, ws)
     K_steps, W_steps, E_steps = args.steps, args.warmup, args.e2e_steps
     total_steps = W_steps + K_steps + E_steps
     caches = []
@@ -260,15 +280,11 @@ def run_ours(args, w):
     ms = e0.elapsed_time(e1)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec_events)
     launches = K_steps * w.layers * 3 + flushes   # append + decode + combine, plus flushes
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     for c in caches:
         c.check_device()
 
-    tokens = w.B * K_steps * ws
-    value = tokens / (ms * 1e-3)
+    value = job_tokens_per_s(w.B, K_steps, ws, ms)
     n_launch = K_steps * w.layers
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -294,12 +310,8 @@ def run_ours(args, w):
         x1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = x0.elapsed_time(x1)
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": w.B * E_steps * ws / (ems * 1e-3), "unit": "tokens/s",
+        ems = max_over_ranks(x0.elapsed_time(x1), dev)
+        e2e = {"value": job_tokens_per_s(w.B, E_steps, ws, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in pin[0])),
                "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()), "steps": E_steps}
 

@@ -31,8 +31,6 @@
 //     channels for P.V, fp32 accumulation, online softmax across chunks.
 #include <math_constants.h>
 
-#include <type_traits>
-
 #include "ott_internal.cuh"
 
 namespace ott {
@@ -511,135 +509,167 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
 
 // ---------------------------------------------------------------- fp16 segment
 // fp16 chunks [c0, c1) of unit u (chunk c = residual-then-pool tokens
-// 32c .. 32c+31); the partial goes to part[slot].
-template <int D, int GQ>
-__device__ void fp16_segment(const DecodeArgs &a, size_t slot, int u, int c0, int c1, float *qsm, int lane) {
-    constexpr int CPL = Cfg<D, GQ>::CPL;
-    const int nfp = a.ntail + a.npool;
-    load_queries<D, GQ>(a, u, qsm, lane);
+// 32c .. 32c+31); the partial goes to part[slot]. Tokens stream through the
+// warp's stage ring 8 at a time: one 1-D bulk copy per key and value row into
+// rows padded to d+8 halves (conflict-free ldmatrix). Scores: A = key rows
+// (ldmatrix), B = q (exact fp16). P.V: A = value rows transposed
+// (ldmatrix.trans), B = p split into fp16 hi + lo, mma.sync m16n8k8.
+__device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(b0));
+}
+__device__ __forceinline__ void bulk_copy_only(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
 
-    auto row_of = [&](int f, const __half *ringb, const __half *poolb) -> const __half * {
+template <int D, int GQ>
+__device__ bool fp16_segment(const DecodeArgs &a, size_t slot, int u, int c0, int c1, uint8_t *stg0,
+                             uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
+    constexpr int NKT = D / 16;
+    constexpr int RS = D + 8;                 // padded row stride (halves)
+    constexpr int SUB = 8;                    // tokens per sub-tile
+    const int r = lane >> 2, i = lane & 3;
+    const int nfp = a.ntail + a.npool;
+    const int fb = c0 * FP16_CHUNK, fe = min(c1 * FP16_CHUNK, nfp);
+    const int nsub = (fe - fb + SUB - 1) / SUB;
+
+    auto row_ptr = [&](int f, bool val) -> const __half * {
+        const __half *base = val ? a.rv : a.rk;
         if (f < a.ntail) {
             int s = a.ring_start + f;   // f < ntail < ring
             if (s >= a.ring) s -= a.ring;
-            return ringb + ((size_t)u * a.ring + s) * D;
+            return base + ((size_t)u * a.ring + s) * D;
         }
-        return poolb + ((size_t)u * a.P + (f - a.ntail)) * D;
+        return (val ? a.pv : a.pk) + ((size_t)u * a.P + (f - a.ntail)) * D;
     };
+    // lanes 0..7 copy key rows, 8..15 value rows; rows past the end repeat
+    // the sub-tile's first token (finite values, masked by a zero weight)
+    auto issue = [&](int k, int st) {
+        uint8_t *dst = st ? stg1 : stg0;
+        if (lane == 0) expect_tx(&bars[st], 2 * SUB * D * 2);
+        __syncwarp();
+        if (lane < 2 * SUB) {
+            const int x = lane & (SUB - 1);
+            int f = fb + k * SUB + x;
+            if (f >= fe) f = fb + k * SUB;
+            bulk_copy_only(dst + (size_t)lane * RS * 2, row_ptr(f, lane >= SUB), D * 2, &bars[st]);
+        }
+    };
+    int st_issue = 0;
+    for (int k = 0; k < 2 && k < nsub; ++k) {
+        issue(k, st_issue);
+        st_issue ^= 1;
+    }
+    load_queries<D, GQ>(a, u, qsm, lane);
+    // score B operand: column r = (head r/2, piece r&1); q is exact in fp16
+    const int hB = r >> 1;
+    uint32_t Bq[NKT][2];
+#pragma unroll
+    for (int kt = 0; kt < NKT; ++kt)
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const float2 qq = *reinterpret_cast<const float2 *>(qsm + (hB < GQ ? hB : 0) * D + 16 * kt + 2 * i + 8 * o);
+            Bq[kt][o] = (hB < GQ && (r & 1) == 0) ? h2bits(__floats2half2_rn(qq.x, qq.y)) : 0u;
+        }
+    float acc[NKT][4];
+#pragma unroll
+    for (int mt = 0; mt < NKT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+    float m_run = -CUDART_INF_F, l_run = 0.0f;   // head i
+    const float pm = (r & 1) ? 1.0f : 0.0f;
+    const int src0 = 4 * (2 * i) + hB, src1 = 4 * (2 * i + 1) + hB;
+    const int lrow = lane & 7, lsel = lane >> 3;   // ldmatrix row provider
 
-    float m_run[GQ], l_run[GQ], acc[GQ][CPL];
+    int st = 0;
+    for (int k = 0; k < nsub; ++k) {
+        const uint8_t *stage = st ? stg1 : stg0;
+        if (!mbar_wait(&bars[st], (phase >> st) & 1u)) {
+            if (lane == 0) atomicExch(&a.ctl[1], 1);
+            mbar_wait(&bars[st ^ 1], (phase >> (st ^ 1)) & 1u);
+            return false;
+        }
+        phase ^= 1u << st;
+        const __half *krows = reinterpret_cast<const __half *>(stage);
+        const __half *vrows = krows + SUB * RS;
+        const int nvalid = min(SUB, fe - (fb + k * SUB));
+        // scores: rows 0..7 = tokens (rows 8..15 of the A tile are zero)
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        m_run[h] = -CUDART_INF_F;
-        l_run[h] = 0.0f;
+        for (int kt = 0; kt < NKT; kt += 2) {
+            uint32_t a0, a2, b0, b2;   // (kt, lo), (kt, hi), (kt+1, lo), (kt+1, hi)
+            ldsm_x4(a0, a2, b0, b2, krows + lrow * RS + 16 * kt + 8 * lsel);
+            mma16816(d, a0, 0u, a2, 0u, Bq[kt][0], Bq[kt][1]);
+            mma16816(d, b0, 0u, b2, 0u, Bq[kt + 1][0], Bq[kt + 1][1]);
+        }
+        float lg = (r < nvalid && i < GQ) ? d[0] * a.sl2 : -CUDART_INF_F;
+        float mloc = lg;
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
+        const float m_new = fmaxf(m_run, mloc);
+        if (__any_sync(0xffffffffu, m_new > m_run)) {
+            const float alpha = m_new > m_run ? ex2(m_run - m_new) : 1.0f;   // head i = this lane's D columns
+            l_run *= alpha;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[h][c] = 0.0f;
+            for (int mt = 0; mt < NKT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][e] *= alpha;
+            m_run = m_new;
+        }
+        const float pv = ex2(lg - (m_run == -CUDART_INF_F ? 0.0f : m_run));
+        l_run += pv;
+        // B of P.V: tokens 2i, 2i+1 of head r/2, piece r&1
+        const float x0 = __shfl_sync(0xffffffffu, pv, src0), x1 = __shfl_sync(0xffffffffu, pv, src1);
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(hh);
+        const uint32_t bp = hB < GQ ? h2bits(__floats2half2_rn(x0 - pm * hf.x, x1 - pm * hf.y)) : 0u;
+#pragma unroll
+        for (int mt = 0; mt < NKT; mt += 2) {
+            uint32_t a0, a1, b0, b1;   // channels (mt, lo), (mt, hi), (mt+1, lo), (mt+1, hi)
+            ldsm_x4_t(a0, a1, b0, b1, vrows + lrow * RS + 16 * mt + 8 * lsel);
+            mma1688(acc[mt], a0, a1, bp);
+            mma1688(acc[mt + 1], b0, b1, bp);
+        }
+        __syncwarp();
+        fence_async_shared();
+        if (k + 2 < nsub) issue(k + 2, st);
+        st ^= 1;
     }
-    for (int chk = c0; chk < c1; ++chk) {
-        // keep the query rows in shared memory (re-read per chunk) instead of
-        // letting them be hoisted into registers across chunks
-        asm volatile("" ::: "memory");
-        const int f0 = chk * FP16_CHUNK, nvalid = min(FP16_CHUNK, nfp - f0);
-        const bool valid = lane < nvalid;
-        float dot[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
-        {
-            // this lane's token's key row, half a row of loads in flight at a time
-            constexpr int KV = D / 8, KH = KV > 8 ? 8 : KV;
-            const __half *kr = row_of(valid ? f0 + lane : f0, a.rk, a.pk);
-#pragma unroll
-            for (int hb = 0; hb < KV; hb += KH) {
-                uint4 kv[KH];
-#pragma unroll
-                for (int x = 0; x < KH; ++x)
-                    kv[x] = valid ? reinterpret_cast<const uint4 *>(kr)[hb + x] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int x = 0; x < KH; ++x) {
-                    const int c8 = hb + x;
-                    const __half2 *kh = reinterpret_cast<const __half2 *>(&kv[x]);
-                    float kf[8];
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        const float2 f = __half22float2(kh[y]);
-                        kf[2 * y] = f.x;
-                        kf[2 * y + 1] = f.y;
-                    }
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) {
-                        const float4 qa = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[0];
-                        const float4 qb = reinterpret_cast<const float4 *>(qsm + h * D + 8 * c8)[1];
-                        dot[h] = fmaf(qa.x, kf[0], dot[h]);
-                        dot[h] = fmaf(qa.y, kf[1], dot[h]);
-                        dot[h] = fmaf(qa.z, kf[2], dot[h]);
-                        dot[h] = fmaf(qa.w, kf[3], dot[h]);
-                        dot[h] = fmaf(qb.x, kf[4], dot[h]);
-                        dot[h] = fmaf(qb.y, kf[5], dot[h]);
-                        dot[h] = fmaf(qb.z, kf[6], dot[h]);
-                        dot[h] = fmaf(qb.w, kf[7], dot[h]);
-                    }
-                }
-            }
-        }
-        float p[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            const float lg = valid ? dot[h] * a.sl2 : -CUDART_INF_F;
-            float mx = lg;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_new = fmaxf(m_run[h], mx);   // finite: the chunk has >= 1 token
-            const float alpha = ex2(m_run[h] - m_new);
-            l_run[h] *= alpha;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[h][c] *= alpha;
-            m_run[h] = m_new;
-            p[h] = ex2(lg - m_new);
-            l_run[h] += p[h];
-        }
-        // this lane's channels of the value rows, eight tokens' loads in flight at a time
-        using VT = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
-#pragma unroll 1
-        for (int tb = 0; tb < nvalid; tb += 8) {
-            VT vv[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-                vv[x] = (tb + x < nvalid) ? *reinterpret_cast<const VT *>(row_of(f0 + tb + x, a.rv, a.pv) + lane * CPL)
-                                          : VT{};
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                float vf[CPL];
-                if constexpr (CPL == 4) {
-                    const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].x));
-                    const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x].y));
-                    vf[0] = fa.x; vf[1] = fa.y; vf[2] = fb.x; vf[3] = fb.y;
-                } else {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vv[x]));
-                    vf[0] = f.x; vf[1] = f.y;
-                }
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) {
-                    const float pt = __shfl_sync(0xffffffffu, p[h], (tb + x) & 31);
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(pt, vf[c], acc[h][c]);
-                }
-            }
-        }
-    }
+    float l = l_run;
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
     float *pb = a.part + slot * GQ * (D + 2);
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        float l = l_run[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            pb[h * (D + 2) + 0] = m_run[h];
-            pb[h * (D + 2) + 1] = l;
+    if (i < GQ) {
+        if (r == 0) {
+            pb[i * (D + 2) + 0] = m_run;
+            pb[i * (D + 2) + 1] = l;
         }
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) pb[h * (D + 2) + 2 + lane * CPL + c] = acc[h][c];
+        for (int mt = 0; mt < NKT; ++mt) {
+            pb[i * (D + 2) + 2 + 16 * mt + r] = acc[mt][0] + acc[mt][1];
+            pb[i * (D + 2) + 2 + 16 * mt + r + 8] = acc[mt][2] + acc[mt][3];
+        }
     }
-    __syncwarp();
+    return true;
 }
 
 template <int D, int GQ>
@@ -671,7 +701,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
         const int off = (int)(x - ubase);
         if (off < a.Sf) {
             const int end = (int)min(x1 - ubase, (long long)a.Sf);
-            fp16_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 0), u, off, end, qsm, lane);
+            if (!fp16_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars, phase,
+                                     qsm, lane))
+                return;
             x = ubase + end;
         } else {
             const int end = (int)min(x1 - ubase, (long long)a.Iu);
