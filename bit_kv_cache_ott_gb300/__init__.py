@@ -37,7 +37,7 @@ class StateExport(C.Structure):
                 ("bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tk", "tv", "pidx", "pnorm", "pk", "pv")]
 
 
-SYMBOLS = ("ott_create", "ott_destroy", "ott_prefill", "ott_append", "ott_decode_attn",
+SYMBOLS = ("ott_create", "ott_destroy", "ott_prefill", "ott_append", "ott_decode_attn", "ott_decode_attn_static",
            "ott_get_counts", "ott_block_count", "ott_export_state", "ott_check_device",
            "ott_device_bytes", "ott_status_str")
 
@@ -63,6 +63,7 @@ def load(build_if_missing: bool = False):
     L.ott_prefill.argtypes = [P, P, P, i32, P]
     L.ott_append.argtypes = [P, P, P, P]
     L.ott_decode_attn.argtypes = [P, P, P, P]
+    L.ott_decode_attn_static.argtypes = [P, P, P, P]
     L.ott_get_counts.argtypes = [P, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
     L.ott_block_count.argtypes = [P, i32]
     L.ott_export_state.argtypes = [P, i32, i32, C.POINTER(StateExport)]

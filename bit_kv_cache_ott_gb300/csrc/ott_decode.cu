@@ -833,3 +833,114 @@ cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cuda
 }
 
 }  // namespace ott
+
+// ---------------------------------------------------------------- allocation-free decode
+//
+// ott_decode_attn_static: the same two kernels as ott_decode_attn, but the
+// split-K partials go to a fixed array in this module's device global memory
+// instead of memory the library allocates. It is for callers that may not
+// allocate device memory on their decode path: engines that hand all free HBM
+// to their own pool at start-up and forbid any later growth, or latency-
+// critical loops that cannot afford cudaMalloc's implicit synchronization.
+#include <mutex>
+
+namespace ott {
+
+// 32 MiB of split-K partials, created when a GPU loads this library and held
+// by every such GPU until the process exits. All calls share it and it keeps
+// the last call's contents; no part of it needs clearing, because a decode
+// writes every partial it later reads. Calls that overlap on the GPU (other
+// streams, other handles) race on it and must be ordered by the caller.
+constexpr size_t kStaticScratchFloats = (size_t)8 << 20;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+
+namespace {
+
+std::mutex g_static_mu;
+float *g_static_ptr[1024];   // host copy of the array's device address, per device ordinal
+
+// The array's name is only a host-side stand-in in host code: its device
+// address is looked up once per device, with that device current.
+cudaError_t static_scratch_address(int dev, float **out) {
+    if (dev < 0 || dev >= 1024) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_static_ptr[dev];
+    return cudaSuccess;
+}
+
+template <int D, int GQ>
+cudaError_t launch_decode_static_t(const ott_cache *c, const __half *q, __half *out, float *scratch,
+                                   cudaStream_t s) {
+    DecodeArgs a;
+    a.blk = c->blk;
+    a.blk_bytes = c->blk_bytes;
+    a.NB = c->NB;
+    a.rk = c->rk;
+    a.rv = c->rv;
+    a.ring = c->ring;
+    a.pk = c->pk;
+    a.pv = c->pv;
+    a.P = c->P;
+    a.q = q;
+    a.out = out;
+    a.part = scratch;
+    a.ctl = c->ctl;
+    a.Hq = c->Hq;
+    a.Hkv = c->Hkv;
+    a.G = c->G;
+    a.nf = c->nf;
+    a.jfull = (c->P + c->G - 1) / c->G;
+    const long long tail_start = (long long)c->nf * c->G;
+    a.ring_start = (int)(tail_start % c->ring);
+    a.ntail = (int)(c->T - tail_start);
+    a.npool = pool_after(c->P, c->G, c->nf);
+    a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
+    a.Iu = a.Sf + c->nf;
+    a.W = (long long)c->U * a.Iu;
+    a.NWp = c->sm_count * DEC_WARPS;
+    a.MAXU = c->maxu;
+    a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
+    k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = c->B * c->Hq, th = 256, bl = (warps * 32 + th - 1) / th;
+    k_combine<D, GQ><<<bl, th, 0, s>>>(a, c->B);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace ott
+
+extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream) {
+    using namespace ott;
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || c->T < 1) return OTT_ERR_STATE;
+    if (!q || !out || q == out || (reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
+        return OTT_ERR_INVALID;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return OTT_ERR_CUDA;
+    if (dev != c->device) return OTT_ERR_STATE;   // the cache's device must be current
+    const size_t need = (size_t)c->sm_count * DEC_WARPS * c->maxu * 2 * c->gq * (c->d + 2);
+    if (need > kStaticScratchFloats) return OTT_ERR_CAPACITY;
+    float *scratch = nullptr;
+    if (static_scratch_address(dev, &scratch) != cudaSuccess) return OTT_ERR_CUDA;
+    cudaError_t e = cudaErrorInvalidValue;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half *qh = static_cast<const __half *>(q);
+    __half *oh = static_cast<__half *>(out);
+#define OTT_DEC_S(D_, G_) \
+    if (c->d == D_ && c->gq == G_) e = launch_decode_static_t<D_, G_>(c, qh, oh, scratch, s);
+    OTT_DEC_S(128, 1) OTT_DEC_S(128, 2) OTT_DEC_S(128, 4) OTT_DEC_S(64, 1) OTT_DEC_S(64, 2) OTT_DEC_S(64, 4)
+#undef OTT_DEC_S
+    if (e != cudaSuccess) {
+        c->poisoned = 1;
+        return OTT_ERR_CUDA;
+    }
+    return OTT_OK;
+}

@@ -108,6 +108,29 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream);
  */
 int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
 
+/*
+ * The same decode as ott_decode_attn, but allocation-free: it calls no
+ * cudaMalloc, cudaFree or allocating library routine, and it does not use the
+ * split-K scratch that ott_create set aside. Its partial results go to a fixed
+ * 32 MiB array in libott's device global memory, which every GPU that loads
+ * the library holds until the process exits. It serves callers that may not
+ * allocate device memory on their decode path: engines that hand all free
+ * memory to their own pool at start-up and allow no later growth, and
+ * latency-critical loops that cannot afford the implicit synchronization of
+ * an allocation. The paper has no counterpart; this is a deployment variant.
+ *   - The first call on a device looks up the array's device address (with
+ *     the cache's device current); make that first call before any stream
+ *     capture.
+ *   - Every call shares the array. Calls that overlap on the GPU (other
+ *     streams, other handles) race on it; order them (same stream or events).
+ *     Nothing in it needs clearing between calls.
+ * Errors: as ott_decode_attn, plus OTT_ERR_STATE if the cache's device is not
+ * the current device, and OTT_ERR_CAPACITY if this shape's partials
+ * (SMs x 16 warps x (units/warps + 2) x 2 x Hq/Hkv x (d+2) floats) exceed
+ * the array.
+ */
+int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream);
+
 /* Counts (same for every sequence and kv head): tokens seen, blocks (flushes),
  * residual tokens, pool tokens. Host-side, no device access. */
 int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_pool);
