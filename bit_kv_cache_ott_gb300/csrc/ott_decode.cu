@@ -689,6 +689,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
+    // the combine kernel may be scheduled now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t phase = 0;
     // this warp's contiguous range of work items, split into (unit, type) segments
     const int gw = blockIdx.x * DEC_WARPS + warp;
@@ -715,43 +717,111 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     }
 }
 
-// One warp per (sequence, query head): find the partials of its unit (the
-// warps whose ranges overlap the unit's items) and merge them.
+// Merge the partials of each (sequence, query head). A CTA of `cw` warps
+// serves one (b, hq): the candidate segments of its unit -- (warp, item type)
+// pairs of the decode grid whose ranges overlap the unit -- are dealt to the
+// warps, each warp folds its share with an online log-sum-exp merge (loads of
+// four segments in flight at a time), and warp 0 merges the warps' results
+// from shared memory. Launched as a programmatic dependent of k_decode: it
+// starts while the decode grid drains and waits for its results.
+constexpr int COMB_MAXW = 8;
+
 template <int D, int GQ>
-__global__ void k_combine(DecodeArgs a, int B) {
-    constexpr int CPL = D / 32;
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (w >= B * a.Hq) return;
-    const int b = w / a.Hq, hq = w % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
+__global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, int B) {
+    constexpr int CPL = D / 32, GRP = 4;
+    __shared__ float red[COMB_MAXW][D + 2];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
     const long long ub = (long long)u * a.Iu, ue = ub + a.Iu;
     const int wa = warp_of(a.W, a.NWp, ub), wb = warp_of(a.W, a.NWp, ue - 1);
+    const int ncand = 2 * (wb - wa + 1);
     float M = -CUDART_INF_F, L = 0.0f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int ww = wa; ww <= wb; ++ww) {
-            const long long s0 = range_start(a.W, a.NWp, ww), s1 = range_start(a.W, a.NWp, ww + 1);
-            const int uf = (int)(s0 / a.Iu);
+    for (int k0 = wi * GRP; k0 < ncand; k0 += cw * GRP) {
+        const float *ps[GRP];
+        float ms[GRP];
 #pragma unroll
-            for (int type = 0; type < 2; ++type) {
+        for (int g = 0; g < GRP; ++g) {
+            ps[g] = nullptr;
+            ms[g] = -CUDART_INF_F;
+            const int k = k0 + g;
+            if (k < ncand) {
+                const int ww = wa + (k >> 1), type = k & 1;
+                const long long s0 = range_start(a.W, a.NWp, ww), s1 = range_start(a.W, a.NWp, ww + 1);
                 const long long t0 = type ? ub + a.Sf : ub, t1 = type ? ue : ub + a.Sf;
-                if (max(s0, t0) >= min(s1, t1)) continue;   // no overlap
-                const float *ps = a.part + (part_slot(a, ww, u - uf, type) * GQ + h) * (D + 2);
-                const float ms = ps[0];
-                if (pass == 0) {
-                    M = fmaxf(M, ms);
-                } else {
-                    const float wgt = ms == -CUDART_INF_F ? 0.0f : ex2(ms - M);
-                    L = fmaf(wgt, ps[1], L);
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[c] = fmaf(wgt, ps[2 + lane * CPL + c], acc[c]);
+                if (max(s0, t0) < min(s1, t1)) {
+                    ps[g] = a.part + (part_slot(a, ww, u - (int)(s0 / a.Iu), type) * GQ + h) * (D + 2);
+                    ms[g] = ps[g][0];
                 }
             }
+        }
+        float mn = M;
+#pragma unroll
+        for (int g = 0; g < GRP; ++g) mn = fmaxf(mn, ms[g]);
+        if (mn == -CUDART_INF_F) continue;
+        const float so = ex2(M - mn);
+        L *= so;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] *= so;
+#pragma unroll
+        for (int g = 0; g < GRP; ++g) {
+            if (ms[g] == -CUDART_INF_F) continue;
+            const float sn = ex2(ms[g] - mn);
+            L = fmaf(sn, ps[g][1], L);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(sn, ps[g][2 + lane * CPL + c], acc[c]);
+        }
+        M = mn;
+    }
+    if (cw > 1) {
+        if (lane == 0) {
+            red[wi][0] = M;
+            red[wi][1] = L;
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) red[wi][2 + lane * CPL + c] = acc[c];
+        __syncthreads();
+        if (wi != 0) return;
+        M = -CUDART_INF_F;
+        for (int x = 0; x < cw; ++x) M = fmaxf(M, red[x][0]);
+        L = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
+        for (int x = 0; x < cw; ++x) {
+            const float mx = red[x][0];
+            if (mx == -CUDART_INF_F) continue;
+            const float sx = ex2(mx - M);
+            L = fmaf(sx, red[x][1], L);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(sx, red[x][2 + lane * CPL + c], acc[c]);
         }
     }
     __half *o = a.out + ((size_t)b * a.Hq + hq) * D + lane * CPL;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) o[c] = __float2half_rn(acc[c] / L);
+}
+
+// Launch the combine as a programmatic dependent of the decode grid just
+// queued on stream s: one CTA per (sequence, query head).
+template <int D, int GQ>
+cudaError_t launch_combine(const DecodeArgs &a, int B, cudaStream_t s) {
+    // candidate segments per unit: about 2 * (warps covering a unit)
+    const long long per_unit_warps = (a.NWp + (a.W / a.Iu) - 1) / (a.W / a.Iu) + 1;
+    int cw = (int)((2 * per_unit_warps + 4 * 4 - 1) / (4 * 4));
+    cw = cw < 1 ? 1 : (cw > COMB_MAXW ? COMB_MAXW : cw);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * a.Hq));
+    cfg.blockDim = dim3((unsigned)(32 * cw));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ>, a, B);
 }
 
 template <int D, int GQ>
@@ -788,9 +858,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cu
     k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int warps = c->B * c->Hq, th = 256, bl = (warps * 32 + th - 1) / th;
-    k_combine<D, GQ><<<bl, th, 0, s>>>(a, c->B);
-    return cudaGetLastError();
+    return launch_combine<D, GQ>(a, c->B, s);
 }
 
 template <int D, int GQ>
@@ -909,9 +977,7 @@ cudaError_t launch_decode_static_t(const ott_cache *c, const __half *q, __half *
     k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int warps = c->B * c->Hq, th = 256, bl = (warps * 32 + th - 1) / th;
-    k_combine<D, GQ><<<bl, th, 0, s>>>(a, c->B);
-    return cudaGetLastError();
+    return launch_combine<D, GQ>(a, c->B, s);
 }
 
 }  // namespace
