@@ -694,6 +694,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     uint32_t phase = 0;
     // this warp's contiguous range of work items, split into (unit, type) segments
     const int gw = blockIdx.x * DEC_WARPS + warp;
+    if (gw >= a.NWp) return;
     long long x = range_start(a.W, a.NWp, gw);
     const long long x1 = range_start(a.W, a.NWp, gw + 1);
     const int u_first = (int)(x / a.Iu);
@@ -852,7 +853,8 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cu
     a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
     a.Iu = a.Sf + c->nf;
     a.W = (long long)c->U * a.Iu;
-    a.NWp = c->sm_count * DEC_WARPS;
+    // never more active warps than items: every active warp owns >= 1 item
+    a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
     a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
     k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
@@ -971,7 +973,8 @@ cudaError_t launch_decode_static_t(const ott_cache *c, const __half *q, __half *
     a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
     a.Iu = a.Sf + c->nf;
     a.W = (long long)c->U * a.Iu;
-    a.NWp = c->sm_count * DEC_WARPS;
+    // never more active warps than items: every active warp owns >= 1 item
+    a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
     a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
     k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);

@@ -33,7 +33,8 @@ def decode_bytes_per_unit(T: int, d: int, g: int, G: int, R: int, P: int) -> int
     npool = pool_size(T, G, R, P)
     nq = nf * G - npool
     tail = T - nf * G
-    nonempty = sum(1 for j in range(nf) if block_count(j, G, P) > 0)
+    # block j is empty exactly when the pool absorbs its whole group: (j+1)G <= P
+    nonempty = nf - min(nf, P // G)
     return (2 * nq * d // 4 + nonempty * d * 4 + nq * (d // 32) * 4
             + (tail + npool) * d * 4 + g * d * 4)
 

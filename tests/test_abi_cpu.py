@@ -61,3 +61,20 @@ def test_status_strings_and_null_handles(libott):
     assert libott.ott_create(1, 1, 1, 96, 128, 32, 32, 100, C.byref(out)) == -1    # d = 96
     assert libott.ott_create(1, 2, 4, 128, 128, 32, 32, 100, C.byref(out)) == -1   # Hq < Hkv
     assert libott.ott_create(1, 1, 1, 128, 0, 32, 32, 100, C.byref(out)) == -1     # G = 0
+
+
+def test_decode_bytes_formula():
+    """The closed-form byte count against a direct per-block sum, and the
+    hand-computed figure per unit at T = 4096, G = 128, R = 32, P = 32, d = 128:
+    3936 quantized tokens x 80 B (codes and value scale/zero) + 31 blocks x
+    512 B (key scale/zero) + 160 fp16 tokens x 512 B + 512 B (query, output)
+    = 413,184 B."""
+    from bit_kv_cache_ott_gb300 import metrics
+    assert metrics.decode_bytes_per_unit(4096, 128, 1, 128, 32, 32) == 413184
+    for T, G, R, P in [(300, 16, 4, 40), (1000, 32, 0, 200), (77, 8, 3, 0), (5000, 128, 32, 64)]:
+        nf = metrics.flush_count(T, G, R)
+        npool = metrics.pool_size(T, G, R, P)
+        nq = nf * G - npool
+        nonempty = sum(1 for j in range(nf) if metrics.block_count(j, G, P) > 0)
+        direct = (nq * 128 // 4) * 2 + nonempty * 128 * 4 + nq * 4 * 4 + (T - nf * G + npool) * 128 * 4 + 128 * 4
+        assert metrics.decode_bytes_per_unit(T, 128, 1, G, R, P) == direct
