@@ -722,21 +722,30 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
 // serves one (b, hq): the candidate segments of its unit -- (warp, item type)
 // pairs of the decode grid whose ranges overlap the unit -- are dealt to the
 // warps, each warp folds its share with an online log-sum-exp merge (loads of
-// four segments in flight at a time), and warp 0 merges the warps' results
-// from shared memory. Launched as a programmatic dependent of k_decode: it
-// starts while the decode grid drains and waits for its results.
-constexpr int COMB_MAXW = 8;
+// COMB_GRP segments in flight at a time), and warp 0 merges the warps'
+// results from shared memory. `cw` is chosen so that each warp needs about
+// two rounds: a unit that many decode warps cover (long sequences, few kv
+// heads) gets up to 32 combine warps. Launched as a programmatic dependent of
+// k_decode: it starts while the decode grid drains and waits for its results.
+constexpr int COMB_MAXW = 32;
+constexpr int COMB_GRP = 8;     // candidate segments a warp loads at a time
 
 template <int D, int GQ>
-__global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, int B) {
-    constexpr int CPL = D / 32, GRP = 4;
+__global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
+    constexpr int CPL = D / 32, GRP = COMB_GRP;
     __shared__ float red[COMB_MAXW][D + 2];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
-    const long long ub = (long long)u * a.Iu, ue = ub + a.Iu;
-    const int wa = warp_of(a.W, a.NWp, ub), wb = warp_of(a.W, a.NWp, ue - 1);
-    const int ncand = 2 * (wb - wa + 1);
+    // The unit's items are [ub, ub + Sf) fp16 then [ub + Sf, ue) quantized; the
+    // decode warps holding them are contiguous ranges [f0, f1] and [q0, q1].
+    // Only the first of them can have started in an earlier unit.
+    const long long ub = (long long)u * a.Iu, ue = ub + a.Iu, um = ub + a.Sf;
+    const int wa = warp_of(a.W, a.NWp, ub);
+    const int f1 = a.Sf > 0 ? warp_of(a.W, a.NWp, um - 1) : wa - 1;
+    const int q0 = um < ue ? warp_of(a.W, a.NWp, um) : 0, q1 = um < ue ? warp_of(a.W, a.NWp, ue - 1) : -1;
+    const int n0 = f1 - wa + 1, ncand = n0 + (q1 - q0 + 1);
+    const int uo_a = u - (int)(range_start(a.W, a.NWp, wa) / a.Iu);   // unit offset within warp wa's slots
     float M = -CUDART_INF_F, L = 0.0f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
@@ -749,13 +758,11 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, int B)
             ms[g] = -CUDART_INF_F;
             const int k = k0 + g;
             if (k < ncand) {
-                const int ww = wa + (k >> 1), type = k & 1;
-                const long long s0 = range_start(a.W, a.NWp, ww), s1 = range_start(a.W, a.NWp, ww + 1);
-                const long long t0 = type ? ub + a.Sf : ub, t1 = type ? ue : ub + a.Sf;
-                if (max(s0, t0) < min(s1, t1)) {
-                    ps[g] = a.part + (part_slot(a, ww, u - (int)(s0 / a.Iu), type) * GQ + h) * (D + 2);
-                    ms[g] = ps[g][0];
-                }
+                const int type = k < n0 ? 0 : 1;
+                const int ww = type ? q0 + (k - n0) : wa + k;
+                const int uo = ww == wa ? uo_a : 0;
+                ps[g] = a.part + (part_slot(a, ww, uo, type) * GQ + h) * (D + 2);
+                ms[g] = ps[g][0];
             }
         }
         float mn = M;
@@ -810,7 +817,7 @@ template <int D, int GQ>
 cudaError_t launch_combine(const DecodeArgs &a, int B, cudaStream_t s) {
     // candidate segments per unit: about 2 * (warps covering a unit)
     const long long per_unit_warps = (a.NWp + (a.W / a.Iu) - 1) / (a.W / a.Iu) + 1;
-    int cw = (int)((2 * per_unit_warps + 4 * 4 - 1) / (4 * 4));
+    int cw = (int)((2 * per_unit_warps + 2 * COMB_GRP - 1) / (2 * COMB_GRP));   // about two rounds per warp
     cw = cw < 1 ? 1 : (cw > COMB_MAXW ? COMB_MAXW : cw);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * a.Hq));
@@ -822,7 +829,7 @@ cudaError_t launch_combine(const DecodeArgs &a, int B, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ>, a, B);
+    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ>, a);
 }
 
 template <int D, int GQ>
