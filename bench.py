@@ -365,7 +365,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-units", type=int, default=64)
-    ap.add_argument("--oracle-steps", type=int, default=8)
+    ap.add_argument("--oracle-steps", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
