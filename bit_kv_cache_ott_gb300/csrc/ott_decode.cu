@@ -692,8 +692,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     // the combine kernel may be scheduled now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t phase = 0;
-    // this warp's contiguous range of work items, split into (unit, type) segments
-    const int gw = blockIdx.x * DEC_WARPS + warp;
+    // this warp's contiguous range of work items, split into (unit, type)
+    // segments; warp indices are dealt across the CTAs first, so that with
+    // fewer active warps than slots every SM still gets its share
+    const int gw = warp * gridDim.x + blockIdx.x;
     if (gw >= a.NWp) return;
     long long x = range_start(a.W, a.NWp, gw);
     const long long x1 = range_start(a.W, a.NWp, gw + 1);
@@ -734,7 +736,6 @@ template <int D, int GQ>
 __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
     constexpr int CPL = D / 32, GRP = COMB_GRP;
     __shared__ float red[COMB_MAXW][D + 2];
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
     // The unit's items are [ub, ub + Sf) fp16 then [ub + Sf, ue) quantized; the
@@ -746,6 +747,9 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
     const int q0 = um < ue ? warp_of(a.W, a.NWp, um) : 0, q1 = um < ue ? warp_of(a.W, a.NWp, ue - 1) : -1;
     const int n0 = f1 - wa + 1, ncand = n0 + (q1 - q0 + 1);
     const int uo_a = u - (int)(range_start(a.W, a.NWp, wa) / a.Iu);   // unit offset within warp wa's slots
+    // everything above depends on the arguments only; the partials are the
+    // decode grid's results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float M = -CUDART_INF_F, L = 0.0f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
