@@ -138,6 +138,9 @@ struct Cfg {
     static constexpr bool COOP = GQ <= 2;          // per-block constants computed cooperatively
     static constexpr int QHL = COOP ? GQ * 2 * (D + 8) * 2 : 0;   // hi/lo staging bytes
     static constexpr int WARP_SMEM = 2 * STAGE + 16 + GQ * D * 4 + QHL;
+    // the fp16 path stages 8 key and 8 value rows of d+8 halves in each of
+    // the same two stage buffers
+    static_assert(2 * 8 * (D + 8) * 2 <= STAGE, "fp16 sub-tile staging must fit a stage buffer");
 };
 
 __device__ __forceinline__ int block_cnt(const DecodeArgs &a, int j) {
