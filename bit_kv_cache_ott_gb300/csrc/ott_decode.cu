@@ -148,11 +148,25 @@ __device__ __forceinline__ int block_cnt(const DecodeArgs &a, int j) {
 }
 
 // First item of warp w's range (items are split as evenly as integers allow).
-__device__ __forceinline__ long long range_start(long long W, int NWp, long long w) { return w * W / NWp; }
+// The quotients are exact either way; 32-bit division is several times
+// cheaper than 64-bit and covers every realistic size.
+__device__ __forceinline__ long long range_start(long long W, int NWp, long long w) {
+    const unsigned long long num = (unsigned long long)w * (unsigned long long)W;
+    if (num <= 0xffffffffull) return (long long)((unsigned)num / (unsigned)NWp);
+    return (long long)(num / (unsigned long long)NWp);
+}
 
 // The warp whose range holds item x.
 __device__ __forceinline__ int warp_of(long long W, int NWp, long long x) {
-    return (int)(((x + 1) * NWp + W - 1) / W - 1);
+    const unsigned long long num = (unsigned long long)(x + 1) * (unsigned long long)NWp + (unsigned long long)W - 1;
+    if (num <= 0xffffffffull) return (int)((unsigned)num / (unsigned)W) - 1;
+    return (int)(num / (unsigned long long)W) - 1;
+}
+
+// Unit of item x (x < W).
+__device__ __forceinline__ int unit_of(long long x, int Iu) {
+    if ((unsigned long long)x <= 0xffffffffull) return (int)((unsigned)x / (unsigned)Iu);
+    return (int)(x / Iu);
 }
 
 __device__ __forceinline__ size_t part_slot(const DecodeArgs &a, int w, int unit_off, int type) {
@@ -702,9 +716,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     if (gw >= a.NWp) return;
     long long x = range_start(a.W, a.NWp, gw);
     const long long x1 = range_start(a.W, a.NWp, gw + 1);
-    const int u_first = (int)(x / a.Iu);
+    const int u_first = unit_of(x, a.Iu);
     while (x < x1) {
-        const int u = (int)(x / a.Iu);
+        const int u = unit_of(x, a.Iu);
         const long long ubase = (long long)u * a.Iu;
         const int off = (int)(x - ubase);
         if (off < a.Sf) {
@@ -749,7 +763,7 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
     const int f1 = a.Sf > 0 ? warp_of(a.W, a.NWp, um - 1) : wa - 1;
     const int q0 = um < ue ? warp_of(a.W, a.NWp, um) : 0, q1 = um < ue ? warp_of(a.W, a.NWp, ue - 1) : -1;
     const int n0 = f1 - wa + 1, ncand = n0 + (q1 - q0 + 1);
-    const int uo_a = u - (int)(range_start(a.W, a.NWp, wa) / a.Iu);   // unit offset within warp wa's slots
+    const int uo_a = u - unit_of(range_start(a.W, a.NWp, wa), a.Iu);   // unit offset within warp wa's slots
     // everything above depends on the arguments only; the partials are the
     // decode grid's results
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -871,7 +885,10 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cu
     a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
     a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
-    k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
+    // CTAs only as wide as the active warps need: with few items, the SMs keep
+    // room for the combine's CTAs, which then start while the decode drains
+    const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
+    k_decode<D, GQ><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ>(a, c->B, s);
@@ -991,7 +1008,10 @@ cudaError_t launch_decode_static_t(const ott_cache *c, const __half *q, __half *
     a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
     a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
-    k_decode<D, GQ><<<c->sm_count, DEC_WARPS * 32, Cfg<D, GQ>::WARP_SMEM * DEC_WARPS, s>>>(a);
+    // CTAs only as wide as the active warps need: with few items, the SMs keep
+    // room for the combine's CTAs, which then start while the decode drains
+    const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
+    k_decode<D, GQ><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ>(a, c->B, s);
