@@ -54,6 +54,7 @@ def lib():
             L.orc_destroy.argtypes = [P]
             L.orc_append.argtypes = [P, P, P]
             L.orc_prefill.argtypes = [P, P, P, i32]
+            L.orc_prefill_lens.argtypes = [P, P, P, P, i32]
             L.orc_decode.argtypes = [P, P, P]
             L.orc_decode_head.argtypes = [P, i32, i32, P, P]
             L.orc_counts.argtypes = [P, i32, P, P, P, P]
@@ -150,6 +151,18 @@ class OracleCache:
         rc = lib().orc_prefill(self._h, _ptr(Kb), _ptr(Vb), L)
         if rc:
             raise RuntimeError("prefill on a non-empty oracle cache")
+
+    def prefill_lens(self, K, V, lens):
+        """Ragged prefill: K, V fp16 [B][Hkv][Lmax][d]; sequence b takes its
+        first lens[b] tokens."""
+        Kb, Vb = _bits(K), _bits(V)
+        Lmax = Kb.shape[2]
+        ln = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+        if ln.shape != (self.B,):
+            raise ValueError("lens must hold one length per sequence")
+        rc = lib().orc_prefill_lens(self._h, _ptr(Kb), _ptr(Vb), _ptr(ln), Lmax)
+        if rc:
+            raise RuntimeError("ragged prefill rejected (non-empty cache or bad lengths)")
 
     def append(self, k, v):
         """k, v: fp16 [B][Hkv][d]."""

@@ -44,6 +44,11 @@
  *  R8  Pool and residual tokens keep their fp16 values ("full precision").
  *  R9  Decode attends over every token seen, with scale 1/sqrt(d); query
  *      head h reads kv head h / (Hq / Hkv).
+ *  R10 Batches may be ragged: each sequence keeps its own token count (a
+ *      prefill may give every sequence its own length), an append adds one
+ *      token to every sequence, and R1 applies to each unit on its own. The
+ *      pages state the method for one sequence; this is that method applied
+ *      to each sequence of a batch independently.
  *
  * Floating point: decisions that yield integers or stored bits (norms,
  * scales, zeros, codes) are taken in fp32 exactly as the library takes them.
@@ -210,7 +215,8 @@ typedef struct {
 
 typedef struct {
     int B, Hq, Hkv, d, G, R, P;
-    long long T;
+    long long T;        /* appends plus the longest prefill (0: empty) */
+    long long *Tb;      /* [B] tokens seen by each sequence (R10) */
     orc_unit *u;        /* [B*Hkv] */
 } orc_cache;
 
@@ -251,6 +257,7 @@ void orc_destroy(void *hp)
         free(u->blk);
     }
     free(h->u);
+    free(h->Tb);
     free(h);
 }
 
@@ -262,6 +269,7 @@ void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
     orc_cache *h = (orc_cache *)calloc(1, sizeof(orc_cache));
     h->B = B; h->Hq = Hq; h->Hkv = Hkv; h->d = d; h->G = G; h->R = R; h->P = P;
     h->u = (orc_unit *)calloc((size_t)B * Hkv, sizeof(orc_unit));
+    h->Tb = (long long *)calloc((size_t)B, sizeof(long long));
     for (int i = 0; i < B * Hkv; ++i) {
         orc_unit *u = &h->u[i];
         u->tail_cap = G + R;
@@ -379,7 +387,9 @@ int orc_append(void *hp, const uint16_t *k, const uint16_t *v)
     orc_cache *h = (orc_cache *)hp;
     const int U = h->B * h->Hkv;
     for (int i = 0; i < U; ++i)
-        append_unit(h, &h->u[i], h->T, k + (size_t)i * h->d, v + (size_t)i * h->d);
+        append_unit(h, &h->u[i], h->Tb[i / h->Hkv], k + (size_t)i * h->d, v + (size_t)i * h->d);
+    for (int b = 0; b < h->B; ++b)
+        h->Tb[b] += 1;
     h->T += 1;
     return 0;
 }
@@ -396,6 +406,34 @@ int orc_prefill(void *hp, const uint16_t *K, const uint16_t *V, int L)
             append_unit(h, &h->u[i], t, K + ((size_t)i * L + t) * d,
                         V + ((size_t)i * L + t) * d);
     h->T = L;
+    for (int b = 0; b < h->B; ++b)
+        h->Tb[b] = L;
+    return 0;
+}
+
+/* R10. K, V: fp16 bits [B][Hkv][Lmax][d]; sequence b takes its first
+ * lens[b] tokens (0 <= lens[b] <= Lmax); only on an empty cache. */
+int orc_prefill_lens(void *hp, const uint16_t *K, const uint16_t *V, const int32_t *lens, int Lmax)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (h->T != 0 || Lmax < 0)
+        return -2;
+    for (int b = 0; b < h->B; ++b)
+        if (lens[b] < 0 || lens[b] > Lmax)
+            return -1;
+    const int U = h->B * h->Hkv, d = h->d;
+    long long longest = 0;
+    for (int i = 0; i < U; ++i) {
+        const int L = lens[i / h->Hkv];
+        for (int t = 0; t < L; ++t)
+            append_unit(h, &h->u[i], t, K + ((size_t)i * Lmax + t) * d,
+                        V + ((size_t)i * Lmax + t) * d);
+    }
+    for (int b = 0; b < h->B; ++b) {
+        h->Tb[b] = lens[b];
+        longest = lens[b] > longest ? lens[b] : longest;
+    }
+    h->T = longest;
     return 0;
 }
 
@@ -408,12 +446,12 @@ int orc_prefill(void *hp, const uint16_t *K, const uint16_t *V, int L)
 int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
 {
     orc_cache *h = (orc_cache *)hp;
-    if (h->T < 1 || b < 0 || b >= h->B || hq < 0 || hq >= h->Hq)
+    if (b < 0 || b >= h->B || hq < 0 || hq >= h->Hq || h->Tb[b] < 1)
         return -2;
     const int d = h->d, ng = d / 32;
     const orc_unit *u = &h->u[b * h->Hkv + hq / (h->Hq / h->Hkv)];
     const double sigma = 1.0 / sqrt((double)d);
-    const long long n = h->T;
+    const long long n = h->Tb[b];
     double *score = (double *)malloc(sizeof(double) * n);
     double *q = (double *)malloc(sizeof(double) * d);
     for (int c = 0; c < d; ++c)
@@ -494,8 +532,9 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
 int orc_decode(void *hp, const uint16_t *q, double *out)
 {
     orc_cache *h = (orc_cache *)hp;
-    if (h->T < 1)
-        return -2;
+    for (int b = 0; b < h->B; ++b)
+        if (h->Tb[b] < 1)
+            return -2;
     for (int b = 0; b < h->B; ++b)
         for (int hq = 0; hq < h->Hq; ++hq) {
             size_t o = ((size_t)b * h->Hq + hq) * h->d;
@@ -511,7 +550,7 @@ int orc_decode(void *hp, const uint16_t *q, double *out)
 void orc_counts(void *hp, int u, long long *T, int *nf, int *tail, int *npool)
 {
     orc_cache *h = (orc_cache *)hp;
-    *T = h->T;
+    *T = h->Tb[u / h->Hkv];
     *nf = h->u[u].nb;
     *tail = h->u[u].tail_n;
     *npool = h->u[u].pool_n;

@@ -313,3 +313,43 @@ def test_decode_is_softmax_attention_over_three_stores(oracle_mod, d, G, R, P, T
         kh, vh = dequantized_tokens(o.export_unit(h // g), d)
         ref = _torch_attention(q[0, h:h + 1], kh[None], vh[None], 1, 1)[0]
         assert np.max(np.abs(out[h] - ref)) < 1e-11
+
+
+def test_ragged_batch_is_independent_sequences(oracle_mod):
+    """Reading R10: a ragged batch (per-sequence prefill lengths, then appends
+    to every sequence) is each sequence's cache side by side. Sequence b's
+    state and decode output equal a one-sequence oracle fed only its own
+    lens[b] tokens and then the same appends -- through flushes that happen
+    at different steps for different sequences."""
+    B, Hq, Hkv, d, G, R, P = 4, 4, 2, 32, 8, 3, 5
+    lens = [1, 9, 23, 40]       # before the first flush, around it, several flushes
+    Lmax = max(lens)
+    rng = np.random.default_rng(11)
+    K = rng.standard_normal((B, Hkv, Lmax, d)).astype(np.float16)
+    V = rng.standard_normal((B, Hkv, Lmax, d)).astype(np.float16)
+    rag = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    rag.prefill_lens(K, V, lens)
+    solo = []
+    for b in range(B):
+        o = oracle_mod.OracleCache(1, Hq, Hkv, d, G, R, P)
+        o.prefill(np.ascontiguousarray(K[b:b + 1, :, :lens[b]]), np.ascontiguousarray(V[b:b + 1, :, :lens[b]]))
+        solo.append(o)
+    for step in range(25):
+        k = rng.standard_normal((B, Hkv, d)).astype(np.float16)
+        v = rng.standard_normal((B, Hkv, d)).astype(np.float16)
+        q = rng.standard_normal((B, Hq, d)).astype(np.float16)
+        rag.append(k, v)
+        out = rag.decode(q)
+        for b in range(B):
+            solo[b].append(np.ascontiguousarray(k[b:b + 1]), np.ascontiguousarray(v[b:b + 1]))
+            np.testing.assert_array_equal(out[b], solo[b].decode(np.ascontiguousarray(q[b:b + 1]))[0])
+            for h in range(Hkv):
+                assert rag.counts(b * Hkv + h) == solo[b].counts(h)
+                e_r, e_s = rag.export_unit(b * Hkv + h), solo[b].export_unit(h)
+                for key in e_s:
+                    np.testing.assert_array_equal(e_r[key], e_s[key], err_msg=f"step {step} seq {b} {key}")
+    with pytest.raises(RuntimeError):
+        rag.prefill_lens(K, V, lens)                       # only on an empty cache
+    bad = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    with pytest.raises(RuntimeError):
+        bad.prefill_lens(K, V, [1, 2, 3, Lmax + 1])       # a length beyond the staged tokens
