@@ -37,9 +37,9 @@ class StateExport(C.Structure):
                 ("bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tk", "tv", "pidx", "pnorm", "pk", "pv")]
 
 
-SYMBOLS = ("ott_create", "ott_destroy", "ott_prefill", "ott_append", "ott_decode_attn", "ott_decode_attn_static",
-           "ott_get_counts", "ott_block_count", "ott_export_state", "ott_check_device",
-           "ott_device_bytes", "ott_status_str")
+SYMBOLS = ("ott_create", "ott_create_ragged", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
+           "ott_decode_attn", "ott_decode_attn_static", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
+           "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str")
 
 
 def lib_path() -> str:
@@ -59,12 +59,15 @@ def load(build_if_missing: bool = False):
     L = C.CDLL(_LIB_PATH)
     P, i32, i64 = C.c_void_p, C.c_int, C.c_longlong
     L.ott_create.argtypes = [i32] * 8 + [C.POINTER(P)]
+    L.ott_create_ragged.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_destroy.argtypes = [P]
     L.ott_prefill.argtypes = [P, P, P, i32, P]
+    L.ott_prefill_lens.argtypes = [P, P, P, C.POINTER(i32), i32, P]
     L.ott_append.argtypes = [P, P, P, P]
     L.ott_decode_attn.argtypes = [P, P, P, P]
     L.ott_decode_attn_static.argtypes = [P, P, P, P]
     L.ott_get_counts.argtypes = [P, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
+    L.ott_get_seq_counts.argtypes = [P, i32, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
     L.ott_block_count.argtypes = [P, i32]
     L.ott_export_state.argtypes = [P, i32, i32, C.POINTER(StateExport)]
     L.ott_check_device.argtypes = [P]
@@ -99,14 +102,19 @@ def _stream(stream) -> int:
 
 
 class OTTCache:
-    """One OTT cache (one attention layer): ``create/prefill/append/decode_attn/destroy``."""
+    """One OTT cache (one attention layer): ``create/prefill/append/decode_attn/destroy``.
+    ``ragged=True`` creates it with ``ott_create_ragged`` so that ``prefill_lens``
+    can give every sequence its own length."""
 
-    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192):
+    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False):
         L = load()
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
         self.max_tokens = max_tokens
+        self.ragged = ragged
         h = C.c_void_p()
-        _check(L.ott_create(B, Hq, Hkv, d, G, R, P, max_tokens, C.byref(h)), "ott_create")
+        create = L.ott_create_ragged if ragged else L.ott_create
+        _check(create(B, Hq, Hkv, d, G, R, P, max_tokens, C.byref(h)),
+               "ott_create_ragged" if ragged else "ott_create")
         self._h = h
 
     def close(self):
@@ -136,6 +144,16 @@ class OTTCache:
         _check(load().ott_prefill(self._h, _dev_ptr(K, shp, "K"), _dev_ptr(V, shp, "V"), Lq,
                                   _stream(stream)), "ott_prefill")
 
+    def prefill_lens(self, K: torch.Tensor, V: torch.Tensor, lens, stream=None):
+        """Ragged prefill: K, V [B][Hkv][Lmax][d]; sequence b takes its first lens[b] tokens."""
+        Lmax = K.shape[2] if K.dim() == 4 else -1
+        shp = (self.B, self.Hkv, Lmax, self.d)
+        ln = (C.c_int * self.B)(*[int(x) for x in lens])
+        if len(lens) != self.B:
+            raise ValueError("lens must hold one length per sequence")
+        _check(load().ott_prefill_lens(self._h, _dev_ptr(K, shp, "K"), _dev_ptr(V, shp, "V"), ln, Lmax,
+                                       _stream(stream)), "ott_prefill_lens")
+
     def append(self, k: torch.Tensor, v: torch.Tensor, stream=None):
         shp = (self.B, self.Hkv, self.d)
         _check(load().ott_append(self._h, _dev_ptr(k, shp, "k"), _dev_ptr(v, shp, "v"),
@@ -155,6 +173,12 @@ class OTTCache:
                "ott_get_counts")
         return T.value, nf.value, tail.value, npool.value
 
+    def seq_counts(self, b: int):
+        T, nf, tail, npool = C.c_longlong(), C.c_int(), C.c_int(), C.c_int()
+        _check(load().ott_get_seq_counts(self._h, b, C.byref(T), C.byref(nf), C.byref(tail), C.byref(npool)),
+               "ott_get_seq_counts")
+        return T.value, nf.value, tail.value, npool.value
+
     def block_count(self, j: int) -> int:
         rc = load().ott_block_count(self._h, j)
         if rc < 0:
@@ -168,10 +192,11 @@ class OTTCache:
         _check(load().ott_check_device(self._h), "ott_check_device")
 
     def export_state(self, u0: int = 0, nu: int | None = None) -> dict:
-        """Canonical host arrays of units [u0, u0+nu) (numpy)."""
+        """Canonical host arrays of units [u0, u0+nu) (numpy). In a ragged
+        batch the units must belong to one sequence."""
         import numpy as np
         nu = self.B * self.Hkv - u0 if nu is None else nu
-        T, nf, nt, npool = self.counts()
+        T, nf, nt, npool = self.seq_counts(u0 // self.Hkv)
         G, P, d = self.G, self.P, self.d
         e = dict(
             bidx=np.zeros((nu, nf, G), np.int32),

@@ -29,6 +29,13 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Flush needed after T tokens with nf flushes done?
 bool flush_due(const ott_cache *c) { return c->T - (long long)c->nf * c->G >= (long long)c->G + c->R; }
+bool flush_due_seq(const ott_cache *c, int b) {
+    return c->Tb[b] - (long long)c->nfb[b] * c->G >= (long long)c->G + c->R;
+}
+int flushes_after(const ott_cache *c, long long T) { return T >= c->G + c->R ? (int)((T - c->R) / c->G) : 0; }
+
+int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
+                 ott_cache **out);
 
 }  // namespace
 
@@ -48,6 +55,23 @@ const char *ott_status_str(int code) {
 }
 
 int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, out);
+}
+
+int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
+    if (B > RAGGED_MAX) {
+        if (out) *out = nullptr;
+        return OTT_ERR_INVALID;
+    }
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 1, out);
+}
+
+}  // extern "C"
+
+namespace {
+
+int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
+                 ott_cache **out) {
     if (!out) return OTT_ERR_INVALID;
     *out = nullptr;
     if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
@@ -81,6 +105,20 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_token
     // (at most W/NW + 1 items) touches at most U/NW + 2 units
     const int nwarps = sms * DEC_WARPS;
     c->maxu = (int)((long long)B * Hkv / nwarps) + 2;
+    // ragged batches: units differ in length, so a range of L items can touch
+    // up to L units; L <= ceil(W_max / warps) with at most NB blocks and
+    // ceil((G + R + P) / 32) fp16 items per unit
+    c->ragged_capable = ragged;
+    c->ragged = 0;
+    c->maxu_r = 0;
+    if (ragged) {
+        const long long iu_max = (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + (long long)c->NB;
+        const long long w_max = (long long)B * Hkv * iu_max;
+        c->maxu_r = (int)((w_max + nwarps - 1) / nwarps) + 2;
+        c->Tb.assign(B, 0);
+        c->nfb.assign(B, 0);
+    }
+    const int maxu_alloc = c->maxu > c->maxu_r ? c->maxu : c->maxu_r;
 
     const size_t U = (size_t)c->U;
     const size_t sz_blk = U * c->NB * (size_t)c->blk_bytes;
@@ -88,7 +126,7 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_token
     const size_t sz_ring = U * c->ring * (size_t)d * 2;
     const size_t sz_pool = U * (size_t)P * d * 2;
     const size_t sz_pn = U * (size_t)P * 4;
-    const size_t sz_part = (size_t)nwarps * c->maxu * 2 * gq * (d + 2) * 4;
+    const size_t sz_part = (size_t)nwarps * maxu_alloc * 2 * gq * (d + 2) * 4;
     size_t off = 0;
     const size_t o_blk = off; off = round_up(off + sz_blk, 256);
     const size_t o_bidx = off; off = round_up(off + sz_bidx, 256);
@@ -140,6 +178,10 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_token
     return OTT_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 int ott_destroy(ott_cache *c) {
     if (!c) return OTT_OK;
     cudaError_t e = cudaDeviceSynchronize();
@@ -172,12 +214,80 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     return OTT_OK;
 }
 
+int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens, int Lmax, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (!c->ragged_capable || c->poisoned || c->T != 0) return OTT_ERR_STATE;
+    if (!lens || Lmax < 1 || !K || !V || !aligned16(K) || !aligned16(V)) return OTT_ERR_INVALID;
+    if (Lmax > c->max_tokens) return OTT_ERR_CAPACITY;
+    int nf_max = 0;
+    for (int b = 0; b < c->B; ++b) {
+        if (lens[b] < 1 || lens[b] > Lmax) return OTT_ERR_INVALID;
+        const int nf = flushes_after(c, lens[b]);
+        nf_max = nf > nf_max ? nf : nf_max;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
+    // group j of every sequence that has one, in token order
+    for (int j = 0; j < nf_max; ++j) {
+        FlushList fl;
+        fl.n = 0;
+        for (int b = 0; b < c->B; ++b)
+            if (flushes_after(c, lens[b]) > j) {
+                fl.lb[fl.n] = b;
+                fl.lj[fl.n] = j;
+                ++fl.n;
+            }
+        cudaError_t e = launch_flush_list(c, Kh, Vh, (long long)Lmax * c->d, LLONG_MAX, fl, s);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
+    long long Tmax = 0;
+    for (int b = 0; b < c->B; ++b) {
+        const int nf = flushes_after(c, lens[b]);
+        cudaError_t e = launch_copy_tail_units(c, Kh, Vh, b * c->Hkv, c->Hkv, Lmax, (long long)nf * c->G,
+                                               lens[b], s);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+        c->Tb[b] = lens[b];
+        c->nfb[b] = nf;
+        Tmax = lens[b] > Tmax ? lens[b] : Tmax;
+    }
+    c->ragged = 1;
+    c->T = Tmax;
+    c->nf = 0;
+    return OTT_OK;
+}
+
+namespace {
+
+int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+    cudaError_t e = launch_append_ragged(c, k, v, s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    FlushList fl;
+    fl.n = 0;
+    for (int b = 0; b < c->B; ++b) {
+        c->Tb[b] += 1;
+        if (flush_due_seq(c, b)) {
+            fl.lb[fl.n] = b;
+            fl.lj[fl.n] = c->nfb[b];
+            ++fl.n;
+        }
+    }
+    c->T += 1;
+    e = launch_flush_list(c, c->rk, c->rv, (long long)c->ring * c->d, c->ring, fl, s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    for (int i = 0; i < fl.n; ++i) c->nfb[fl.lb[i]] += 1;
+    return OTT_OK;
+}
+
+}  // namespace
+
 int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     if (!c) return OTT_ERR_INVALID;
     if (c->poisoned) return OTT_ERR_STATE;
     if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
     if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (c->ragged)
+        return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
     cudaError_t e = launch_append(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T += 1;
@@ -198,8 +308,20 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
     return fail_cuda(c, e);
 }
 
+int ott_get_seq_counts(const ott_cache *c, int b, long long *T, int *nf, int *tail, int *n_pool) {
+    if (!c || b < 0 || b >= c->B) return OTT_ERR_INVALID;
+    const long long Tb = c->ragged ? c->Tb[b] : c->T;
+    const int nfb = c->ragged ? c->nfb[b] : c->nf;
+    if (T) *T = Tb;
+    if (nf) *nf = nfb;
+    if (tail) *tail = (int)(Tb - (long long)nfb * c->G);
+    if (n_pool) *n_pool = pool_after(c->P, c->G, nfb);
+    return OTT_OK;
+}
+
 int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_pool) {
     if (!c) return OTT_ERR_INVALID;
+    if (c->ragged) return ott_get_seq_counts(c, 0, T, nf, tail, n_pool);
     if (T) *T = c->T;
     if (nf) *nf = c->nf;
     if (tail) *tail = (int)(c->T - (long long)c->nf * c->G);
@@ -208,7 +330,11 @@ int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_
 }
 
 int ott_block_count(const ott_cache *c, int j) {
-    if (!c || j < 0 || j >= c->nf) return OTT_ERR_INVALID;
+    if (!c) return OTT_ERR_INVALID;
+    int nf = c->nf;
+    if (c->ragged)
+        for (int b = 0; b < c->B; ++b) nf = c->nfb[b] > nf ? c->nfb[b] : nf;
+    if (j < 0 || j >= nf) return OTT_ERR_INVALID;
     return block_count(c->P, c->G, j);
 }
 
@@ -229,19 +355,23 @@ int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst) 
     if (c->poisoned) return OTT_ERR_STATE;
     if (u0 < 0 || nu < 0 || u0 + nu > c->U) return OTT_ERR_INVALID;
     if (nu == 0) return OTT_OK;
-    const int d = c->d, G = c->G, P = c->P, nf = c->nf;
-    const int nt = (int)(c->T - (long long)nf * G);
+    // a ragged batch is exported one sequence at a time (its units share T and nf)
+    if (c->ragged && u0 / c->Hkv != (u0 + nu - 1) / c->Hkv) return OTT_ERR_INVALID;
+    const int sb0 = u0 / c->Hkv;
+    const long long Tx = c->ragged ? c->Tb[sb0] : c->T;
+    const int d = c->d, G = c->G, P = c->P, nf = c->ragged ? c->nfb[sb0] : c->nf;
+    const int nt = (int)(Tx - (long long)nf * G);
     const int np = pool_after(P, G, nf);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(c, e);
 
     // blocks: canonical codes and scales through a staging buffer
     if (nf > 0 && (dst->kcode || dst->vcode || dst->ks || dst->kz || dst->vs || dst->vz)) {
-        const size_t sb = export_stage_bytes(c, nu);
+        const size_t sb = export_stage_bytes(c, nu, nf);
         uint8_t *stage = nullptr;
         e = cudaMalloc(&stage, sb);
         if (e != cudaSuccess) { cudaGetLastError(); return OTT_ERR_OOM; }
-        e = launch_export(c, u0, nu, stage, 0);
+        e = launch_export(c, u0, nu, nf, stage, 0);
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         const size_t nblk = (size_t)nu * nf;
         const size_t n_code = nblk * G * (d / 4), n_ksz = nblk * d, n_vsz = nblk * G * (d / 32);

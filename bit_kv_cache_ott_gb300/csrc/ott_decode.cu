@@ -31,6 +31,8 @@
 //     channels for P.V, fp32 accumulation, online softmax across chunks.
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "ott_internal.cuh"
 
 namespace ott {
@@ -124,6 +126,7 @@ struct DecodeArgs {
     int NWp;            // warps in the grid
     int MAXU;           // units a warp's range can touch
     float sl2;          // softmax scale 1/sqrt(d) times log2(e)
+    int B;              // sequences (the ragged table's length)
 };
 
 template <int D, int GQ>
@@ -171,6 +174,49 @@ __device__ __forceinline__ int unit_of(long long x, int Iu) {
 
 __device__ __forceinline__ size_t part_slot(const DecodeArgs &a, int w, int unit_off, int type) {
     return ((size_t)w * a.MAXU + unit_off) * 2 + type;
+}
+
+// Per-sequence counts: scalars in DecodeArgs when every sequence has the
+// same length, a table (kernel parameter) when the batch is ragged.
+struct NoTable {};
+template <bool RG>
+using TableT = typename std::conditional<RG, SeqTable, NoTable>::type;
+
+struct UnitInfo {
+    long long ub;       // the unit's first work item
+    int u, ntail, npool, ring_start, Sf, Iu;
+};
+
+// The unit holding work item x (x < W), with its counts.
+template <bool RG>
+__device__ __forceinline__ UnitInfo unit_at(const DecodeArgs &a, const TableT<RG> &st, long long x) {
+    UnitInfo r;
+    if constexpr (RG) {
+        int lo = 0, hi = a.B;   // e[lo].base <= x < e[hi].base
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (st.e[mid].base <= x) lo = mid;
+            else hi = mid;
+        }
+        const SeqEntry &e = st.e[lo];
+        const int h = (int)((unsigned)(x - e.base) / (unsigned)e.Iu);
+        r.u = lo * a.Hkv + h;
+        r.ub = e.base + (long long)h * e.Iu;
+        r.ntail = e.ntail;
+        r.npool = e.npool;
+        r.ring_start = e.ring_start;
+        r.Sf = e.Sf;
+        r.Iu = e.Iu;
+    } else {
+        r.u = unit_of(x, a.Iu);
+        r.ub = (long long)r.u * a.Iu;
+        r.ntail = a.ntail;
+        r.npool = a.npool;
+        r.ring_start = a.ring_start;
+        r.Sf = a.Sf;
+        r.Iu = a.Iu;
+    }
+    return r;
 }
 
 template <int NW>
@@ -559,24 +605,24 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 
 template <int D, int GQ>
-__device__ bool fp16_segment(const DecodeArgs &a, size_t slot, int u, int c0, int c1, uint8_t *stg0,
-                             uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
+__device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slot, int u, int c0, int c1,
+                             uint8_t *stg0, uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
     constexpr int NKT = D / 16;
     constexpr int RS = D + 8;                 // padded row stride (halves)
     constexpr int SUB = 8;                    // tokens per sub-tile
     const int r = lane >> 2, i = lane & 3;
-    const int nfp = a.ntail + a.npool;
+    const int nfp = ui.ntail + ui.npool;
     const int fb = c0 * FP16_CHUNK, fe = min(c1 * FP16_CHUNK, nfp);
     const int nsub = (fe - fb + SUB - 1) / SUB;
 
     auto row_ptr = [&](int f, bool val) -> const __half * {
         const __half *base = val ? a.rv : a.rk;
-        if (f < a.ntail) {
-            int s = a.ring_start + f;   // f < ntail < ring
+        if (f < ui.ntail) {
+            int s = ui.ring_start + f;   // f < ntail < ring
             if (s >= a.ring) s -= a.ring;
             return base + ((size_t)u * a.ring + s) * D;
         }
-        return (val ? a.pv : a.pk) + ((size_t)u * a.P + (f - a.ntail)) * D;
+        return (val ? a.pv : a.pk) + ((size_t)u * a.P + (f - ui.ntail)) * D;
     };
     // lanes 0..7 copy key rows, 8..15 value rows; rows past the end repeat
     // the sub-tile's first token (finite values, masked by a zero weight)
@@ -689,8 +735,8 @@ __device__ bool fp16_segment(const DecodeArgs &a, size_t slot, int u, int c0, in
     return true;
 }
 
-template <int D, int GQ>
-__global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
+template <int D, int GQ, bool RG>
+__global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, const __grid_constant__ TableT<RG> st) {
     using C = Cfg<D, GQ>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -716,20 +762,21 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
     if (gw >= a.NWp) return;
     long long x = range_start(a.W, a.NWp, gw);
     const long long x1 = range_start(a.W, a.NWp, gw + 1);
-    const int u_first = unit_of(x, a.Iu);
+    const int u_first = unit_at<RG>(a, st, x).u;
     while (x < x1) {
-        const int u = unit_of(x, a.Iu);
-        const long long ubase = (long long)u * a.Iu;
+        const UnitInfo ui = unit_at<RG>(a, st, x);
+        const int u = ui.u;
+        const long long ubase = ui.ub;
         const int off = (int)(x - ubase);
-        if (off < a.Sf) {
-            const int end = (int)min(x1 - ubase, (long long)a.Sf);
-            if (!fp16_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars, phase,
-                                     qsm, lane))
+        if (off < ui.Sf) {
+            const int end = (int)min(x1 - ubase, (long long)ui.Sf);
+            if (!fp16_segment<D, GQ>(a, ui, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars,
+                                     phase, qsm, lane))
                 return;
             x = ubase + end;
         } else {
-            const int end = (int)min(x1 - ubase, (long long)a.Iu);
-            if (!quant_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 1), u, off - a.Sf, end - a.Sf, stg0,
+            const int end = (int)min(x1 - ubase, (long long)ui.Iu);
+            if (!quant_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
                                       stg1, bars, phase, qsm, qhl, lane))
                 return;
             x = ubase + end;
@@ -749,8 +796,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a) {
 constexpr int COMB_MAXW = 32;
 constexpr int COMB_GRP = 8;     // candidate segments a warp loads at a time
 
-template <int D, int GQ>
-__global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
+template <int D, int GQ, bool RG>
+__global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const __grid_constant__ TableT<RG> st) {
     constexpr int CPL = D / 32, GRP = COMB_GRP;
     __shared__ float red[COMB_MAXW][D + 2];
     const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -758,12 +805,24 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
     // The unit's items are [ub, ub + Sf) fp16 then [ub + Sf, ue) quantized; the
     // decode warps holding them are contiguous ranges [f0, f1] and [q0, q1].
     // Only the first of them can have started in an earlier unit.
-    const long long ub = (long long)u * a.Iu, ue = ub + a.Iu, um = ub + a.Sf;
+    long long ub;
+    int Iu, Sf;
+    if constexpr (RG) {
+        const SeqEntry &e = st.e[b];
+        ub = e.base + (long long)(hq / GQ) * e.Iu;
+        Iu = e.Iu;
+        Sf = e.Sf;
+    } else {
+        ub = (long long)u * a.Iu;
+        Iu = a.Iu;
+        Sf = a.Sf;
+    }
+    const long long ue = ub + Iu, um = ub + Sf;
     const int wa = warp_of(a.W, a.NWp, ub);
-    const int f1 = a.Sf > 0 ? warp_of(a.W, a.NWp, um - 1) : wa - 1;
+    const int f1 = Sf > 0 ? warp_of(a.W, a.NWp, um - 1) : wa - 1;
     const int q0 = um < ue ? warp_of(a.W, a.NWp, um) : 0, q1 = um < ue ? warp_of(a.W, a.NWp, ue - 1) : -1;
     const int n0 = f1 - wa + 1, ncand = n0 + (q1 - q0 + 1);
-    const int uo_a = u - unit_of(range_start(a.W, a.NWp, wa), a.Iu);   // unit offset within warp wa's slots
+    const int uo_a = u - unit_at<RG>(a, st, range_start(a.W, a.NWp, wa)).u;   // unit offset within warp wa's slots
     // everything above depends on the arguments only; the partials are the
     // decode grid's results
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -834,10 +893,11 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a) {
 
 // Launch the combine as a programmatic dependent of the decode grid just
 // queued on stream s: one CTA per (sequence, query head).
-template <int D, int GQ>
-cudaError_t launch_combine(const DecodeArgs &a, int B, cudaStream_t s) {
-    // candidate segments per unit: about 2 * (warps covering a unit)
-    const long long per_unit_warps = (a.NWp + (a.W / a.Iu) - 1) / (a.W / a.Iu) + 1;
+template <int D, int GQ, bool RG>
+cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cudaStream_t s) {
+    // candidate segments per unit: about 2 * (decode warps covering a unit)
+    const long long U = (long long)B * a.Hkv;
+    const long long per_unit_warps = (a.NWp + U - 1) / U + 1;
     int cw = (int)((2 * per_unit_warps + 2 * COMB_GRP - 1) / (2 * COMB_GRP));   // about two rounds per warp
     cw = cw < 1 ? 1 : (cw > COMB_MAXW ? COMB_MAXW : cw);
     cudaLaunchConfig_t cfg = {};
@@ -850,11 +910,25 @@ cudaError_t launch_combine(const DecodeArgs &a, int B, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ>, a);
+    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ, RG>, a, st);
 }
 
-template <int D, int GQ>
-cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cudaStream_t s) {
+// One sequence's counts after T tokens and nf flushes.
+inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf) {
+    SeqEntry e;
+    const long long tail_start = (long long)nf * c->G;
+    e.base = 0;
+    e.nf = nf;
+    e.ring_start = (int)(tail_start % c->ring);
+    e.ntail = (int)(T - tail_start);
+    e.npool = pool_after(c->P, c->G, nf);
+    e.Sf = (e.ntail + e.npool + FP16_CHUNK - 1) / FP16_CHUNK;
+    e.Iu = e.Sf + nf;
+    return e;
+}
+
+template <int D, int GQ, bool RG>
+cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
     DecodeArgs a;
     a.blk = c->blk;
     a.blk_bytes = c->blk_bytes;
@@ -867,36 +941,60 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, cu
     a.P = c->P;
     a.q = q;
     a.out = out;
-    a.part = c->part;
+    a.part = part;
     a.ctl = c->ctl;
     a.Hq = c->Hq;
     a.Hkv = c->Hkv;
     a.G = c->G;
-    a.nf = c->nf;
+    a.B = c->B;
     a.jfull = (c->P + c->G - 1) / c->G;   // from this block on, the pool is full
-    const long long tail_start = (long long)c->nf * c->G;
-    a.ring_start = (int)(tail_start % c->ring);
-    a.ntail = (int)(c->T - tail_start);
-    a.npool = pool_after(c->P, c->G, c->nf);
-    a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
-    a.Iu = a.Sf + c->nf;
-    a.W = (long long)c->U * a.Iu;
+    TableT<RG> st;
+    if constexpr (RG) {
+        long long base = 0;
+        for (int b = 0; b < c->B; ++b) {
+            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b]);
+            st.e[b].base = base;
+            base += (long long)c->Hkv * st.e[b].Iu;
+        }
+        st.e[c->B] = SeqEntry{};
+        st.e[c->B].base = base;
+        a.W = base;
+        a.nf = a.ntail = a.npool = a.ring_start = a.Sf = a.Iu = 0;   // per sequence in the table
+        a.MAXU = c->maxu_r;
+    } else {
+        const SeqEntry e = seq_entry(c, c->T, c->nf);
+        a.nf = e.nf;
+        a.ring_start = e.ring_start;
+        a.ntail = e.ntail;
+        a.npool = e.npool;
+        a.Sf = e.Sf;
+        a.Iu = e.Iu;
+        a.W = (long long)c->U * a.Iu;
+        a.MAXU = c->maxu;
+    }
     // never more active warps than items: every active warp owns >= 1 item
     a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
-    a.MAXU = c->maxu;
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
     // CTAs only as wide as the active warps need: with few items, the SMs keep
     // room for the combine's CTAs, which then start while the decode drains
     const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
-    k_decode<D, GQ><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a);
+    k_decode<D, GQ, RG><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_combine<D, GQ>(a, c->B, s);
+    return launch_combine<D, GQ, RG>(a, st, c->B, s);
 }
 
 template <int D, int GQ>
 cudaError_t set_decode_attr(int smem_max) {
-    return cudaFuncSetAttribute(k_decode<D, GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    cudaError_t e = cudaFuncSetAttribute(k_decode<D, GQ, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_decode<D, GQ, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+}
+
+template <int D, int GQ>
+cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
+    return c->ragged ? launch_decode_t<D, GQ, true>(c, q, out, part, s)
+                     : launch_decode_t<D, GQ, false>(c, q, out, part, s);
 }
 
 }  // namespace
@@ -927,7 +1025,7 @@ cudaError_t set_kernel_attributes(int d, int gq, int smem_max) {
 
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s) {
 #define OTT_DEC(D_, G_) \
-    if (c->d == D_ && c->gq == G_) return launch_decode_t<D_, G_>(c, q, out, s);
+    if (c->d == D_ && c->gq == G_) return launch_decode_any<D_, G_>(c, q, out, c->part, s);
     OTT_DEC(128, 1) OTT_DEC(128, 2) OTT_DEC(128, 4) OTT_DEC(64, 1) OTT_DEC(64, 2) OTT_DEC(64, 4)
 #undef OTT_DEC
     return cudaErrorInvalidValue;
@@ -975,48 +1073,6 @@ cudaError_t static_scratch_address(int dev, float **out) {
     return cudaSuccess;
 }
 
-template <int D, int GQ>
-cudaError_t launch_decode_static_t(const ott_cache *c, const __half *q, __half *out, float *scratch,
-                                   cudaStream_t s) {
-    DecodeArgs a;
-    a.blk = c->blk;
-    a.blk_bytes = c->blk_bytes;
-    a.NB = c->NB;
-    a.rk = c->rk;
-    a.rv = c->rv;
-    a.ring = c->ring;
-    a.pk = c->pk;
-    a.pv = c->pv;
-    a.P = c->P;
-    a.q = q;
-    a.out = out;
-    a.part = scratch;
-    a.ctl = c->ctl;
-    a.Hq = c->Hq;
-    a.Hkv = c->Hkv;
-    a.G = c->G;
-    a.nf = c->nf;
-    a.jfull = (c->P + c->G - 1) / c->G;
-    const long long tail_start = (long long)c->nf * c->G;
-    a.ring_start = (int)(tail_start % c->ring);
-    a.ntail = (int)(c->T - tail_start);
-    a.npool = pool_after(c->P, c->G, c->nf);
-    a.Sf = (a.ntail + a.npool + FP16_CHUNK - 1) / FP16_CHUNK;
-    a.Iu = a.Sf + c->nf;
-    a.W = (long long)c->U * a.Iu;
-    // never more active warps than items: every active warp owns >= 1 item
-    a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
-    a.MAXU = c->maxu;
-    a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
-    // CTAs only as wide as the active warps need: with few items, the SMs keep
-    // room for the combine's CTAs, which then start while the decode drains
-    const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
-    k_decode<D, GQ><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_combine<D, GQ>(a, c->B, s);
-}
-
 }  // namespace
 }  // namespace ott
 
@@ -1029,7 +1085,8 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return OTT_ERR_CUDA;
     if (dev != c->device) return OTT_ERR_STATE;   // the cache's device must be current
-    const size_t need = (size_t)c->sm_count * DEC_WARPS * c->maxu * 2 * c->gq * (c->d + 2);
+    const int maxu = c->ragged ? c->maxu_r : c->maxu;
+    const size_t need = (size_t)c->sm_count * DEC_WARPS * maxu * 2 * c->gq * (c->d + 2);
     if (need > kStaticScratchFloats) return OTT_ERR_CAPACITY;
     float *scratch = nullptr;
     if (static_scratch_address(dev, &scratch) != cudaSuccess) return OTT_ERR_CUDA;
@@ -1038,7 +1095,7 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
     const __half *qh = static_cast<const __half *>(q);
     __half *oh = static_cast<__half *>(out);
 #define OTT_DEC_S(D_, G_) \
-    if (c->d == D_ && c->gq == G_) e = launch_decode_static_t<D_, G_>(c, qh, oh, scratch, s);
+    if (c->d == D_ && c->gq == G_) e = launch_decode_any<D_, G_>(c, qh, oh, scratch, s);
     OTT_DEC_S(128, 1) OTT_DEC_S(128, 2) OTT_DEC_S(128, 4) OTT_DEC_S(64, 1) OTT_DEC_S(64, 2) OTT_DEC_S(64, 4)
 #undef OTT_DEC_S
     if (e != cudaSuccess) {

@@ -49,18 +49,30 @@ struct FlushArgs {
     long long t0;                // first token of the group
     long long blk_bytes;
     int G, P, NB, ntile, j, np0;
+    int Hkv;
 };
 
+// One CTA per unit. Without a list, CTA u flushes group a.j of unit u; with
+// one (ragged batches), CTA i flushes group fl.lj[i / Hkv] of kv head i % Hkv
+// of sequence fl.lb[i / Hkv].
 template <int D>
-__global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a) {
+__global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __grid_constant__ FlushList fl) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int RS = D + 8;          // padded row stride (halves): 16B-aligned rows
     constexpr int VPR = D / 8;         // 16-byte vectors per row
     constexpr int NG = D / 32;         // value groups
     constexpr int NKT = D / 16;
     constexpr int NW = D / 32;
-    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
-    const int G = a.G, P = a.P, np0 = a.np0, nc = np0 + G;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    int u = blockIdx.x, jj = a.j;
+    long long t0 = a.t0;
+    if (fl.n > 0) {
+        const int e = blockIdx.x / a.Hkv;
+        u = fl.lb[e] * a.Hkv + blockIdx.x % a.Hkv;
+        jj = fl.lj[e];
+        t0 = (long long)jj * a.G;
+    }
+    const int G = a.G, P = a.P, np0 = fl.n > 0 ? pool_after(P, G, jj) : a.np0, nc = np0 + G;
 
     __half *ck = reinterpret_cast<__half *>(smem);
     __half *cv = ck + (size_t)nc * RS;
@@ -81,7 +93,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a) {
             sk = a.pk + off;
             sv = a.pv + off;
         } else {
-            const long long t = a.t0 + (row - np0);
+            const long long t = t0 + (row - np0);
             const size_t off = (size_t)u * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
             sk = a.srcK + off;
             sv = a.srcV + off;
@@ -106,7 +118,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a) {
                 s = __fadd_rn(s, __fmul_rn(x, x));
             }
             nrm = s;
-            idx = (int)(a.t0 + (row - np0));
+            idx = (int)(t0 + (row - np0));
         }
         key[row] = ((uint64_t)__float_as_uint(nrm) << 32) | (uint32_t)idx;
     }
@@ -149,10 +161,10 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a) {
     }
     __syncthreads();
 
-    uint8_t *bb = a.blk + ((size_t)u * a.NB + a.j) * a.blk_bytes;
+    uint8_t *bb = a.blk + ((size_t)u * a.NB + jj) * a.blk_bytes;
     uint8_t *tiles = bb + ksz_bytes(D);
     for (int t = tid; t < G; t += nth)
-        a.bidx[((size_t)u * a.NB + a.j) * G + t] = t < cnt ? (int32_t)(uint32_t)key[bmap[t]] : -1;
+        a.bidx[((size_t)u * a.NB + jj) * G + t] = t < cnt ? (int32_t)(uint32_t)key[bmap[t]] : -1;
 
     // 6. keys: one (scale, zero) per channel over the block's tokens
     for (int ch = tid; ch < D; ch += nth) {
@@ -239,19 +251,35 @@ __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ 
     }
 }
 
-// tokens [t_begin, L) of K, V [U][L][d] -> their ring slots
-__global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half *rv, int U, int d,
-                            int ring, int L, long long t_begin) {
+// Ragged batches: k, v [U][d] -> ring slot slot[b] of every unit of sequence b.
+struct SlotTable {
+    int slot[RAGGED_MAX];
+};
+
+__global__ void k_append_ragged(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
+                                __half *rv, int U, int Hkv, int d, int ring, const __grid_constant__ SlotTable st) {
     const int vpr = d / 8;
-    const long long ntok = L - t_begin;
-    const long long total = (long long)U * ntok * vpr;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
+        const int u = e / vpr, x = e % vpr;
+        const size_t off = ((size_t)u * ring + st.slot[u / Hkv]) * d;
+        reinterpret_cast<uint4 *>(rk + off)[x] = k[e];
+        reinterpret_cast<uint4 *>(rv + off)[x] = v[e];
+    }
+}
+
+// tokens [t_begin, t_end) of units [u0, u0+nu) of K, V [U][Lstride][d] -> their ring slots
+__global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half *rv, int u0, int nu, int d,
+                            int ring, int Lstride, long long t_begin, long long t_end) {
+    const int vpr = d / 8;
+    const long long ntok = t_end - t_begin;
+    const long long total = (long long)nu * ntok * vpr;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
         const int x = (int)(e % vpr);
         const long long tt = (e / vpr) % ntok;
-        const int u = (int)(e / vpr / ntok);
+        const int u = u0 + (int)(e / vpr / ntok);
         const long long t = t_begin + tt;
-        const size_t src = ((size_t)u * L + t) * d;
+        const size_t src = ((size_t)u * Lstride + t) * d;
         const size_t dst = ((size_t)u * ring + (size_t)(t % ring)) * d;
         reinterpret_cast<uint4 *>(rk + dst)[x] = reinterpret_cast<const uint4 *>(K + src)[x];
         reinterpret_cast<uint4 *>(rv + dst)[x] = reinterpret_cast<const uint4 *>(V + src)[x];
@@ -339,9 +367,10 @@ cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
-                         long long src_unit_stride, long long src_mod, long long t0, int j,
-                         cudaStream_t s) {
+namespace {
+
+FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV, long long src_unit_stride,
+                     long long src_mod, long long t0, int j) {
     FlushArgs a;
     a.blk = c->blk;
     a.bidx = c->bidx;
@@ -361,37 +390,74 @@ cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *s
     a.ntile = c->ntile;
     a.j = j;
     a.np0 = pool_after(c->P, c->G, j);
+    a.Hkv = c->Hkv;
+    return a;
+}
+
+cudaError_t run_flush(const ott_cache *c, const FlushArgs &a, const FlushList &fl, int ctas, cudaStream_t s) {
     const int smem = flush_smem_bytes(c->d, c->G, c->P);
     if (c->d == 128)
-        k_flush<128><<<c->U, FLUSH_THREADS, smem, s>>>(a);
+        k_flush<128><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
     else
-        k_flush<64><<<c->U, FLUSH_THREADS, smem, s>>>(a);
+        k_flush<64><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
+                         long long src_unit_stride, long long src_mod, long long t0, int j,
+                         cudaStream_t s) {
+    FlushList none;
+    none.n = 0;
+    return run_flush(c, flush_args(c, srcK, srcV, src_unit_stride, src_mod, t0, j), none, c->U, s);
+}
+
+cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __half *srcV,
+                              long long src_unit_stride, long long src_mod, const FlushList &fl,
+                              cudaStream_t s) {
+    if (fl.n <= 0) return cudaSuccess;
+    return run_flush(c, flush_args(c, srcK, srcV, src_unit_stride, src_mod, 0, 0), fl, fl.n * c->Hkv, s);
+}
+
+cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+    SlotTable st;
+    for (int b = 0; b < c->B; ++b) st.slot[b] = (int)(c->Tb[b] % c->ring);
+    const int n = c->U * c->d / 8;
+    const int th = 256, bl = (n + th - 1) / th;
+    k_append_ragged<<<bl, th, 0, s>>>(reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
+                                      c->rk, c->rv, c->U, c->Hkv, c->d, c->ring, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
+                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s) {
+    if (t_begin >= t_end || nu <= 0) return cudaSuccess;
+    const long long total = (long long)nu * (t_end - t_begin) * (c->d / 8);
+    const int th = 256;
+    const long long bl = (total + th - 1) / th;
+    k_copy_tail<<<(int)(bl < 65535 ? bl : 65535), th, 0, s>>>(K, V, c->rk, c->rv, u0, nu, c->d, c->ring,
+                                                               Lstride, t_begin, t_end);
     return cudaGetLastError();
 }
 
 cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *V, int L,
                              long long t_begin, cudaStream_t s) {
-    if (t_begin >= L) return cudaSuccess;
-    const long long total = (long long)c->U * (L - t_begin) * (c->d / 8);
-    const int th = 256;
-    const long long bl = (total + th - 1) / th;
-    k_copy_tail<<<(int)(bl < 65535 ? bl : 65535), th, 0, s>>>(K, V, c->rk, c->rv, c->U, c->d, c->ring,
-                                                               L, t_begin);
-    return cudaGetLastError();
+    return launch_copy_tail_units(c, K, V, 0, c->U, L, t_begin, L, s);
 }
 
-size_t export_stage_bytes(const ott_cache *c, int nu) {
-    const size_t nblk = (size_t)nu * c->nf;
+size_t export_stage_bytes(const ott_cache *c, int nu, int nf) {
+    const size_t nblk = (size_t)nu * nf;
     return nblk * c->G * (c->d / 4) * 2 + nblk * c->d * 2 * 2 + nblk * c->G * (c->d / 32) * 2 * 2 + 64;
 }
 
-cudaError_t launch_export(const ott_cache *c, int u0, int nu, uint8_t *stage, cudaStream_t s) {
-    const size_t nblk = (size_t)nu * c->nf;
+cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *stage, cudaStream_t s) {
+    const size_t nblk = (size_t)nu * nf;
     ExportArgs a;
     a.blk = c->blk;
     a.blk_bytes = c->blk_bytes;
     a.NB = c->NB;
-    a.nf = c->nf;
+    a.nf = nf;
     a.G = c->G;
     a.d = c->d;
     a.u0 = u0;

@@ -41,6 +41,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/ott.h"
 
 namespace ott {
@@ -49,6 +51,7 @@ constexpr int TILE = 16;          // token slots per tile
 constexpr int CHUNK_TILES = 4;    // tiles per staged chunk in the decode kernel
 constexpr int DEC_WARPS = 16;     // warps per decode CTA
 constexpr int FP16_CHUNK = 32;    // fp16 tokens per decode split (one per lane)
+constexpr int RAGGED_MAX = 256;   // sequences in a cache whose sequences may differ in length
 
 __host__ __device__ constexpr int ksz_bytes(int d) { return 4 * d; }
 __host__ __device__ constexpr int tile_bytes(int d) { return 10 * d; }
@@ -120,19 +123,47 @@ struct ott_cache {
     int32_t *pidx;          // [U][P]
     float *part;            // [warps][maxu][2][gq][d+2] split-K partials
     int *ctl;               // [1] status flag set by a bounded wait that timed out
+    // sequences of different lengths (ott_create_ragged + ott_prefill_lens)
+    int ragged_capable;     // partials sized for ragged decode
+    int ragged;             // per-sequence lengths in effect
+    int maxu_r;             // units a decode warp's range can touch in a ragged batch
+    std::vector<long long> Tb;   // [B] tokens of each sequence (ragged)
+    std::vector<int> nfb;        // [B] flushes of each sequence (ragged)
 };
 
 namespace ott {
 
+// One sequence of a ragged batch as the decode kernels see it: its work
+// items start at `base` (items of unit b*Hkv + h at base + h*Iu), and its
+// counts. e[B].base holds the total item count.
+struct SeqEntry {
+    long long base;
+    int nf, ntail, npool, ring_start, Sf, Iu;
+};
+struct SeqTable {
+    SeqEntry e[RAGGED_MAX + 1];
+};
+// Sequences to flush in one launch (ragged batches): sequence lb[i], group lj[i].
+struct FlushList {
+    int n;
+    int lb[RAGGED_MAX], lj[RAGGED_MAX];
+};
+
 cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s);
+cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s);
 cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
                          long long src_unit_stride, long long src_mod, long long t0, int j,
                          cudaStream_t s);
+cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __half *srcV,
+                              long long src_unit_stride, long long src_mod, const FlushList &fl,
+                              cudaStream_t s);
 cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *V, int L,
                              long long t_begin, cudaStream_t s);
+cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
+                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s);
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
-cudaError_t launch_export(const ott_cache *c, int u0, int nu, uint8_t *stage, cudaStream_t s);
-size_t export_stage_bytes(const ott_cache *c, int nu);
+cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *stage, cudaStream_t s);
+size_t export_stage_bytes(const ott_cache *c, int nu, int nf);
 int flush_smem_bytes(int d, int G, int P);
 int decode_smem_bytes(int d, int gq);
 cudaError_t set_kernel_attributes(int d, int gq, int smem_max);

@@ -80,6 +80,19 @@ enum {
 int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P,
                int max_tokens, ott_cache **out);
 
+/*
+ * As ott_create, for a batch whose sequences may differ in length: the pages
+ * state the method for one sequence, and a serving batch holds sequences of
+ * different lengths, each quantized, pooled and flushed on its own schedule
+ * (zijie-tian.site sec. 3.1 and 3.2 applied per sequence). Additionally
+ * requires B <= 256. The split-K scratch is sized for ranges of work that
+ * cross many short sequences, so it is larger than ott_create's. Such a
+ * cache accepts ott_prefill (all sequences equally long) or
+ * ott_prefill_lens (one length per sequence).
+ */
+int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P,
+                      int max_tokens, ott_cache **out);
+
 /* Free everything. NULL-safe. Waits for the device to finish. */
 int ott_destroy(ott_cache *c);
 
@@ -90,6 +103,21 @@ int ott_destroy(ott_cache *c);
  * T > 0, OTT_ERR_CAPACITY if L > max_tokens.
  */
 int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream);
+
+/*
+ * Ragged prefill into an EMPTY cache made by ott_create_ragged. K, V: device
+ * fp16 [B][Hkv][Lmax][d]; lens: HOST int32[B], read during the call, with
+ * 1 <= lens[b] <= Lmax <= max_tokens. Sequence b takes its first lens[b]
+ * tokens (the rest of its rows are not read), equivalent to lens[b] appends
+ * to that sequence alone. Afterwards every sequence keeps its own token
+ * count: ott_append adds one token to each and flushes exactly the
+ * sequences whose residual window reached G+R; ott_decode_attn attends each
+ * sequence over its own tokens. Errors: OTT_ERR_STATE if the cache is not
+ * ragged-capable or not empty, OTT_ERR_INVALID for a length outside
+ * [1, Lmax], OTT_ERR_CAPACITY if Lmax > max_tokens.
+ */
+int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens, int Lmax,
+                     void *stream);
 
 /*
  * Append one token to every sequence. k, v: device fp16 [B][Hkv][d]. The
@@ -132,8 +160,13 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
 int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream);
 
 /* Counts (same for every sequence and kv head): tokens seen, blocks (flushes),
- * residual tokens, pool tokens. Host-side, no device access. */
+ * residual tokens, pool tokens. Host-side, no device access. After
+ * ott_prefill_lens the counts differ per sequence; this then reports
+ * sequence 0 (see ott_get_seq_counts). */
 int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_pool);
+
+/* The same counts for sequence b (0 <= b < B), in either kind of batch. */
+int ott_get_seq_counts(const ott_cache *c, int b, long long *T, int *nf, int *tail, int *n_pool);
 
 /* Valid tokens of block j (0 <= j < nf). Host-side. Returns the count or
  * OTT_ERR_INVALID. */
@@ -152,7 +185,9 @@ int ott_block_count(const ott_cache *c, int j);
  *   pidx  [nu][P] int32 ascending (-1 pad); pnorm [nu][P] fp32 bits;
  *   pk,pv [nu][P][d]       pool tokens in ascending token order (0 padded)
  * Padding slots are zero. Synchronizes the device; allocates a temporary
- * device staging buffer. Errors: OTT_ERR_INVALID for a bad unit range.
+ * device staging buffer. After ott_prefill_lens the units of one call must
+ * belong to one sequence (nf and nt are that sequence's). Errors:
+ * OTT_ERR_INVALID for a bad unit range.
  */
 typedef struct {
     int32_t *bidx;
