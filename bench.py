@@ -149,6 +149,25 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle arm
 
+def synth_T(w) -> str:
+    return f"{w.len_lo}..{w.L}" if w.ragged else f"{w.L}"
+
+
+def step_bytes(w, Ts) -> int:
+    """Algorithmic bytes of one decode call with sequence b at Ts[b] tokens."""
+    if len(set(Ts)) == 1:
+        return metrics.decode_bytes(Ts[0], len(Ts), w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+    return sum(metrics.decode_bytes(t, 1, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) for t in Ts)
+
+
+def _oracle_prefill(orc, w, lens):
+    K, V = synth.prefill_kv(w)
+    if w.ragged:
+        orc.prefill_lens(K, V, lens)
+    else:
+        orc.prefill(K, V)
+
+
 def oracle_rate(w, steps: int, warmup: int, units_sample: int):
     """The CPU oracle (single thread) on a sample of the workload's units:
     prefill, then `warmup` untimed and `steps` timed decode steps (append +
@@ -158,9 +177,8 @@ def oracle_rate(w, steps: int, warmup: int, units_sample: int):
     Bs = max(1, min(w.B, units_sample // w.Hkv))
     ws = w.with_(B=Bs)
     orc = OracleCache(ws.B, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P)
-    K, V = synth.prefill_kv(ws)
-    orc.prefill(K, V)
-    del K, V
+    lens = synth.seq_lens(w)
+    _oracle_prefill(orc, ws, lens[:Bs])
     inputs = [synth.step_kvq(ws, s) for s in range(warmup + steps)]
     for s in range(warmup):
         k, v, q = inputs[s]
@@ -172,11 +190,12 @@ def oracle_rate(w, steps: int, warmup: int, units_sample: int):
         orc.append(k, v)
         orc.decode(q)
     dt = time.perf_counter() - t0
-    frac = (Bs * ws.Hkv) / (w.B * w.Hkv)
+    # scaled to the whole workload by algorithmic bytes (= by units when all lengths are equal)
+    frac = step_bytes(ws, lens[:Bs]) / step_bytes(w, lens)
     per_step_full = dt / steps / frac
     rate = w.B / (per_step_full * w.layers)   # tokens/s: each token passes every layer
     sample = (f"{Bs} of {w.B} sequences ({Bs * w.Hkv} of {w.B * w.Hkv} (sequence, kv head) units), "
-              f"{steps} timed decode steps after {warmup} warm-up, T={w.L}+; one layer; scaled by units")
+              f"{steps} timed decode steps after {warmup} warm-up, T={synth_T(w)}+; one layer; scaled by bytes")
     return rate, dt, sample
 
 
@@ -192,15 +211,13 @@ def _oracle_worker(task):
     """One host process of the all-cores baseline: the oracle on its own
     slice of (sequence, kv head) units, timed after every worker has
     prefilled (so that the timed regions run concurrently)."""
-    name, hk, seed, steps, warmup = task
+    name, hk, seed, steps, warmup, length = task
     from oracle.oracle import OracleCache
     w = synth.WORKLOADS[name]
     g = w.Hq // w.Hkv
     ws = w.with_(B=1, Hkv=hk, Hq=g * hk, seed=seed)
     orc = OracleCache(1, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P)
-    K, V = synth.prefill_kv(ws)
-    orc.prefill(K, V)
-    del K, V
+    _oracle_prefill(orc, ws, [length])
     inputs = [synth.step_kvq(ws, s) for s in range(warmup + steps)]
     for s in range(warmup):
         k, v, q = inputs[s]
@@ -228,16 +245,20 @@ def oracle_rate_cores(w, steps: int, warmup: int, units_per_proc: int):
     nproc = max(1, min(ncore, (U + hk - 1) // hk))
     ctx = mp.get_context("spawn")
     barrier = ctx.Barrier(nproc)
-    tasks = [(w.name, hk, w.seed + 7919 * (i + 1), steps, warmup) for i in range(nproc)]
+    lens = synth.seq_lens(w)
+    tasks = [(w.name, hk, w.seed + 7919 * (i + 1), steps, warmup, lens[i % w.B]) for i in range(nproc)]
     with ctx.Pool(nproc, initializer=_oracle_worker_init, initargs=(barrier,)) as pool:
         # a worker that cannot start would stall the barrier: bound the wait
         dts = pool.map_async(_oracle_worker, tasks).get(timeout=900)
     dt = max(dts)
     units = nproc * hk
-    per_step_full = dt / steps * U / units
+    # scaled to the whole workload by algorithmic bytes (= by units when all lengths are equal)
+    w1 = w.with_(Hkv=hk, Hq=(w.Hq // w.Hkv) * hk)
+    sampled = sum(step_bytes(w1, [lens[i % w.B]]) for i in range(nproc))
+    per_step_full = dt / steps * step_bytes(w, lens) / sampled
     rate = w.B / (per_step_full * w.layers)
     sample = (f"{nproc} processes x {hk} (sequence, kv head) units ({units} of {U}), {steps} timed decode steps "
-              f"after {warmup} warm-up, timed concurrently, T={w.L}+; one layer; scaled by units")
+              f"after {warmup} warm-up, timed concurrently, T={synth_T(w)}+; one layer; scaled by bytes")
     return rate, dt, sample, nproc
 
 
@@ -282,10 +303,14 @@ def run_ours(args, w):
     K_steps, W_steps, E_steps = args.steps, args.warmup, args.e2e_steps
     total_steps = W_steps + K_steps + E_steps
     caches = []
+    lens = synth.seq_lens(wr)
     for layer in range(w.layers):
-        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps)
+        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged)
         K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
-        c.prefill(K, V)
+        if w.ragged:
+            c.prefill_lens(K, V, lens)
+        else:
+            c.prefill(K, V)
         del K, V
         caches.append(c)
     torch.cuda.synchronize()
@@ -317,7 +342,8 @@ def run_ours(args, w):
                   for _ in range(K_steps * w.layers)]
     dec_bytes = 0
     flushes = 0
-    T0 = caches[0].counts()[0]
+    Ts = [caches[0].seq_counts(b)[0] for b in range(w.B)]
+    T0 = max(Ts)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
@@ -325,16 +351,16 @@ def run_ours(args, w):
         e0.record(stream)
         for s in range(K_steps):
             k, v, q = dev_in[(W_steps + s) % n_distinct]
+            Ts = [t + 1 for t in Ts]
+            flush_launch = any((t - w.R) % w.G == 0 and t >= w.G + w.R for t in Ts)   # some sequence flushes now
             for li, c in enumerate(caches):
-                nf_before = c.counts()[1]
                 c.append(k, v, stream)
-                T, nf_after, _, _ = c.counts()
-                flushes += nf_after - nf_before
+                flushes += int(flush_launch)
                 ev = dec_events[s * w.layers + li]
                 ev[0].record(stream)
                 c.decode_attn(q, out, stream)
                 ev[1].record(stream)
-                dec_bytes += metrics.decode_bytes(T, w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+                dec_bytes += step_bytes(w, Ts)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -417,13 +443,15 @@ def run_ours(args, w):
 
     if rank == 0:
         cache_bytes = caches[0].device_bytes() * w.layers
-        fp16_bytes = metrics.fp16_cache_bytes(T0, w.B, w.Hkv, w.d) * w.layers
+        fp16_bytes = sum(metrics.fp16_cache_bytes(t, 1, w.Hkv, w.d) for t in synth.seq_lens(wr)) * w.layers
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K_steps,
             "warmup": W_steps, "ms_per_step": ms / K_steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16 storage, fp32 accumulation", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
                        "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
+                       **({"ragged_lens": {"min": min(lens), "max": max(lens),
+                                           "mean": round(sum(lens) / len(lens), 1)}} if w.ragged else {}),
                        "l2": (f"cache {cache_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"
                               if cache_bytes > L2_BYTES else "cache fits L2: L2-resident numbers"),
                        "parallelism": f"weak-scaled shards x{ws}" if ws > 1 else "1 GPU"},

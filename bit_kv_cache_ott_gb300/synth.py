@@ -46,10 +46,15 @@ class Workload:
     outlier_rate: float = 0.005
     layers: int = 1   # independent caches (one per layer)
     seed: int = 1000
+    len_lo: int = 0   # > 0: sequence b's prefill length is drawn uniformly from [len_lo, L]
 
     @property
     def g(self) -> int:
         return self.Hq // self.Hkv
+
+    @property
+    def ragged(self) -> bool:
+        return self.len_lo > 0
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -77,9 +82,21 @@ WORKLOADS = {
     "llama31_8b_131k": Workload("llama31_8b_131k", B=1, Hq=32, Hkv=8, d=128, L=131072,
                                 steps=128, G=128, R=32, P=64, outlier_rate=0.002,
                                 layers=32, seed=1004),
+    # a serving batch whose sequences differ in length (mean ~4096 tokens)
+    "batch_b32_ragged": Workload("batch_b32_ragged", B=32, Hq=32, Hkv=32, d=128, L=7168, steps=512,
+                                 G=128, R=32, P=32, seed=1005, len_lo=1024),
 }
 
 HEADLINE = "batch_b32"
+
+
+def seq_lens(w: Workload) -> list[int]:
+    """Prefill length of every sequence: w.L for all, or (ragged workloads)
+    drawn uniformly from [w.len_lo, w.L] by the workload's seed."""
+    if not w.ragged:
+        return [w.L] * w.B
+    g = _gen(w.seed * 104729 + 11)
+    return [int(x) for x in torch.randint(w.len_lo, w.L + 1, (w.B,), generator=g)]
 
 
 def _gen(seed: int, device="cpu") -> torch.Generator:

@@ -75,3 +75,51 @@ def test_mistral_gqa(oracle_mod, ott, name):
 
 def test_llama31_8b_131k_one_layer(oracle_mod, ott):
     run_fullsize(oracle_mod, ott, "llama31_8b_131k", 128, {0, 31, 32, 127}, heads=8)
+
+
+def _compare_seq_state(c, orc, b, Hkv, STATE_KEYS):
+    gpu = c.export_state(b * Hkv, Hkv)
+    for h in range(Hkv):
+        e = orc.export_unit(b * Hkv + h)
+        assert (gpu["T"], gpu["nf"], gpu["tail"], gpu["npool"]) == (e["T"], e["nf"], e["tail"], e["npool"]), (b, h)
+        assert np.array_equal(gpu["bcount"], e["bcount"]), (b, h)
+        for k in STATE_KEYS:
+            assert np.array_equal(gpu[k][h], e[k]), f"seq {b} head {h} field {k}"
+
+
+def test_batch_b32_ragged(oracle_mod, ott):
+    """The ragged serving batch (32 sequences of 1K..7K tokens): the state of
+    every sequence that flushes is checked at the step it flushes, sampled
+    outputs at chosen steps."""
+    from tests.parity_util import STATE_KEYS
+    w = synth.WORKLOADS["batch_b32_ragged"]
+    lens = synth.seq_lens(w)
+    steps, decode_steps = 200, {0, 37, 38, 120, 199}
+    K, V = synth.prefill_kv(w)
+    orc = oracle_mod.OracleCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+    orc.prefill_lens(K, V, lens)
+    pairs = _sample_heads(w, 12, 3)
+    with ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + steps, ragged=True) as c:
+        c.prefill_lens(K.cuda(), V.cuda(), lens)
+        del K, V
+        for b in (0, 7, 19, w.B - 1):
+            _compare_seq_state(c, orc, b, w.Hkv, STATE_KEYS)
+        nf_prev = [c.seq_counts(b)[1] for b in range(w.B)]
+        flushed = 0
+        for s in range(steps):
+            k, v, q = synth.step_kvq(w, s)
+            c.append(k.cuda(), v.cuda())
+            orc.append(k, v)
+            for b in range(w.B):
+                nf = c.seq_counts(b)[1]
+                if nf != nf_prev[b]:
+                    _compare_seq_state(c, orc, b, w.Hkv, STATE_KEYS)
+                    nf_prev[b] = nf
+                    flushed += 1
+            if s in decode_steps:
+                out = c.decode_attn(q.cuda()).float().cpu().numpy()
+                ref = np.stack([orc.decode_head(b, h, q[b, h]) for b, h in pairs])
+                got = torch.from_numpy(np.stack([out[b, h] for b, h in pairs]))
+                compare_out(got, ref, f"ragged step {s}")
+        assert flushed > w.B // 2        # the sequences flushed at different steps
+        c.check_device()
