@@ -285,9 +285,16 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     float acc[NKT][4];
 #pragma unroll
     for (int mt = 0; mt < NKT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-    float zs[NV];
+    // With an even number of B variants (GQA), the two lanes that hold the hi
+    // and lo piece of one column split the variants: each computes p*s for
+    // half of them (both pieces) and receives its piece of the other half
+    // from its partner (lane ^ 4). zs[k] then sums variant 2k + piece.
+    constexpr bool SPLIT = NV % 2 == 0;
+    constexpr int NZ = SPLIT ? NV / 2 : NV;
+    static_assert(!SPLIT || NV * GPV == NG, "split variants cover every value group");
+    float zs[NZ];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) zs[v] = 0.0f;
+    for (int v = 0; v < NZ; ++v) zs[v] = 0.0f;
     float m_run = -CUDART_INF_F, l_run = 0.0f;   // head i
     uint32_t Bk[NKT][2];
     float c1 = 0.0f, c0 = 0.0f;
@@ -466,7 +473,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                 for (int e = 0; e < 4; ++e) acc[mt][e] *= aD;
             const float aZ = __shfl_sync(0xffffffffu, alpha, hV);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) zs[v] *= aZ;
+            for (int v = 0; v < NZ; ++v) zs[v] *= aZ;
             m_run = m_new;
         }
         const float m_use = m_run == -CUDART_INF_F ? 0.0f : m_run;
@@ -485,10 +492,12 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                 const float pb = __shfl_sync(0xffffffffu, p0, src1);
                 const float pc = __shfl_sync(0xffffffffu, p1, src0);
                 const float pd = __shfl_sync(0xffffffffu, p1, src1);
+                if constexpr (SPLIT) {
+                    const bool lo_lane = (r & 1) != 0;
 #pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    const int gamma = v * GPV + glow;
-                    if (gamma < NG) {
+                    for (int k = 0; k < NV / 2; ++k) {
+                        // this lane's variant 2k + piece, both pieces; the partner's piece goes across
+                        const int gamma = (2 * k + (lo_lane ? 1 : 0)) * GPV + glow;
                         const uint4 sz =
                             *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
                         const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
@@ -496,14 +505,44 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                         const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
                         const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
                         const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
-                        zs[v] = fmaf(pa, e0.y, zs[v]);
-                        zs[v] = fmaf(pb, e1.y, zs[v]);
-                        zs[v] = fmaf(pc, e2.y, zs[v]);
-                        zs[v] = fmaf(pd, e3.y, zs[v]);
+                        zs[k] = fmaf(pa, e0.y, zs[k]);
+                        zs[k] = fmaf(pb, e1.y, zs[k]);
+                        zs[k] = fmaf(pc, e2.y, zs[k]);
+                        zs[k] = fmaf(pd, e3.y, zs[k]);
                         const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
                         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                        bv[tau][v][0] = h2bits(__floats2half2_rn(x0 - pm * f01.x, x1 - pm * f01.y));
-                        bv[tau][v][1] = h2bits(__floats2half2_rn(x2 - pm * f23.x, x3 - pm * f23.y));
+                        const uint32_t hi0 = h2bits(h01), hi1 = h2bits(h23);
+                        const uint32_t lo0 = h2bits(__floats2half2_rn(x0 - f01.x, x1 - f01.y));
+                        const uint32_t lo1 = h2bits(__floats2half2_rn(x2 - f23.x, x3 - f23.y));
+                        const uint32_t own0 = lo_lane ? lo0 : hi0, own1 = lo_lane ? lo1 : hi1;
+                        const uint32_t got0 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi0 : lo0, 4);
+                        const uint32_t got1 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi1 : lo1, 4);
+                        bv[tau][2 * k][0] = lo_lane ? got0 : own0;
+                        bv[tau][2 * k][1] = lo_lane ? got1 : own1;
+                        bv[tau][2 * k + 1][0] = lo_lane ? own0 : got0;
+                        bv[tau][2 * k + 1][1] = lo_lane ? own1 : got1;
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        const int gamma = v * GPV + glow;
+                        if (gamma < NG) {
+                            const uint4 sz =
+                                *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
+                            const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
+                            const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
+                            const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
+                            const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
+                            const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
+                            zs[v] = fmaf(pa, e0.y, zs[v]);
+                            zs[v] = fmaf(pb, e1.y, zs[v]);
+                            zs[v] = fmaf(pc, e2.y, zs[v]);
+                            zs[v] = fmaf(pd, e3.y, zs[v]);
+                            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+                            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                            bv[tau][v][0] = h2bits(__floats2half2_rn(x0 - pm * f01.x, x1 - pm * f01.y));
+                            bv[tau][v][1] = h2bits(__floats2half2_rn(x2 - pm * f23.x, x3 - pm * f23.y));
+                        }
                     }
                 }
             }
@@ -545,7 +584,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
+    for (int v = 0; v < NZ; ++v) {
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 1);
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 2);
     }
@@ -558,7 +597,9 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
 #pragma unroll
     for (int mt = 0; mt < NKT; ++mt) {
         const int gamma = mt >> 1, v = gamma / GPV, gl = gamma % GPV;
-        const float zval = __shfl_sync(0xffffffffu, zs[v], 4 * (2 * (hD * GPV + gl)));
+        // the lane that summed variant v: piece 0 of its column, or (split) piece v & 1
+        const float zval = SPLIT ? __shfl_sync(0xffffffffu, zs[v >> 1], 4 * (2 * (hD * GPV + gl) + (v & 1)))
+                                 : __shfl_sync(0xffffffffu, zs[v], 4 * (2 * (hD * GPV + gl)));
         if (gl == i % GPV && hD < GQ) {
             const int ch0 = 16 * mt + r;
             const float sc0 = pow2i(24 - 2 * cls_of_pos(mt & 7));
