@@ -285,10 +285,13 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     float acc[NKT][4];
 #pragma unroll
     for (int mt = 0; mt < NKT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-    // With an even number of B variants (GQA), the two lanes that hold the hi
-    // and lo piece of one column split the variants: each computes p*s for
-    // half of them (both pieces) and receives its piece of the other half
-    // from its partner (lane ^ 4). zs[k] then sums variant 2k + piece.
+    // The two lanes that hold the hi and lo piece of one P.V column (lanes l
+    // and l ^ 4) share the work of p*s: with an even number of B variants
+    // (GQA) each computes half of the variants, with one variant (MHA) half of
+    // the four tokens, both pieces, and receives its piece of the other half
+    // from its partner. zs[k] sums variant 2k + piece (split variants) or the
+    // lane's two tokens of its one variant.
+    static_assert(NV == 1 || NV % 2 == 0, "one or an even number of B variants");
     constexpr bool SPLIT = NV % 2 == 0;
     constexpr int NZ = SPLIT ? NV / 2 : NV;
     static_assert(!SPLIT || NV * GPV == NG, "split variants cover every value group");
@@ -523,27 +526,24 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                         bv[tau][2 * k + 1][1] = lo_lane ? own1 : got1;
                     }
                 } else {
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        const int gamma = v * GPV + glow;
-                        if (gamma < NG) {
-                            const uint4 sz =
-                                *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
-                            const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
-                            const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                            const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
-                            const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
-                            const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
-                            zs[v] = fmaf(pa, e0.y, zs[v]);
-                            zs[v] = fmaf(pb, e1.y, zs[v]);
-                            zs[v] = fmaf(pc, e2.y, zs[v]);
-                            zs[v] = fmaf(pd, e3.y, zs[v]);
-                            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-                            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                            bv[tau][v][0] = h2bits(__floats2half2_rn(x0 - pm * f01.x, x1 - pm * f01.y));
-                            bv[tau][v][1] = h2bits(__floats2half2_rn(x2 - pm * f23.x, x3 - pm * f23.y));
-                        }
-                    }
+                    // one variant: this lane takes tokens 2i, 2i+1 (hi lane) or 2i+8, 2i+9 (lo lane)
+                    const bool lo_lane = (r & 1) != 0;
+                    const bool gv = glow < NG;           // columns past the value groups stay zero
+                    const int gamma = gv ? glow : 0;
+                    const uint2 sz = *reinterpret_cast<const uint2 *>(
+                        tb + tile_sz_off(D) + (((gamma * 4 + i) * 4) + (lo_lane ? 2 : 0)) * 4);
+                    const float2 ea = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
+                    const float2 eb = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
+                    const float pA = lo_lane ? pc : pa, pB = lo_lane ? pd : pb;
+                    const float xA = pA * ea.x, xB = pB * eb.x;
+                    if (gv) zs[0] = fmaf(pB, eb.y, fmaf(pA, ea.y, zs[0]));
+                    const __half2 h = __floats2half2_rn(xA, xB);
+                    const float2 f = __half22float2(h);
+                    const uint32_t hi = h2bits(h), lo = h2bits(__floats2half2_rn(xA - f.x, xB - f.y));
+                    // hi lane: keeps hi of (2i, 2i+1), gets hi of (2i+8, 2i+9); lo lane the lo pieces
+                    const uint32_t got = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 4);
+                    bv[tau][0][0] = gv ? (lo_lane ? got : hi) : 0u;
+                    bv[tau][0][1] = gv ? (lo_lane ? lo : got) : 0u;
                 }
             }
         }
@@ -587,6 +587,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     for (int v = 0; v < NZ; ++v) {
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 1);
         zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 2);
+        if constexpr (!SPLIT) zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], 4);   // the pair's tokens
     }
     float *pb = a.part + slot * GQ * (D + 2);
     if (r == 0 && i < GQ) {
