@@ -51,6 +51,9 @@ def lib():
             i32, i64, u16 = C.c_int, C.c_longlong, C.c_uint16
             L.orc_create.restype = P
             L.orc_create.argtypes = [i32] * 7
+            L.orc_create_policy.restype = P
+            L.orc_create_policy.argtypes = [i32] * 8
+            L.orc_export_cold.argtypes = [P, i32, P, P, P]
             L.orc_destroy.argtypes = [P]
             L.orc_append.argtypes = [P, P, P]
             L.orc_prefill.argtypes = [P, P, P, i32]
@@ -125,11 +128,15 @@ def quant_group(x) -> tuple[int, int, np.ndarray]:
 # ---------------------------------------------------------------- the cache
 
 class OracleCache:
-    """The oracle's OTT cache: same create/prefill/append/decode calls as the library."""
+    """The oracle's OTT cache: same create/prefill/append/decode calls as the library.
 
-    def __init__(self, B, Hq, Hkv, d, G, R, P):
+    ``cold=None`` writes displaced pool tokens back into the new block;
+    ``cold=C`` (an int >= 0) is the cold-pool policy with capacity C."""
+
+    def __init__(self, B, Hq, Hkv, d, G, R, P, cold=None):
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
-        self._h = lib().orc_create(B, Hq, Hkv, d, G, R, P)
+        self.cold = cold
+        self._h = lib().orc_create_policy(B, Hq, Hkv, d, G, R, P, -1 if cold is None else int(cold))
         if not self._h:
             raise ValueError("invalid OTT shape")
 
@@ -217,4 +224,11 @@ class OracleCache:
         ptrs = [_ptr(e[k]) if e[k].size else None for k in order]
         lib().orc_export_unit(self._h, u, *ptrs)
         e.update(T=T, nf=nf, tail=nt, npool=npool)
+        if self.cold is not None:
+            Cc = int(self.cold)
+            cidx = np.zeros(max(Cc, 1), np.int32)
+            ck = np.zeros((max(Cc, 1), d), np.uint16)
+            cv = np.zeros((max(Cc, 1), d), np.uint16)
+            n = lib().orc_export_cold(self._h, u, _ptr(cidx), _ptr(ck), _ptr(cv))
+            e.update(ncold=n, cidx=cidx[:Cc], ck=ck[:Cc], cv=cv[:Cc])
         return e

@@ -49,6 +49,14 @@
  *      token to every sequence, and R1 applies to each unit on its own. The
  *      pages state the method for one sequence; this is that method applied
  *      to each sequence of a batch independently.
+ *  R11 The cold-pool policy ([blog] sec. 3.2, the alternative to writing a
+ *      displaced token back): with cold capacity C, the pool tokens that a
+ *      flush displaces do not join the new block; they enter an fp16
+ *      first-in-first-out "cold" pool, in ascending token order. When it
+ *      holds more than C tokens, the ones that entered first are discarded
+ *      and no store holds them any more. The new block is the group's
+ *      tokens that did not enter the pool. Decode attends the cold pool like
+ *      the outlier pool; discarded tokens are not attended.
  *
  * Floating point: decisions that yield integers or stored bits (norms,
  * scales, zeros, codes) are taken in fp32 exactly as the library takes them.
@@ -211,18 +219,24 @@ typedef struct {
     /* quantized blocks, one per flush */
     int nb, nb_cap;
     orc_block *blk;
+    /* cold pool (R11), oldest first */
+    int cold_n;
+    int32_t *cold_idx;           /* [C] */
+    uint16_t *cold_k, *cold_v;   /* [C][d] */
 } orc_unit;
 
 typedef struct {
     int B, Hq, Hkv, d, G, R, P;
     long long T;        /* appends plus the longest prefill (0: empty) */
     long long *Tb;      /* [B] tokens seen by each sequence (R10) */
+    int C;              /* cold-pool capacity (R11); -1: displaced tokens are written back */
     orc_unit *u;        /* [B*Hkv] */
 } orc_cache;
 
 typedef struct {
     float norm;
     int32_t idx;
+    int from_pool;      /* 1: the candidate was in the pool before this flush */
     const uint16_t *k, *v;
 } orc_cand;
 
@@ -255,19 +269,23 @@ void orc_destroy(void *hp)
             free(b->vcode); free(b->vs); free(b->vz);
         }
         free(u->blk);
+        free(u->cold_idx); free(u->cold_k); free(u->cold_v);
     }
     free(h->u);
     free(h->Tb);
     free(h);
 }
 
-void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
+/* C < 0: displaced pool tokens are written back (R5); C >= 0: the cold-pool
+ * policy with capacity C (R11). */
+void *orc_create_policy(int B, int Hq, int Hkv, int d, int G, int R, int P, int C)
 {
     if (B < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv || d < 32 || d % 32 ||
         G < 1 || R < 0 || P < 0)
         return NULL;
     orc_cache *h = (orc_cache *)calloc(1, sizeof(orc_cache));
     h->B = B; h->Hq = Hq; h->Hkv = Hkv; h->d = d; h->G = G; h->R = R; h->P = P;
+    h->C = C < 0 ? -1 : C;
     h->u = (orc_unit *)calloc((size_t)B * Hkv, sizeof(orc_unit));
     h->Tb = (long long *)calloc((size_t)B, sizeof(long long));
     for (int i = 0; i < B * Hkv; ++i) {
@@ -280,8 +298,40 @@ void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
         u->pool_norm = (float *)calloc(P + 1, sizeof(float));
         u->pool_k = (uint16_t *)calloc((size_t)(P + 1) * d, 2);
         u->pool_v = (uint16_t *)calloc((size_t)(P + 1) * d, 2);
+        if (h->C >= 0) {
+            u->cold_idx = (int32_t *)calloc(h->C + 1, sizeof(int32_t));
+            u->cold_k = (uint16_t *)calloc((size_t)(h->C + 1) * d, 2);
+            u->cold_v = (uint16_t *)calloc((size_t)(h->C + 1) * d, 2);
+        }
     }
     return h;
+}
+
+void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
+{
+    return orc_create_policy(B, Hq, Hkv, d, G, R, P, -1);
+}
+
+/* R11: the displaced pool tokens ev[0..n) (ascending token order) enter the
+ * cold pool one by one; while it is full, the token that entered first
+ * leaves. */
+static void cold_push(orc_cache *h, orc_unit *u, const orc_cand *ev, int n)
+{
+    const int d = h->d;
+    if (h->C == 0)
+        return;
+    for (int e = 0; e < n; ++e) {
+        if (u->cold_n == h->C) {
+            memmove(u->cold_idx, u->cold_idx + 1, sizeof(int32_t) * (h->C - 1));
+            memmove(u->cold_k, u->cold_k + d, (size_t)(h->C - 1) * d * 2);
+            memmove(u->cold_v, u->cold_v + d, (size_t)(h->C - 1) * d * 2);
+            u->cold_n -= 1;
+        }
+        u->cold_idx[u->cold_n] = ev[e].idx;
+        memcpy(u->cold_k + (size_t)u->cold_n * d, ev[e].k, (size_t)d * 2);
+        memcpy(u->cold_v + (size_t)u->cold_n * d, ev[e].v, (size_t)d * 2);
+        u->cold_n += 1;
+    }
 }
 
 /* The flush (R1, R3-R7): the oldest G residual tokens meet the pool. */
@@ -293,6 +343,7 @@ static void flush_unit(orc_cache *h, orc_unit *u)
     for (int i = 0; i < u->pool_n; ++i) {
         cand[i].norm = u->pool_norm[i];
         cand[i].idx = u->pool_idx[i];
+        cand[i].from_pool = 1;
         cand[i].k = u->pool_k + (size_t)i * d;
         cand[i].v = u->pool_v + (size_t)i * d;
     }
@@ -301,14 +352,31 @@ static void flush_unit(orc_cache *h, orc_unit *u)
         c->k = u->tail_k + (size_t)i * d;
         c->v = u->tail_v + (size_t)i * d;
         c->idx = u->tail_idx[i];
+        c->from_pool = 0;
         c->norm = orc_norm(c->k, d);
     }
     /* R4: order by (norm, index); the first P stay in the pool. */
     qsort(cand, ncand, sizeof(orc_cand), cand_cmp_norm);
     const int keep = ncand < P ? ncand : P;
-    const int c = ncand - keep;
+    int c = ncand - keep;
     /* R5: the rest, in token order, become the new block. */
     qsort(cand + keep, c, sizeof(orc_cand), cand_cmp_idx);
+    /* R11: under the cold-pool policy the displaced pool tokens leave the
+     * block for the cold pool; the group's tokens keep their order. */
+    orc_cand *ev = NULL;
+    int nev = 0;
+    if (h->C >= 0) {
+        ev = (orc_cand *)malloc(sizeof(orc_cand) * (c + 1));
+        int nblk = 0;
+        for (int t = 0; t < c; ++t) {
+            const orc_cand x = cand[keep + t];
+            if (x.from_pool)
+                ev[nev++] = x;
+            else
+                cand[keep + nblk++] = x;
+        }
+        c = nblk;
+    }
 
     if (u->nb == u->nb_cap) {
         u->nb_cap = u->nb_cap ? 2 * u->nb_cap : 16;
@@ -351,6 +419,9 @@ static void flush_unit(orc_cache *h, orc_unit *u)
         ni[i] = cand[i].idx;
         nn[i] = cand[i].norm;
     }
+    /* the displaced tokens' rows still live in the old pool arrays */
+    if (ev)
+        cold_push(h, u, ev, nev);
     memcpy(u->pool_k, nk, (size_t)keep * d * 2);
     memcpy(u->pool_v, nv, (size_t)keep * d * 2);
     memcpy(u->pool_idx, ni, sizeof(int32_t) * keep);
@@ -365,6 +436,7 @@ static void flush_unit(orc_cache *h, orc_unit *u)
 
     free(nk); free(nv); free(ni); free(nn);
     free(bk); free(bv);
+    free(ev);
     free(cand);
 }
 
@@ -483,6 +555,12 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
             acc += q[c] * orc_h2f(u->pool_k[(size_t)t * d + c]);
         score[m++] = sigma * acc;
     }
+    for (int t = 0; t < u->cold_n; ++t) {       /* R11 */
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += q[c] * orc_h2f(u->cold_k[(size_t)t * d + c]);
+        score[m++] = sigma * acc;
+    }
 
     /* softmax over the concatenated scores */
     double mx = -INFINITY;
@@ -520,6 +598,11 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
         double p = score[m++];
         for (int c = 0; c < d; ++c)
             out[c] += p * orc_h2f(u->pool_v[(size_t)t * d + c]);
+    }
+    for (int t = 0; t < u->cold_n; ++t) {
+        double p = score[m++];
+        for (int c = 0; c < d; ++c)
+            out[c] += p * orc_h2f(u->cold_v[(size_t)t * d + c]);
     }
     for (int c = 0; c < d; ++c)
         out[c] /= sum;
@@ -643,4 +726,29 @@ int orc_export_unit(void *hp, int ui, int32_t *bcount, int32_t *bidx, uint8_t *k
     }
     free(ord);
     return 0;
+}
+
+/* R11: the cold pool of unit u, oldest first. Any pointer may be NULL.
+ * cidx [C] int32 (-1 padded), ck, cv [C][d] fp16 bits (zero padded).
+ * Returns the number of cold tokens, or -1 without the cold-pool policy. */
+int orc_export_cold(void *hp, int ui, int32_t *cidx, uint16_t *ck, uint16_t *cv)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (h->C < 0)
+        return -1;
+    const orc_unit *u = &h->u[ui];
+    const int d = h->d;
+    for (int i = 0; i < h->C; ++i) {
+        const int valid = i < u->cold_n;
+        if (cidx) cidx[i] = valid ? u->cold_idx[i] : -1;
+        if (ck) {
+            if (valid) memcpy(ck + (size_t)i * d, u->cold_k + (size_t)i * d, (size_t)d * 2);
+            else memset(ck + (size_t)i * d, 0, (size_t)d * 2);
+        }
+        if (cv) {
+            if (valid) memcpy(cv + (size_t)i * d, u->cold_v + (size_t)i * d, (size_t)d * 2);
+            else memset(cv + (size_t)i * d, 0, (size_t)d * 2);
+        }
+    }
+    return u->cold_n;
 }

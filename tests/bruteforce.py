@@ -46,6 +46,32 @@ def state(keys16: np.ndarray, G: int, R: int, P: int):
     return blocks, sorted(prev), list(range(nf * G, T)), n
 
 
+def state_cold(keys16: np.ndarray, G: int, R: int, P: int, C: int):
+    """Membership under the cold-pool policy (capacity C) after T appends.
+
+    Stated globally from the same pool sets: pool_j is the P smallest pairs
+    among all tokens flushed by flush j; the tokens evicted at flush j are
+    pool_{j-1} - pool_j, ranked by (j, index); the cold pool holds the last C
+    of that ranking, oldest first; block j is group_j - pool_j.
+    Returns (blocks, pool, tail, cold, dropped).
+    """
+    T = len(keys16)
+    nf = flush_count(T, G, R)
+    n = norms_fp32(keys16[: nf * G]) if nf else np.zeros(0, np.float32)
+    order_key = lambda t: (float(n[t]), t)
+    prev: set[int] = set()
+    blocks, evicted = [], []
+    for j in range(nf):
+        pool_j = set(sorted(range((j + 1) * G), key=order_key)[:P])
+        group = set(range(j * G, (j + 1) * G))
+        blocks.append(sorted(group - pool_j))
+        evicted += sorted(prev - pool_j)
+        prev = pool_j
+    cold = evicted[max(0, len(evicted) - C):] if C > 0 else []
+    dropped = sorted(set(evicted) - set(cold))
+    return blocks, sorted(prev), list(range(nf * G, T)), cold, dropped
+
+
 def np_quant(x32: np.ndarray, axis: int):
     """Vectorized restatement of the 2-bit rule along ``axis`` (cross-check only)."""
     mn = x32.min(axis=axis, keepdims=True)
