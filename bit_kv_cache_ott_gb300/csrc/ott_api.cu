@@ -347,7 +347,10 @@ int ott_check_device(ott_cache *c) {
     int flag = 0;
     e = cudaMemcpy(&flag, c->ctl + 1, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail_cuda(c, e);
-    return flag ? OTT_ERR_DEVICE : OTT_OK;
+    if (!flag) return OTT_OK;
+    // a kernel gave up part of its work: the state can no longer be trusted
+    c->poisoned = 1;
+    return OTT_ERR_DEVICE;
 }
 
 int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst) {

@@ -205,7 +205,9 @@ int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst);
 
 /*
  * Wait for the device and read the cache's device status word: OTT_OK, or
- * OTT_ERR_DEVICE if a kernel gave up a bounded wait, or OTT_ERR_CUDA.
+ * OTT_ERR_DEVICE if a kernel gave up a bounded wait, or OTT_ERR_CUDA. After
+ * OTT_ERR_DEVICE the handle is poisoned (later calls return OTT_ERR_STATE):
+ * the kernel that gave up left its part of the state or the output unwritten.
  */
 int ott_check_device(ott_cache *c);
 
