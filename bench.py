@@ -160,6 +160,18 @@ def step_bytes(w, Ts) -> int:
     return sum(metrics.decode_bytes(t, 1, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) for t in Ts)
 
 
+def cold_of(w):
+    """The cold-pool capacity of a workload, or None (displaced tokens written back)."""
+    return w.cold if w.cold >= 0 else None
+
+
+def cold_quant_bytes(c) -> int:
+    """Cold-pool policy: bytes of a cache's quantized blocks and cold pool as
+    the device holds them now (their sizes depend on the data)."""
+    bc, nc = c.cold_sizes()
+    return sum(metrics.cold_unit_bytes(bc[u], nc[u], c.d) for u in range(len(nc)))
+
+
 def _oracle_prefill(orc, w, lens):
     K, V = synth.prefill_kv(w)
     if w.ragged:
@@ -176,7 +188,7 @@ def oracle_rate(w, steps: int, warmup: int, units_sample: int):
     from oracle.oracle import OracleCache
     Bs = max(1, min(w.B, units_sample // w.Hkv))
     ws = w.with_(B=Bs)
-    orc = OracleCache(ws.B, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P)
+    orc = OracleCache(ws.B, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P, cold=cold_of(ws))
     lens = synth.seq_lens(w)
     _oracle_prefill(orc, ws, lens[:Bs])
     inputs = [synth.step_kvq(ws, s) for s in range(warmup + steps)]
@@ -216,7 +228,7 @@ def _oracle_worker(task):
     w = synth.WORKLOADS[name]
     g = w.Hq // w.Hkv
     ws = w.with_(B=1, Hkv=hk, Hq=g * hk, seed=seed)
-    orc = OracleCache(1, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P)
+    orc = OracleCache(1, ws.Hq, ws.Hkv, ws.d, ws.G, ws.R, ws.P, cold=cold_of(ws))
     _oracle_prefill(orc, ws, [length])
     inputs = [synth.step_kvq(ws, s) for s in range(warmup + steps)]
     for s in range(warmup):
@@ -305,7 +317,8 @@ def run_ours(args, w):
     caches = []
     lens = synth.seq_lens(wr)
     for layer in range(w.layers):
-        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged)
+        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged,
+                         cold=cold_of(w))
         K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
         if w.ragged:
             c.prefill_lens(K, V, lens)
@@ -344,6 +357,11 @@ def run_ours(args, w):
     flushes = 0
     Ts = [caches[0].seq_counts(b)[0] for b in range(w.B)]
     T0 = max(Ts)
+    # cold-pool policy: the quantized and cold stores' sizes are read before
+    # and after the timed region and taken as linear in the flushes between
+    cold_q0 = [cold_quant_bytes(c) for c in caches] if w.cold >= 0 else None
+    cold_steps = []   # (layer, hot bytes, flush steps so far) per layer-step
+    flush_steps = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
@@ -353,6 +371,7 @@ def run_ours(args, w):
             k, v, q = dev_in[(W_steps + s) % n_distinct]
             Ts = [t + 1 for t in Ts]
             flush_launch = any((t - w.R) % w.G == 0 and t >= w.G + w.R for t in Ts)   # some sequence flushes now
+            flush_steps += int(flush_launch)
             for li, c in enumerate(caches):
                 c.append(k, v, stream)
                 flushes += int(flush_launch)
@@ -360,12 +379,20 @@ def run_ours(args, w):
                 ev[0].record(stream)
                 c.decode_attn(q, out, stream)
                 ev[1].record(stream)
-                dec_bytes += step_bytes(w, Ts)
+                if cold_q0 is None:
+                    dec_bytes += step_bytes(w, Ts)
+                else:
+                    cold_steps.append((li, metrics.hot_bytes(Ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P),
+                                       flush_steps))
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
     ms = e0.elapsed_time(e1)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec_events)
+    if cold_q0 is not None:
+        cold_q1 = [cold_quant_bytes(c) for c in caches]
+        nfl = max(1, flush_steps)
+        dec_bytes = sum(hot + cold_q0[li] + (cold_q1[li] - cold_q0[li]) * f / nfl for li, hot, f in cold_steps)
     launches = K_steps * w.layers * 3 + flushes   # append + decode + combine, plus flushes
     ms = max_over_ranks(ms, dev)
     for c in caches:
@@ -454,6 +481,8 @@ def run_ours(args, w):
             "vs_baseline": None, "dtype": "fp16 storage, fp32 accumulation", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
                        "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
+                       **({"cold": w.cold, "cold_bytes": "block and cold-pool sizes read from the device "
+                           "before and after the timed region, linear in between"} if w.cold >= 0 else {}),
                        **({"ragged_lens": {"min": min(lens), "max": max(lens),
                                            "mean": round(sum(lens) / len(lens), 1)}} if w.ragged else {}),
                        "l2": (f"cache {cache_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"

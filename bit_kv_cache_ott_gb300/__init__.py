@@ -37,7 +37,7 @@ class StateExport(C.Structure):
                 ("bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tk", "tv", "pidx", "pnorm", "pk", "pv")]
 
 
-SYMBOLS = ("ott_create", "ott_create_ragged", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
+SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
            "ott_decode_attn", "ott_decode_attn_static", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
            "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str")
 
@@ -60,6 +60,8 @@ def load(build_if_missing: bool = False):
     P, i32, i64 = C.c_void_p, C.c_int, C.c_longlong
     L.ott_create.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_create_ragged.argtypes = [i32] * 8 + [C.POINTER(P)]
+    L.ott_create_cold.argtypes = [i32] * 9 + [C.POINTER(P)]
+    L.ott_export_cold.argtypes = [P, i32, i32, P, P, P, P, P]
     L.ott_destroy.argtypes = [P]
     L.ott_prefill.argtypes = [P, P, P, i32, P]
     L.ott_prefill_lens.argtypes = [P, P, P, C.POINTER(i32), i32, P]
@@ -104,17 +106,25 @@ def _stream(stream) -> int:
 class OTTCache:
     """One OTT cache (one attention layer): ``create/prefill/append/decode_attn/destroy``.
     ``ragged=True`` creates it with ``ott_create_ragged`` so that ``prefill_lens``
-    can give every sequence its own length."""
+    can give every sequence its own length. ``cold=C`` creates it with
+    ``ott_create_cold``: displaced pool tokens go to a first-in-first-out
+    fp16 cold pool of C slots instead of the new block."""
 
-    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False):
+    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False, cold=None):
         L = load()
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
         self.max_tokens = max_tokens
         self.ragged = ragged
+        self.cold = cold
         h = C.c_void_p()
-        create = L.ott_create_ragged if ragged else L.ott_create
-        _check(create(B, Hq, Hkv, d, G, R, P, max_tokens, C.byref(h)),
-               "ott_create_ragged" if ragged else "ott_create")
+        if cold is not None:
+            if ragged:
+                raise ValueError("the cold-pool policy takes sequences of one length")
+            _check(L.ott_create_cold(B, Hq, Hkv, d, G, R, P, int(cold), max_tokens, C.byref(h)), "ott_create_cold")
+        else:
+            create = L.ott_create_ragged if ragged else L.ott_create
+            _check(create(B, Hq, Hkv, d, G, R, P, max_tokens, C.byref(h)),
+                   "ott_create_ragged" if ragged else "ott_create")
         self._h = h
 
     def close(self):
@@ -179,6 +189,16 @@ class OTTCache:
                "ott_get_seq_counts")
         return T.value, nf.value, tail.value, npool.value
 
+    def cold_sizes(self):
+        """Cold-pool policy: (block sizes [U][nf], cold-pool sizes [U]) from the device."""
+        import numpy as np
+        U, nf = self.B * self.Hkv, self.counts()[1]
+        bc = np.zeros((U, max(nf, 1)), np.int32)
+        nc = np.zeros(U, np.int32)
+        _check(load().ott_export_cold(self._h, 0, U, bc.ctypes.data, nc.ctypes.data, None, None, None),
+               "ott_export_cold")
+        return bc[:, :nf], nc
+
     def block_count(self, j: int) -> int:
         rc = load().ott_block_count(self._h, j)
         if rc < 0:
@@ -210,6 +230,17 @@ class OTTCache:
         )
         st = StateExport(**{k: (v.ctypes.data if v.size else None) for k, v in e.items()})
         _check(load().ott_export_state(self._h, u0, nu, C.byref(st)), "ott_export_state")
-        e["bcount"] = np.array([self.block_count(j) for j in range(nf)], np.int32)
+        if self.cold is None:
+            e["bcount"] = np.array([self.block_count(j) for j in range(nf)], np.int32)
+        else:
+            Cc = int(self.cold)
+            bc = np.zeros((nu, max(nf, 1)), np.int32)
+            nc = np.zeros(nu, np.int32)
+            ci = np.zeros((nu, max(Cc, 1)), np.int32)
+            ck = np.zeros((nu, max(Cc, 1), d), np.uint16)
+            cv = np.zeros((nu, max(Cc, 1), d), np.uint16)
+            _check(load().ott_export_cold(self._h, u0, nu, bc.ctypes.data, nc.ctypes.data, ci.ctypes.data,
+                                          ck.ctypes.data, cv.ctypes.data), "ott_export_cold")
+            e.update(bcount=bc[:, :nf], ncold=nc, cidx=ci[:, :Cc], ck=ck[:, :Cc], cv=cv[:, :Cc])
         e.update(T=T, nf=nf, tail=nt, npool=npool)
         return e

@@ -35,7 +35,7 @@ bool flush_due_seq(const ott_cache *c, int b) {
 int flushes_after(const ott_cache *c, long long T) { return T >= c->G + c->R ? (int)((T - c->R) / c->G) : 0; }
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 ott_cache **out);
+                 int cold, ott_cache **out);
 
 }  // namespace
 
@@ -55,7 +55,15 @@ const char *ott_status_str(int code) {
 }
 
 int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
-    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, out);
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, -1, out);
+}
+
+int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C, int max_tokens, ott_cache **out) {
+    if (C < 0 || C > OTT_COLD_MAX) {
+        if (out) *out = nullptr;
+        return OTT_ERR_INVALID;
+    }
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, C, out);
 }
 
 int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
@@ -63,7 +71,7 @@ int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int ma
         if (out) *out = nullptr;
         return OTT_ERR_INVALID;
     }
-    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 1, out);
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 1, -1, out);
 }
 
 }  // extern "C"
@@ -71,7 +79,7 @@ int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int ma
 namespace {
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 ott_cache **out) {
+                 int cold, ott_cache **out) {
     if (!out) return OTT_ERR_INVALID;
     *out = nullptr;
     if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
@@ -127,6 +135,10 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t sz_pool = U * (size_t)P * d * 2;
     const size_t sz_pn = U * (size_t)P * 4;
     const size_t sz_part = (size_t)nwarps * maxu_alloc * 2 * gq * (d + 2) * 4;
+    c->cold = cold;
+    const size_t Cs = cold > 0 ? (size_t)cold : 0;
+    const size_t sz_cold = U * Cs * d * 2, sz_cidx = U * Cs * 4;
+    const size_t sz_cmeta = cold >= 0 ? U * 8 : 0, sz_bcnt = cold >= 0 ? U * c->NB * 4 : 0;
     size_t off = 0;
     const size_t o_blk = off; off = round_up(off + sz_blk, 256);
     const size_t o_bidx = off; off = round_up(off + sz_bidx, 256);
@@ -138,6 +150,11 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t o_pi = off; off = round_up(off + sz_pn, 256);
     const size_t o_part = off; off = round_up(off + sz_part, 256);
     const size_t o_ctl = off; off = round_up(off + 64, 256);
+    const size_t o_ck = off; off = round_up(off + sz_cold, 256);
+    const size_t o_cv = off; off = round_up(off + sz_cold, 256);
+    const size_t o_ci = off; off = round_up(off + sz_cidx, 256);
+    const size_t o_cm = off; off = round_up(off + sz_cmeta, 256);
+    const size_t o_bc = off; off = round_up(off + sz_bcnt, 256);
     c->mem_bytes = off;
 
     // Host-side fault injection for tests: OTT_FAULT=alloc makes the device
@@ -166,6 +183,11 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->pidx = reinterpret_cast<int32_t *>(base + o_pi);
     c->part = reinterpret_cast<float *>(base + o_part);
     c->ctl = reinterpret_cast<int *>(base + o_ctl);
+    c->ck = sz_cold ? reinterpret_cast<__half *>(base + o_ck) : nullptr;
+    c->cv = sz_cold ? reinterpret_cast<__half *>(base + o_cv) : nullptr;
+    c->cidx = sz_cidx ? reinterpret_cast<int32_t *>(base + o_ci) : nullptr;
+    c->cmeta = sz_cmeta ? reinterpret_cast<int *>(base + o_cm) : nullptr;
+    c->bcnt = sz_bcnt ? reinterpret_cast<int32_t *>(base + o_bc) : nullptr;
     e = cudaMemset(mem, 0, c->mem_bytes);
     if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -335,6 +357,7 @@ int ott_block_count(const ott_cache *c, int j) {
     if (c->ragged)
         for (int b = 0; b < c->B; ++b) nf = c->nfb[b] > nf ? c->nfb[b] : nf;
     if (j < 0 || j >= nf) return OTT_ERR_INVALID;
+    if (c->cold >= 0) return OTT_ERR_STATE;   // sizes differ per unit: ott_export_cold
     return block_count(c->P, c->G, j);
 }
 
@@ -450,6 +473,52 @@ int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst) 
                     if (valid) std::memcpy(dst->pv + o * d, pv.data() + so * d, (size_t)d * 2);
                     else std::memset(dst->pv + o * d, 0, (size_t)d * 2);
                 }
+            }
+        }
+    }
+    return OTT_OK;
+}
+
+int ott_export_cold(ott_cache *c, int u0, int nu, int32_t *bcount, int32_t *ncold, int32_t *cidx,
+                    uint16_t *ck, uint16_t *cv) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || c->cold < 0) return OTT_ERR_STATE;
+    if (u0 < 0 || nu < 0 || u0 + nu > c->U) return OTT_ERR_INVALID;
+    if (nu == 0) return OTT_OK;
+    const int d = c->d, C = c->cold, nf = c->nf;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    if (bcount && nf > 0)
+        for (int uu = 0; uu < nu; ++uu) {
+            e = cudaMemcpy(bcount + (size_t)uu * nf, c->bcnt + (size_t)(u0 + uu) * c->NB, (size_t)nf * 4,
+                           cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return fail_cuda(c, e);
+        }
+    std::vector<int> meta((size_t)nu * 2);
+    e = cudaMemcpy(meta.data(), c->cmeta + (size_t)u0 * 2, meta.size() * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    std::vector<int32_t> ci((size_t)nu * C);
+    std::vector<uint16_t> hk((size_t)nu * C * d), hv(hk.size());
+    if (C > 0) {
+        e = cudaMemcpy(ci.data(), c->cidx + (size_t)u0 * C, ci.size() * 4, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(hk.data(), c->ck + (size_t)u0 * C * d, hk.size() * 2, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(hv.data(), c->cv + (size_t)u0 * C * d, hv.size() * 2, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
+    for (int uu = 0; uu < nu; ++uu) {
+        const int n = C > 0 ? meta[2 * uu] : 0, head = C > 0 ? meta[2 * uu + 1] : 0;
+        if (ncold) ncold[uu] = n;
+        for (int x = 0; x < C; ++x) {
+            const bool valid = x < n;
+            const size_t so = (size_t)uu * C + (valid ? (head + x) % C : 0), o = (size_t)uu * C + x;
+            if (cidx) cidx[o] = valid ? ci[so] : -1;
+            if (ck) {
+                if (valid) std::memcpy(ck + o * d, hk.data() + so * d, (size_t)d * 2);
+                else std::memset(ck + o * d, 0, (size_t)d * 2);
+            }
+            if (cv) {
+                if (valid) std::memcpy(cv + o * d, hv.data() + so * d, (size_t)d * 2);
+                else std::memset(cv + o * d, 0, (size_t)d * 2);
             }
         }
     }

@@ -127,6 +127,11 @@ struct DecodeArgs {
     int MAXU;           // units a warp's range can touch
     float sl2;          // softmax scale 1/sqrt(d) times log2(e)
     int B;              // sequences (the ragged table's length)
+    // cold-pool policy: data-dependent block sizes and a fourth, fp16 store
+    const int32_t *bcnt;       // [U][NB] valid tokens of each block
+    const __half *ck, *cv;     // [U][C][d] cold pool, a ring used first in, first out
+    const int *cmeta;          // [U][2]: tokens in the cold pool, slot of the oldest
+    int C;
 };
 
 template <int D, int GQ>
@@ -146,7 +151,11 @@ struct Cfg {
     static_assert(2 * 8 * (D + 8) * 2 <= STAGE, "fp16 sub-tile staging must fit a stage buffer");
 };
 
-__device__ __forceinline__ int block_cnt(const DecodeArgs &a, int j) {
+// Valid tokens of block j of unit u: fixed by (P, G, j) when displaced pool
+// tokens are written back, written by the flush under the cold-pool policy.
+template <bool CO>
+__device__ __forceinline__ int block_cnt(const DecodeArgs &a, int u, int j) {
+    if constexpr (CO) return __ldg(a.bcnt + (size_t)u * a.NB + j);
     return j >= a.jfull ? a.G : block_count(a.P, a.G, j);
 }
 
@@ -244,7 +253,7 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 
 // ---------------------------------------------------------------- quantized segment
 // Blocks [j0, j1) of unit u; the partial goes to part[slot].
-template <int D, int GQ>
+template <int D, int GQ, bool CO>
 __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
                               int lane) {
@@ -253,13 +262,13 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     constexpr int KSZ = ksz_bytes(D), TB = tile_bytes(D);
     const int r = lane >> 2, i = lane & 3;
 
-    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < block_cnt(a, j); };
+    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < block_cnt<CO>(a, u, j); };
     int lj = j0, lk = 0;
     while (lj < j1 && !active(lj, lk)) { ++lj; lk = 0; }
     int cj_ = lj, ck_ = lk;   // next chunk to consume
     auto issue = [&](int j, int k, int st) {
         if (lane == 0) {
-            const int vt = (block_cnt(a, j) + TILE - 1) / TILE;
+            const int vt = (block_cnt<CO>(a, u, j) + TILE - 1) / TILE;
             const int t0 = k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
             const uint8_t *bsrc = a.blk + ((size_t)u * a.NB + j) * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
@@ -319,7 +328,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
             return false;
         }
         phase ^= 1u << st;
-        const int cj = block_cnt(a, cj_), vt = (cj + TILE - 1) / TILE;
+        const int cj = block_cnt<CO>(a, u, cj_), vt = (cj + TILE - 1) / TILE;
         const int t0 = ck_ * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
 
         if (ck_ == 0) {
@@ -646,15 +655,25 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-template <int D, int GQ>
+// Under the cold-pool policy the fp16 tokens continue with the cold pool
+// (token f >= ntail + npool: its (f - ntail - npool)-th oldest entry); its
+// size is read on the device, and the host sizes the items for C entries.
+template <int D, int GQ, bool CO>
 __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slot, int u, int c0, int c1,
                              uint8_t *stg0, uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
     constexpr int NKT = D / 16;
     constexpr int RS = D + 8;                 // padded row stride (halves)
     constexpr int SUB = 8;                    // tokens per sub-tile
     const int r = lane >> 2, i = lane & 3;
-    const int nfp = ui.ntail + ui.npool;
-    const int fb = c0 * FP16_CHUNK, fe = min(c1 * FP16_CHUNK, nfp);
+    int ncold = 0, chead = 0;
+    if constexpr (CO) {
+        if (a.C > 0) {
+            ncold = __ldg(a.cmeta + 2 * u);
+            chead = __ldg(a.cmeta + 2 * u + 1);
+        }
+    }
+    const int nhot = ui.ntail + ui.npool, nfp = nhot + ncold;
+    const int fb = c0 * FP16_CHUNK, fe = max(fb, min(c1 * FP16_CHUNK, nfp));
     const int nsub = (fe - fb + SUB - 1) / SUB;
 
     auto row_ptr = [&](int f, bool val) -> const __half * {
@@ -663,6 +682,13 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
             int s = ui.ring_start + f;   // f < ntail < ring
             if (s >= a.ring) s -= a.ring;
             return base + ((size_t)u * a.ring + s) * D;
+        }
+        if constexpr (CO) {
+            if (f >= nhot) {
+                int s = chead + (f - nhot);   // f - nhot < ncold <= C
+                if (s >= a.C) s -= a.C;
+                return (val ? a.cv : a.ck) + ((size_t)u * a.C + s) * D;
+            }
         }
         return (val ? a.pv : a.pk) + ((size_t)u * a.P + (f - ui.ntail)) * D;
     };
@@ -777,7 +803,7 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
     return true;
 }
 
-template <int D, int GQ, bool RG>
+template <int D, int GQ, bool RG, bool CO>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, const __grid_constant__ TableT<RG> st) {
     using C = Cfg<D, GQ>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -812,13 +838,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
         const int off = (int)(x - ubase);
         if (off < ui.Sf) {
             const int end = (int)min(x1 - ubase, (long long)ui.Sf);
-            if (!fp16_segment<D, GQ>(a, ui, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars,
+            if (!fp16_segment<D, GQ, CO>(a, ui, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars,
                                      phase, qsm, lane))
                 return;
             x = ubase + end;
         } else {
             const int end = (int)min(x1 - ubase, (long long)ui.Iu);
-            if (!quant_segment<D, GQ>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
+            if (!quant_segment<D, GQ, CO>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
                                       stg1, bars, phase, qsm, qhl, lane))
                 return;
             x = ubase + end;
@@ -964,14 +990,21 @@ inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf) {
     e.ring_start = (int)(tail_start % c->ring);
     e.ntail = (int)(T - tail_start);
     e.npool = pool_after(c->P, c->G, nf);
-    e.Sf = (e.ntail + e.npool + FP16_CHUNK - 1) / FP16_CHUNK;
+    // the cold pool's size is known on the device only: items for all C slots
+    const int ncold_max = c->cold > 0 ? c->cold : 0;
+    e.Sf = (e.ntail + e.npool + ncold_max + FP16_CHUNK - 1) / FP16_CHUNK;
     e.Iu = e.Sf + nf;
     return e;
 }
 
-template <int D, int GQ, bool RG>
+template <int D, int GQ, bool RG, bool CO>
 cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
     DecodeArgs a;
+    a.bcnt = c->bcnt;
+    a.ck = c->ck;
+    a.cv = c->cv;
+    a.cmeta = c->cmeta;
+    a.C = c->cold;
     a.blk = c->blk;
     a.blk_bytes = c->blk_bytes;
     a.NB = c->NB;
@@ -1020,7 +1053,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     // CTAs only as wide as the active warps need: with few items, the SMs keep
     // room for the combine's CTAs, which then start while the decode drains
     const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
-    k_decode<D, GQ, RG><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
+    k_decode<D, GQ, RG, CO><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ, RG>(a, st, c->B, s);
@@ -1028,15 +1061,18 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
 
 template <int D, int GQ>
 cudaError_t set_decode_attr(int smem_max) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode<D, GQ, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    cudaError_t e = cudaFuncSetAttribute(k_decode<D, GQ, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_decode<D, GQ, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    e = cudaFuncSetAttribute(k_decode<D, GQ, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_decode<D, GQ, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
 }
 
 template <int D, int GQ>
 cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
-    return c->ragged ? launch_decode_t<D, GQ, true>(c, q, out, part, s)
-                     : launch_decode_t<D, GQ, false>(c, q, out, part, s);
+    if (c->cold >= 0) return launch_decode_t<D, GQ, false, true>(c, q, out, part, s);
+    return c->ragged ? launch_decode_t<D, GQ, true, false>(c, q, out, part, s)
+                     : launch_decode_t<D, GQ, false, false>(c, q, out, part, s);
 }
 
 }  // namespace

@@ -15,6 +15,14 @@
 // ascending token order. Keys are quantized per channel, values per token per
 // 32 channels, with IEEE fp32 steps (__fsub_rn/__fdiv_rn, round-half-even
 // __float2int_rn) and fp16 round-to-nearest for scale and zero.
+//
+// Cold-pool policy (zijie-tian.site sec. 3.2, the alternative to writing a
+// displaced token back): the displaced pool tokens do not join the block;
+// they enter the unit's cold pool, an fp16 ring of C slots used first in,
+// first out, in ascending token order, and the tokens that entered first are
+// discarded when it overflows. The block is then the group's tokens that did
+// not enter the pool, and its size, which depends on the data, is written to
+// the per-block count array.
 #include "ott_internal.cuh"
 
 namespace ott {
@@ -44,6 +52,11 @@ struct FlushArgs {
     float *pnorm;
     int32_t *pidx;
     const __half *srcK, *srcV;
+    __half *ck, *cv;             // cold pool [U][C][d] (cold-pool policy)
+    int32_t *cidx;               // [U][C] token index of each cold slot
+    int *cmeta;                  // [U][2]: tokens in the cold pool, slot of the oldest
+    int32_t *bcnt;               // [U][NB] valid tokens of each block (cold-pool policy)
+    int C;                       // cold-pool capacity; -1: displaced tokens are written back
     long long src_unit_stride;   // elements between units in the source
     long long src_mod;           // slot = token mod src_mod
     long long t0;                // first token of the group
@@ -79,7 +92,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     uint64_t *key = reinterpret_cast<uint64_t *>(cv + (size_t)nc * RS);
     int *rank = reinterpret_cast<int *>(key + nc);
     int *bmap = rank + nc;
-    float *ks = reinterpret_cast<float *>(bmap + G);
+    int *emap = bmap + G;              // displaced pool rows by token order (cold-pool policy)
+    float *ks = reinterpret_cast<float *>(emap + (P > 0 ? P : 1));
     float *kz = ks + D;
     float *vs = kz + D;
     float *vz = vs + G * NG;
@@ -132,16 +146,36 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         rank[r] = rk;
     }
     __syncthreads();
-    const int keep = min(P, nc), cnt = nc - keep;
+    const int keep = min(P, nc);
+    const bool cold = a.C >= 0;
+    // displaced pool tokens; under the cold-pool policy they leave the block
+    int ev = 0;
+    if (cold)
+        for (int q = 0; q < np0; ++q) ev += rank[q] >= keep;
+    const int cnt = nc - keep - ev;
 
-    // 4. block slot of every leaving candidate: rank by token index
+    // 4. block slot of every leaving candidate (cold-pool policy: of every
+    // leaving group token, and cold order of every displaced pool token):
+    // rank by token index among its own kind
     for (int r = tid; r < nc; r += nth) {
         if (rank[r] >= keep) {
             const uint32_t ir = (uint32_t)key[r];
+            const bool own = cold && r < np0;        // a displaced pool token
+            const int q0 = cold ? (own ? 0 : np0) : 0, q1 = cold ? (own ? np0 : nc) : nc;
             int pos = 0;
-            for (int q = 0; q < nc; ++q) pos += (rank[q] >= keep) && ((uint32_t)key[q] < ir);
-            bmap[pos] = r;
+            for (int q = q0; q < q1; ++q) pos += (rank[q] >= keep) && ((uint32_t)key[q] < ir);
+            if (own)
+                emap[pos] = r;
+            else
+                bmap[pos] = r;
         }
+    }
+    // cold pool before this flush (read by every thread before thread 0
+    // updates it below)
+    int cn0 = 0, ch0 = 0;
+    if (cold && a.C > 0) {
+        cn0 = a.cmeta[2 * u];
+        ch0 = a.cmeta[2 * u + 1];
     }
     // 5. the new pool (old pool rows are already staged in shared memory)
     for (int e = tid; e < nc * VPR; e += nth) {
@@ -160,6 +194,27 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         }
     }
     __syncthreads();
+
+    // the displaced tokens enter the cold pool in token order; of the
+    // cn0 + ev tokens, the last min(C, cn0 + ev) stay
+    if (cold) {
+        if (tid == 0) a.bcnt[(size_t)u * a.NB + jj] = cnt;
+        if (a.C > 0 && ev > 0) {
+            const int n1 = min(a.C, cn0 + ev), skip = ev - min(ev, n1);
+            for (int e = tid; e < (ev - skip) * VPR; e += nth) {
+                const int x = skip + e / VPR, v8 = e % VPR, row = emap[x];
+                const int slotc = (ch0 + cn0 + x) % a.C;
+                const size_t off = ((size_t)u * a.C + slotc) * D;
+                reinterpret_cast<uint4 *>(a.ck + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[v8];
+                reinterpret_cast<uint4 *>(a.cv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[v8];
+                if (v8 == 0) a.cidx[(size_t)u * a.C + slotc] = (int32_t)(uint32_t)key[row];
+            }
+            if (tid == 0) {
+                a.cmeta[2 * u] = n1;
+                a.cmeta[2 * u + 1] = (ch0 + cn0 + ev - n1) % a.C;
+            }
+        }
+    }
 
     uint8_t *bb = a.blk + ((size_t)u * a.NB + jj) * a.blk_bytes;
     uint8_t *tiles = bb + ksz_bytes(D);
@@ -353,6 +408,7 @@ int flush_smem_bytes(int d, int G, int P) {
     const long long b = nc * (d + 8) * 2 * 2   // staged K and V rows
                         + nc * 8               // keys
                         + nc * 4 + (long long)G * 4           // ranks, block map
+                        + (long long)(P > 0 ? P : 1) * 4      // cold order
                         + 2LL * d * 4                         // key scale/zero
                         + 2LL * ntiles_of(G) * TILE * (d / 32) * 4;  // value scale/zero
     return b > (1LL << 30) ? (1 << 30) : (int)b;
@@ -380,6 +436,12 @@ FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV,
     a.pidx = c->pidx;
     a.srcK = srcK;
     a.srcV = srcV;
+    a.ck = c->ck;
+    a.cv = c->cv;
+    a.cidx = c->cidx;
+    a.cmeta = c->cmeta;
+    a.bcnt = c->bcnt;
+    a.C = c->cold;
     a.src_unit_stride = src_unit_stride;
     a.src_mod = src_mod;
     a.t0 = t0;

@@ -35,6 +35,9 @@
 // Residual ring: rk, rv [U][G+R][d], token t in slot t mod (G+R).
 // Outlier pool:  pk, pv [U][P][d], pnorm [U][P], pidx [U][P], kept sorted by
 // (norm, token index) ascending; n_pool = min(P, nf*G) for every unit.
+// Cold pool (cold-pool policy only): ck, cv [U][C][d], cidx [U][C], a ring
+// used first in, first out, with (count, slot of the oldest) in cmeta [U][2];
+// block sizes then depend on the data and are kept in bcnt [U][NB].
 #pragma once
 
 #include <cuda_fp16.h>
@@ -129,6 +132,13 @@ struct ott_cache {
     int maxu_r;             // units a decode warp's range can touch in a ragged batch
     std::vector<long long> Tb;   // [B] tokens of each sequence (ragged)
     std::vector<int> nfb;        // [B] flushes of each sequence (ragged)
+    // cold-pool policy (ott_create_cold): displaced pool tokens enter a
+    // first-in-first-out fp16 pool of `cold` slots instead of the new block
+    int cold;               // capacity C, or -1 (displaced tokens are written back)
+    __half *ck, *cv;        // [U][C][d]
+    int32_t *cidx;          // [U][C]
+    int *cmeta;             // [U][2]: tokens in the cold pool, slot of the oldest
+    int32_t *bcnt;          // [U][NB] valid tokens of each block
 };
 
 namespace ott {

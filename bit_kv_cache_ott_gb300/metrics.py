@@ -43,6 +43,22 @@ def decode_bytes(T: int, B: int, Hq: int, Hkv: int, d: int, G: int, R: int, P: i
     return B * Hkv * decode_bytes_per_unit(T, d, Hq // Hkv, G, R, P)
 
 
+def hot_bytes(T: int, B: int, Hq: int, Hkv: int, d: int, G: int, R: int, P: int) -> int:
+    """Bytes of one decode call outside the quantized blocks and the cold
+    pool: residual and pool tokens (fp16 K and V), the query and the output."""
+    nf = flush_count(T, G, R)
+    npool = pool_size(T, G, R, P)
+    return B * Hkv * ((T - nf * G + npool) * d * 4 + (Hq // Hkv) * d * 4)
+
+
+def cold_unit_bytes(bcount, ncold: int, d: int) -> int:
+    """Cold-pool policy: bytes of one unit's quantized blocks (sizes bcount,
+    read from the device) and of its ncold fp16 cold-pool tokens."""
+    nq = int(sum(int(n) for n in bcount))
+    nonempty = sum(1 for n in bcount if n > 0)
+    return 2 * nq * d // 4 + nonempty * d * 4 + nq * (d // 32) * 4 + int(ncold) * d * 4
+
+
 def fp16_cache_bytes(T: int, B: int, Hkv: int, d: int) -> int:
     """The same cache held entirely in fp16 (K and V)."""
     return B * Hkv * T * d * 4

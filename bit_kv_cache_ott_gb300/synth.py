@@ -47,6 +47,7 @@ class Workload:
     layers: int = 1   # independent caches (one per layer)
     seed: int = 1000
     len_lo: int = 0   # > 0: sequence b's prefill length is drawn uniformly from [len_lo, L]
+    cold: int = -1    # >= 0: the cold-pool eviction policy with this capacity
 
     @property
     def g(self) -> int:
@@ -85,6 +86,9 @@ WORKLOADS = {
     # a serving batch whose sequences differ in length (mean ~4096 tokens)
     "batch_b32_ragged": Workload("batch_b32_ragged", B=32, Hq=32, Hkv=32, d=128, L=7168, steps=512,
                                  G=128, R=32, P=32, seed=1005, len_lo=1024),
+    # the headline batch under the cold-pool policy with the pages' 32 slots
+    "batch_b32_cold": Workload("batch_b32_cold", B=32, Hq=32, Hkv=32, d=128, L=4096, steps=512,
+                               G=128, R=32, P=32, seed=1002, cold=32),
 }
 
 HEADLINE = "batch_b32"

@@ -93,6 +93,23 @@ int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P,
 int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P,
                       int max_tokens, ott_cache **out);
 
+/*
+ * As ott_create, with the cold-pool eviction policy of zijie-tian.site
+ * sec. 3.2 (the alternative to writing a displaced token back to the main
+ * cache; the page sizes the cold pool at 32 tokens). At a flush the pool
+ * tokens displaced by the group do not join the new block: they enter the
+ * unit's cold pool, C fp16 slots used first in, first out, in ascending token
+ * order; once it holds C tokens each new one discards the one that entered
+ * first, which no store holds afterwards. The new block is the group's tokens
+ * that did not enter the pool, so block sizes depend on the data (see
+ * ott_export_cold). ott_decode_attn attends the cold pool like the outlier
+ * pool. 0 <= C <= OTT_COLD_MAX; C = 0 discards displaced tokens at once.
+ * All sequences have one length (no ott_prefill_lens).
+ */
+#define OTT_COLD_MAX 4096
+int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C,
+                    int max_tokens, ott_cache **out);
+
 /* Free everything. NULL-safe. Waits for the device to finish. */
 int ott_destroy(ott_cache *c);
 
@@ -169,7 +186,8 @@ int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_
 int ott_get_seq_counts(const ott_cache *c, int b, long long *T, int *nf, int *tail, int *n_pool);
 
 /* Valid tokens of block j (0 <= j < nf). Host-side. Returns the count or
- * OTT_ERR_INVALID. */
+ * OTT_ERR_INVALID; OTT_ERR_STATE for a cache with the cold-pool policy, whose
+ * block sizes differ per unit (ott_export_cold reports them). */
 int ott_block_count(const ott_cache *c, int j);
 
 /*
@@ -202,6 +220,18 @@ typedef struct {
 } ott_state_export;
 
 int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst);
+
+/*
+ * The cold-pool policy's extra state for units [u0, u0+nu), as HOST arrays
+ * (any pointer may be NULL):
+ *   bcount [nu][nf] int32   valid tokens of each block (as the decode reads them)
+ *   ncold  [nu]     int32   tokens in the cold pool
+ *   cidx   [nu][C]  int32   their token indices, the oldest entry first (-1 pad)
+ *   ck, cv [nu][C][d]       their fp16 keys and values, same order (0 pad)
+ * Synchronizes the device. OTT_ERR_STATE for a cache without the policy.
+ */
+int ott_export_cold(ott_cache *c, int u0, int nu, int32_t *bcount, int32_t *ncold, int32_t *cidx,
+                    uint16_t *ck, uint16_t *cv);
 
 /*
  * Wait for the device and read the cache's device status word: OTT_OK, or

@@ -123,3 +123,49 @@ def test_batch_b32_ragged(oracle_mod, ott):
                 compare_out(got, ref, f"ragged step {s}")
         assert flushed > w.B // 2        # the sequences flushed at different steps
         c.check_device()
+
+
+def test_batch_b32_cold(oracle_mod, ott):
+    """The headline batch under the cold-pool policy (32 slots): per-unit
+    block sizes, blocks, pool and cold pool bit-exact on sampled units after
+    the prefill and at every flush; sampled outputs at chosen steps."""
+    from tests.parity_util import STATE_KEYS
+    w = synth.WORKLOADS["batch_b32_cold"]
+    steps, decode_steps = 300, {0, 31, 32, 160, 299}
+    K, V = synth.prefill_kv(w)
+    orc = oracle_mod.OracleCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, cold=w.cold)
+    orc.prefill(K, V)
+    pairs = _sample_heads(w, 12, 5)
+    units = _units_to_check(w, 48)
+
+    def check():
+        gpu = c.export_state()
+        for u in units:
+            e = orc.export_unit(u)
+            assert (gpu["T"], gpu["nf"], gpu["npool"]) == (e["T"], e["nf"], e["npool"])
+            assert np.array_equal(gpu["bcount"][u], e["bcount"]), u
+            assert gpu["ncold"][u] == e["ncold"], u
+            for k in STATE_KEYS + ("cidx", "ck", "cv"):
+                assert np.array_equal(gpu[k][u], e[k]), f"unit {u} field {k}"
+
+    with ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + steps, cold=w.cold) as c:
+        c.prefill(K.cuda(), V.cuda())
+        del K, V
+        check()
+        bc, nc = c.cold_sizes()
+        assert nc.min() > 0 and (bc[:, 1:] < w.G).any()   # pool tokens were displaced
+        nf_prev = c.counts()[1]
+        for s in range(steps):
+            k, v, q = synth.step_kvq(w, s)
+            c.append(k.cuda(), v.cuda())
+            orc.append(k, v)
+            nf = c.counts()[1]
+            if nf != nf_prev:
+                check()
+                nf_prev = nf
+            if s in decode_steps:
+                out = c.decode_attn(q.cuda()).float().cpu().numpy()
+                ref = np.stack([orc.decode_head(b, h, q[b, h]) for b, h in pairs])
+                got = torch.from_numpy(np.stack([out[b, h] for b, h in pairs]))
+                compare_out(got, ref, f"cold step {s}")
+        c.check_device()
