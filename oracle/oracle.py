@@ -54,6 +54,8 @@ def lib():
             L.orc_create_policy.restype = P
             L.orc_create_policy.argtypes = [i32] * 8
             L.orc_export_cold.argtypes = [P, i32, P, P, P]
+            L.orc_topk_select.argtypes = [P, i32, i32, P, i32, P, P]
+            L.orc_decode_topk.argtypes = [P, P, i32, P]
             L.orc_destroy.argtypes = [P]
             L.orc_append.argtypes = [P, P, P]
             L.orc_prefill.argtypes = [P, P, P, i32]
@@ -183,6 +185,31 @@ class OracleCache:
         if lib().orc_decode(self._h, _ptr(qb), _ptr(out)):
             raise RuntimeError("decode on an empty oracle cache")
         return out
+
+    def decode_topk(self, q, K: int) -> np.ndarray:
+        """Top-K sparse decode: q fp16 [B][Hq][d] -> float64 [B][Hq][d]; each
+        (sequence, kv head) attends its K best-bounded quantized blocks."""
+        qb = _bits(q)
+        out = np.zeros(qb.shape, np.float64)
+        if lib().orc_decode_topk(self._h, _ptr(qb), int(K), _ptr(out)):
+            raise RuntimeError("decode on an empty oracle cache")
+        return out
+
+    def topk_select(self, q, K: int):
+        """The blocks a top-K decode attends: (sel int32 [B*Hkv][K] ascending,
+        -1 padded; bounds float32 [B*Hkv][nf], -inf for empty blocks)."""
+        qb = _bits(q)
+        U = self.B * self.Hkv
+        nf = self.counts(0)[1]
+        sel = np.full((U, max(K, 1)), -1, np.int32)
+        bounds = np.zeros((U, max(nf, 1)), np.float32)
+        for u in range(U):
+            b, hk = divmod(u, self.Hkv)
+            row = np.zeros(max(nf, 1), np.int32)
+            qrow = np.ascontiguousarray(qb[b])
+            m = lib().orc_topk_select(self._h, b, hk, _ptr(qrow), int(K), _ptr(row), _ptr(bounds[u]))
+            sel[u, :m] = row[:m]
+        return sel[:, :K], bounds[:, :nf]
 
     def decode_head(self, b, hq, qv) -> np.ndarray:
         """One query head: qv fp16 [d] -> float64 [d]."""

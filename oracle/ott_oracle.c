@@ -57,6 +57,16 @@
  *      and no store holds them any more. The new block is the group's
  *      tokens that did not enter the pool. Decode attends the cold pool like
  *      the outlier pool; discarded tokens are not attended.
+ *  R12 Top-K sparse access ([blog] sec. 6, combining OTT with sparse KV
+ *      access): a decode call may attend only K of a unit's quantized
+ *      blocks, plus every residual, pool and cold token. The K blocks are
+ *      the non-empty ones with the largest score bound, ties to the lower
+ *      block index. The bound of block j for query head h is the largest
+ *      q.k that a key dequantized from the block's per-channel scale s and
+ *      zero z can reach: the sum over channels of max(q*z, q*(z + 3*s)),
+ *      taken in fp32 (products, 3*s and z + 3*s rounded to nearest, summed
+ *      in channel order); the block's bound is the largest over the query
+ *      heads that share the kv head. A selected block is attended whole.
  *
  * Floating point: decisions that yield integers or stored bits (norms,
  * scales, zeros, codes) are taken in fp32 exactly as the library takes them.
@@ -515,9 +525,10 @@ int orc_prefill_lens(void *hp, const uint16_t *K, const uint16_t *V, const int32
 /* the concatenation; the weights times the matching (dequantized) values.   */
 /* ------------------------------------------------------------------------ */
 
-int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
+/* use_block: NULL attends every block; else block j is attended iff use_block[j]. */
+static int decode_head_blocks(orc_cache *h, int b, int hq, const uint16_t *qv, const char *use_block,
+                              double *out)
 {
-    orc_cache *h = (orc_cache *)hp;
     if (b < 0 || b >= h->B || hq < 0 || hq >= h->Hq || h->Tb[b] < 1)
         return -2;
     const int d = h->d, ng = d / 32;
@@ -533,6 +544,8 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
     long long m = 0;
     for (int j = 0; j < u->nb; ++j) {
         const orc_block *bl = &u->blk[j];
+        if (use_block && !use_block[j])
+            continue;
         for (int t = 0; t < bl->c; ++t) {
             double acc = 0.0;
             for (int c = 0; c < d; ++c) {
@@ -579,6 +592,8 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
     m = 0;
     for (int j = 0; j < u->nb; ++j) {
         const orc_block *bl = &u->blk[j];
+        if (use_block && !use_block[j])
+            continue;
         for (int t = 0; t < bl->c; ++t) {
             double p = score[m++];
             for (int c = 0; c < d; ++c) {
@@ -608,6 +623,115 @@ int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
         out[c] /= sum;
     free(score);
     free(q);
+    return 0;
+}
+
+int orc_decode_head(void *hp, int b, int hq, const uint16_t *qv, double *out)
+{
+    return decode_head_blocks((orc_cache *)hp, b, hq, qv, NULL, out);
+}
+
+/* R12: the score bound of block bl for the fp16 query qv [d], in fp32. */
+static float block_bound(const orc_block *bl, const uint16_t *qv, int d)
+{
+    float beta = 0.0f;
+    for (int c = 0; c < d; ++c) {
+        const float q = orc_h2f(qv[c]);
+        const float s = orc_h2f(bl->ks[c]);
+        const float z = orc_h2f(bl->kz[c]);
+        const float three_s = 3.0f * s;
+        const float top = z + three_s;       /* the largest dequantized value */
+        const float lo = q * z, hi = q * top;
+        beta = beta + (hi > lo ? hi : lo);
+    }
+    return beta;
+}
+
+typedef struct {
+    float bound;
+    int j;
+} orc_rank;
+
+static int rank_cmp(const void *a, const void *b)
+{
+    const orc_rank *x = (const orc_rank *)a, *y = (const orc_rank *)b;
+    if (x->bound > y->bound) return -1;
+    if (x->bound < y->bound) return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+static int cmp_int(const void *a, const void *b)
+{
+    const int x = *(const int *)a, y = *(const int *)b;
+    return (x > y) - (x < y);
+}
+
+/* R12: the blocks that a top-K decode of sequence b attends for kv head hk.
+ * qb: fp16 bits [Hq][d] (sequence b's queries). Writes the selected block
+ * indices in ascending order to sel and returns how many there are
+ * (min(K, non-empty blocks)). bounds, if not NULL, receives [nb] block
+ * bounds (-inf for an empty block). */
+int orc_topk_select(void *hp, int b, int hk, const uint16_t *qb, int K, int32_t *sel, float *bounds)
+{
+    orc_cache *h = (orc_cache *)hp;
+    const int g = h->Hq / h->Hkv, d = h->d;
+    const orc_unit *u = &h->u[b * h->Hkv + hk];
+    orc_rank *r = (orc_rank *)malloc(sizeof(orc_rank) * (u->nb + 1));
+    int n = 0;
+    for (int j = 0; j < u->nb; ++j) {
+        const orc_block *bl = &u->blk[j];
+        float best = -INFINITY;
+        if (bl->c > 0)
+            for (int x = 0; x < g; ++x) {
+                const float bx = block_bound(bl, qb + (size_t)(hk * g + x) * d, d);
+                if (bx > best)
+                    best = bx;
+            }
+        if (bounds)
+            bounds[j] = best;
+        if (bl->c > 0) {
+            r[n].bound = best;
+            r[n].j = j;
+            ++n;
+        }
+    }
+    qsort(r, n, sizeof(orc_rank), rank_cmp);
+    const int m = K < n ? (K < 0 ? 0 : K) : n;
+    int *js = (int *)malloc(sizeof(int) * (m + 1));
+    for (int i = 0; i < m; ++i)
+        js[i] = r[i].j;
+    qsort(js, m, sizeof(int), cmp_int);
+    for (int i = 0; i < m; ++i)
+        sel[i] = js[i];
+    free(js);
+    free(r);
+    return m;
+}
+
+/* R12. q: fp16 bits [B][Hq][d]; out: double [B][Hq][d]. */
+int orc_decode_topk(void *hp, const uint16_t *q, int K, double *out)
+{
+    orc_cache *h = (orc_cache *)hp;
+    const int g = h->Hq / h->Hkv, d = h->d;
+    for (int b = 0; b < h->B; ++b)
+        if (h->Tb[b] < 1)
+            return -2;
+    for (int b = 0; b < h->B; ++b)
+        for (int hk = 0; hk < h->Hkv; ++hk) {
+            const orc_unit *u = &h->u[b * h->Hkv + hk];
+            int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (u->nb + 1));
+            char *use = (char *)calloc(u->nb + 1, 1);
+            const int m = orc_topk_select(h, b, hk, q + (size_t)b * h->Hq * d, K, sel, NULL);
+            for (int i = 0; i < m; ++i)
+                use[sel[i]] = 1;
+            for (int x = 0; x < g; ++x) {
+                const int hq = hk * g + x;
+                const size_t o = ((size_t)b * h->Hq + hq) * d;
+                decode_head_blocks(h, b, hq, q + o, use, out + o);
+            }
+            free(use);
+            free(sel);
+        }
     return 0;
 }
 
