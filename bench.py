@@ -155,9 +155,22 @@ def synth_T(w) -> str:
 
 def step_bytes(w, Ts) -> int:
     """Algorithmic bytes of one decode call with sequence b at Ts[b] tokens."""
+    if w.topk > 0:
+        return sum(metrics.topk_bytes(t, 1, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, w.topk) for t in Ts)
     if len(set(Ts)) == 1:
         return metrics.decode_bytes(Ts[0], len(Ts), w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
     return sum(metrics.decode_bytes(t, 1, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) for t in Ts)
+
+
+def decode_call(c, w, q, out, stream):
+    """The workload's decode entry point: full, or Top-K sparse."""
+    if w.topk > 0:
+        return c.decode_attn_topk(q, w.topk, out, stream=stream)
+    return c.decode_attn(q, out, stream)
+
+
+def oracle_decode(orc, w, q):
+    return orc.decode_topk(q, w.topk) if w.topk > 0 else orc.decode(q)
 
 
 def cold_of(w):
@@ -195,12 +208,12 @@ def oracle_rate(w, steps: int, warmup: int, units_sample: int):
     for s in range(warmup):
         k, v, q = inputs[s]
         orc.append(k, v)
-        orc.decode(q)
+        oracle_decode(orc, ws, q)
     t0 = time.perf_counter()
     for s in range(warmup, warmup + steps):
         k, v, q = inputs[s]
         orc.append(k, v)
-        orc.decode(q)
+        oracle_decode(orc, ws, q)
     dt = time.perf_counter() - t0
     # scaled to the whole workload by algorithmic bytes (= by units when all lengths are equal)
     frac = step_bytes(ws, lens[:Bs]) / step_bytes(w, lens)
@@ -234,13 +247,13 @@ def _oracle_worker(task):
     for s in range(warmup):
         k, v, q = inputs[s]
         orc.append(k, v)
-        orc.decode(q)
+        oracle_decode(orc, ws, q)
     _WORKER_BARRIER.wait()
     t0 = time.perf_counter()
     for s in range(warmup, warmup + steps):
         k, v, q = inputs[s]
         orc.append(k, v)
-        orc.decode(q)
+        oracle_decode(orc, ws, q)
     return time.perf_counter() - t0
 
 
@@ -341,7 +354,7 @@ def run_ours(args, w):
             c.append(k, v, stream)
             if ev is not None:
                 ev[0].record(stream)
-            c.decode_attn(q, out, stream)
+            decode_call(c, w, q, out, stream)
             if ev is not None:
                 ev[1].record(stream)
 
@@ -360,7 +373,7 @@ def run_ours(args, w):
     # cold-pool policy: the quantized and cold stores' sizes are read before
     # and after the timed region and taken as linear in the flushes between
     cold_q0 = [cold_quant_bytes(c) for c in caches] if w.cold >= 0 else None
-    cold_steps = []   # (layer, hot bytes, flush steps so far) per layer-step
+    step_log = []     # (token counts, flush steps so far) per timed step
     flush_steps = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -377,23 +390,26 @@ def run_ours(args, w):
                 flushes += int(flush_launch)
                 ev = dec_events[s * w.layers + li]
                 ev[0].record(stream)
-                c.decode_attn(q, out, stream)
+                decode_call(c, w, q, out, stream)
                 ev[1].record(stream)
-                if cold_q0 is None:
-                    dec_bytes += step_bytes(w, Ts)
-                else:
-                    cold_steps.append((li, metrics.hot_bytes(Ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P),
-                                       flush_steps))
+            # the byte count is taken after the timed region (only the
+            # per-step token counts are kept here, so the host stays ahead)
+            step_log.append((tuple(Ts), flush_steps))
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
     ms = e0.elapsed_time(e1)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec_events)
-    if cold_q0 is not None:
+    if cold_q0 is None:
+        dec_bytes = sum(step_bytes(w, list(ts)) for ts, _ in step_log) * w.layers
+    else:
         cold_q1 = [cold_quant_bytes(c) for c in caches]
         nfl = max(1, flush_steps)
-        dec_bytes = sum(hot + cold_q0[li] + (cold_q1[li] - cold_q0[li]) * f / nfl for li, hot, f in cold_steps)
-    launches = K_steps * w.layers * 3 + flushes   # append + decode + combine, plus flushes
+        dec_bytes = sum(metrics.hot_bytes(ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
+                        + cold_q0[li] + (cold_q1[li] - cold_q0[li]) * f / nfl
+                        for ts, f in step_log for li in range(w.layers))
+    # append + decode + combine (+ the Top-K selection), plus flushes
+    launches = K_steps * w.layers * (4 if w.topk > 0 else 3) + flushes
     ms = max_over_ranks(ms, dev)
     for c in caches:
         c.check_device()
@@ -448,7 +464,7 @@ def run_ours(args, w):
             dk, dv, dq = din[b]
             for c in caches:
                 c.append(dk, dv, stream)
-                c.decode_attn(dq, douts[b], stream)
+                decode_call(c, w, dq, douts[b], stream)
             computed[b].record(stream)
             with torch.cuda.stream(cstream):
                 cstream.wait_event(computed[b])
@@ -481,6 +497,8 @@ def run_ours(args, w):
             "vs_baseline": None, "dtype": "fp16 storage, fp32 accumulation", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
                        "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
+                       **({"topk": w.topk, "topk_bytes": "bound pass over every non-empty block's scale/zero "
+                           "header, plus the K smallest non-empty blocks (a lower bound)"} if w.topk > 0 else {}),
                        **({"cold": w.cold, "cold_bytes": "block and cold-pool sizes read from the device "
                            "before and after the timed region, linear in between"} if w.cold >= 0 else {}),
                        **({"ragged_lens": {"min": min(lens), "max": max(lens),
@@ -495,7 +513,8 @@ def run_ours(args, w):
             "cache_bytes": cache_bytes, "fp16_cache_bytes": fp16_bytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
-                         "kernel": "k_decode + k_combine (ott_decode_attn)",
+                         "kernel": ("k_topk_select + k_decode + k_combine (ott_decode_attn_topk)" if w.topk > 0
+                                    else "k_decode + k_combine (ott_decode_attn)"),
                          "algorithmic_bytes_per_launch": dec_bytes / n_launch,
                          "traffic": recorded_traffic(w.name)},
             "clocks": clk.summary(),

@@ -38,7 +38,7 @@ class StateExport(C.Structure):
 
 
 SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
-           "ott_decode_attn", "ott_decode_attn_static", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
+           "ott_decode_attn", "ott_decode_attn_static", "ott_decode_attn_topk", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
            "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str")
 
 
@@ -68,6 +68,7 @@ def load(build_if_missing: bool = False):
     L.ott_append.argtypes = [P, P, P, P]
     L.ott_decode_attn.argtypes = [P, P, P, P]
     L.ott_decode_attn_static.argtypes = [P, P, P, P]
+    L.ott_decode_attn_topk.argtypes = [P, P, P, i32, P, P]
     L.ott_get_counts.argtypes = [P, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
     L.ott_get_seq_counts.argtypes = [P, i32, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
     L.ott_block_count.argtypes = [P, i32]
@@ -175,6 +176,25 @@ class OTTCache:
             out = torch.empty(shp, dtype=torch.float16, device=q.device)
         _check(load().ott_decode_attn(self._h, _dev_ptr(q, shp, "q"), _dev_ptr(out, shp, "out"),
                                       _stream(stream)), "ott_decode_attn")
+        return out
+
+    def decode_attn_topk(self, q: torch.Tensor, K: int, out: torch.Tensor | None = None,
+                         sel: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Top-K sparse decode: each (sequence, kv head) attends its K blocks
+        with the largest score bound plus all fp16 tokens. ``sel``, if given,
+        is a CUDA int32 tensor [B*Hkv][min(K, nf)] that receives the blocks."""
+        shp = (self.B, self.Hq, self.d)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float16, device=q.device)
+        sp = None
+        if sel is not None:
+            kc = min(int(K), self.counts()[1])
+            if (not sel.is_cuda or sel.dtype != torch.int32 or not sel.is_contiguous()
+                    or tuple(sel.shape) != (self.B * self.Hkv, kc)):
+                raise ValueError(f"sel: expected a contiguous CUDA int32 tensor {(self.B * self.Hkv, kc)}")
+            sp = sel.data_ptr()
+        _check(load().ott_decode_attn_topk(self._h, _dev_ptr(q, shp, "q"), _dev_ptr(out, shp, "out"), int(K), sp,
+                                           _stream(stream)), "ott_decode_attn_topk")
         return out
 
     def counts(self):

@@ -139,6 +139,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t Cs = cold > 0 ? (size_t)cold : 0;
     const size_t sz_cold = U * Cs * d * 2, sz_cidx = U * Cs * 4;
     const size_t sz_cmeta = cold >= 0 ? U * 8 : 0, sz_bcnt = cold >= 0 ? U * c->NB * 4 : 0;
+    const size_t sz_sel = U * c->NB * 4;   // also the size of the bound scratch
     size_t off = 0;
     const size_t o_blk = off; off = round_up(off + sz_blk, 256);
     const size_t o_bidx = off; off = round_up(off + sz_bidx, 256);
@@ -155,6 +156,8 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t o_ci = off; off = round_up(off + sz_cidx, 256);
     const size_t o_cm = off; off = round_up(off + sz_cmeta, 256);
     const size_t o_bc = off; off = round_up(off + sz_bcnt, 256);
+    const size_t o_sel = off; off = round_up(off + sz_sel, 256);
+    const size_t o_bnd = off; off = round_up(off + sz_sel, 256);
     c->mem_bytes = off;
 
     // Host-side fault injection for tests: OTT_FAULT=alloc makes the device
@@ -188,8 +191,12 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->cidx = sz_cidx ? reinterpret_cast<int32_t *>(base + o_ci) : nullptr;
     c->cmeta = sz_cmeta ? reinterpret_cast<int *>(base + o_cm) : nullptr;
     c->bcnt = sz_bcnt ? reinterpret_cast<int32_t *>(base + o_bc) : nullptr;
+    c->sel = reinterpret_cast<int32_t *>(base + o_sel);
+    c->bound = reinterpret_cast<float *>(base + o_bnd);
+    c->topk_ok = topk_smem_bytes(d, gq, c->NB) <= smem_optin;
     e = cudaMemset(mem, 0, c->mem_bytes);
     if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
+    if (e == cudaSuccess) e = set_topk_attributes(d, gq, smem_optin);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(mem);
@@ -327,6 +334,21 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
     if (!q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
     cudaError_t e = launch_decode(c, static_cast<const __half *>(q), static_cast<__half *>(out),
                                   static_cast<cudaStream_t>(stream));
+    return fail_cuda(c, e);
+}
+
+int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t *sel, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || c->T < 1 || c->ragged) return OTT_ERR_STATE;
+    if (K < 1 || !c->topk_ok || !q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half *qh = static_cast<const __half *>(q);
+    const int Kc = K < c->nf ? K : c->nf;
+    cudaError_t e = cudaSuccess;
+    if (Kc > 0) e = launch_topk_select(c, qh, K, Kc, s);
+    if (e == cudaSuccess) e = launch_decode_topk(c, qh, static_cast<__half *>(out), Kc, s);
+    if (e == cudaSuccess && sel && Kc > 0)
+        e = cudaMemcpyAsync(sel, c->sel, (size_t)c->U * Kc * 4, cudaMemcpyDeviceToDevice, s);
     return fail_cuda(c, e);
 }
 

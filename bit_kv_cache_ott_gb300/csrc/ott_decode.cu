@@ -132,6 +132,10 @@ struct DecodeArgs {
     const __half *ck, *cv;     // [U][C][d] cold pool, a ring used first in, first out
     const int *cmeta;          // [U][2]: tokens in the cold pool, slot of the oldest
     int C;
+    // Top-K sparse decode: the quantized items of unit u are the blocks
+    // sel[u][0..Ksel) (ascending, -1 for none) instead of blocks 0..nf-1
+    const int32_t *sel;
+    int Ksel;
 };
 
 template <int D, int GQ>
@@ -141,7 +145,6 @@ struct Cfg {
     static constexpr int NG = D / 32;              // value groups of 32 channels
     static constexpr int GPV = 4 / GQ;             // value groups per PV B variant
     static constexpr int NV = (NG + GPV - 1) / GPV;  // PV B variants
-    static constexpr int CPL = D / 32;             // channels per lane, fp16 path
     static constexpr int STAGE = stage_bytes(D);
     static constexpr bool COOP = GQ <= 2;          // per-block constants computed cooperatively
     static constexpr int QHL = COOP ? GQ * 2 * (D + 8) * 2 : 0;   // hi/lo staging bytes
@@ -252,8 +255,9 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 }
 
 // ---------------------------------------------------------------- quantized segment
-// Blocks [j0, j1) of unit u; the partial goes to part[slot].
-template <int D, int GQ, bool CO>
+// Blocks [j0, j1) of unit u (Top-K: the blocks listed at positions [j0, j1)
+// of the unit's selection); the partial goes to part[slot].
+template <int D, int GQ, bool CO, bool TK>
 __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
                               int lane) {
@@ -262,15 +266,27 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     constexpr int KSZ = ksz_bytes(D), TB = tile_bytes(D);
     const int r = lane >> 2, i = lane & 3;
 
-    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < block_cnt<CO>(a, u, j); };
+    // position j -> block index; a position without a block holds no token
+    auto blk_of = [&](int j) -> int {
+        if constexpr (TK) return __ldg(a.sel + (size_t)u * a.Ksel + j);
+        return j;
+    };
+    auto cnt_of = [&](int j) -> int {
+        if constexpr (TK) {
+            const int bj = blk_of(j);
+            return bj < 0 ? 0 : block_cnt<CO>(a, u, bj);
+        }
+        return block_cnt<CO>(a, u, j);
+    };
+    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < cnt_of(j); };
     int lj = j0, lk = 0;
     while (lj < j1 && !active(lj, lk)) { ++lj; lk = 0; }
     int cj_ = lj, ck_ = lk;   // next chunk to consume
     auto issue = [&](int j, int k, int st) {
         if (lane == 0) {
-            const int vt = (block_cnt<CO>(a, u, j) + TILE - 1) / TILE;
+            const int vt = (cnt_of(j) + TILE - 1) / TILE;
             const int t0 = k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
-            const uint8_t *bsrc = a.blk + ((size_t)u * a.NB + j) * a.blk_bytes;
+            const uint8_t *bsrc = a.blk + ((size_t)u * a.NB + blk_of(j)) * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
             if (k == 0)
                 bulk_load(dst, bsrc, (uint32_t)(KSZ + nt * TB), &bars[st]);
@@ -328,7 +344,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
             return false;
         }
         phase ^= 1u << st;
-        const int cj = block_cnt<CO>(a, u, cj_), vt = (cj + TILE - 1) / TILE;
+        const int cj = cnt_of(cj_), vt = (cj + TILE - 1) / TILE;
         const int t0 = ck_ * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
 
         if (ck_ == 0) {
@@ -803,7 +819,7 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
     return true;
 }
 
-template <int D, int GQ, bool RG, bool CO>
+template <int D, int GQ, bool RG, bool CO, bool TK>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, const __grid_constant__ TableT<RG> st) {
     using C = Cfg<D, GQ>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -844,7 +860,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
             x = ubase + end;
         } else {
             const int end = (int)min(x1 - ubase, (long long)ui.Iu);
-            if (!quant_segment<D, GQ, CO>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
+            if (!quant_segment<D, GQ, CO, TK>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
                                       stg1, bars, phase, qsm, qhl, lane))
                 return;
             x = ubase + end;
@@ -982,7 +998,7 @@ cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cud
 }
 
 // One sequence's counts after T tokens and nf flushes.
-inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf) {
+inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf, int nq_items) {
     SeqEntry e;
     const long long tail_start = (long long)nf * c->G;
     e.base = 0;
@@ -993,13 +1009,17 @@ inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf) {
     // the cold pool's size is known on the device only: items for all C slots
     const int ncold_max = c->cold > 0 ? c->cold : 0;
     e.Sf = (e.ntail + e.npool + ncold_max + FP16_CHUNK - 1) / FP16_CHUNK;
-    e.Iu = e.Sf + nf;
+    e.Iu = e.Sf + nq_items;
     return e;
 }
 
-template <int D, int GQ, bool RG, bool CO>
-cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
+// Kc >= 0: Top-K sparse decode over the Kc selected blocks of every unit.
+template <int D, int GQ, bool RG, bool CO, bool TK>
+cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s,
+                            int Kc = -1) {
     DecodeArgs a;
+    a.sel = c->sel;
+    a.Ksel = Kc;
     a.bcnt = c->bcnt;
     a.ck = c->ck;
     a.cv = c->cv;
@@ -1027,7 +1047,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     if constexpr (RG) {
         long long base = 0;
         for (int b = 0; b < c->B; ++b) {
-            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b]);
+            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], c->nfb[b]);
             st.e[b].base = base;
             base += (long long)c->Hkv * st.e[b].Iu;
         }
@@ -1037,7 +1057,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
         a.nf = a.ntail = a.npool = a.ring_start = a.Sf = a.Iu = 0;   // per sequence in the table
         a.MAXU = c->maxu_r;
     } else {
-        const SeqEntry e = seq_entry(c, c->T, c->nf);
+        const SeqEntry e = seq_entry(c, c->T, c->nf, TK ? Kc : c->nf);
         a.nf = e.nf;
         a.ring_start = e.ring_start;
         a.ntail = e.ntail;
@@ -1053,7 +1073,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     // CTAs only as wide as the active warps need: with few items, the SMs keep
     // room for the combine's CTAs, which then start while the decode drains
     const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
-    k_decode<D, GQ, RG, CO><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
+    k_decode<D, GQ, RG, CO, TK><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ, RG>(a, st, c->B, s);
@@ -1061,18 +1081,31 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
 
 template <int D, int GQ>
 cudaError_t set_decode_attr(int smem_max) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode<D, GQ, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_decode<D, GQ, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_decode<D, GQ, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    const void *fns[] = {
+        reinterpret_cast<const void *>(k_decode<D, GQ, false, false, false>),
+        reinterpret_cast<const void *>(k_decode<D, GQ, false, true, false>),
+        reinterpret_cast<const void *>(k_decode<D, GQ, true, false, false>),
+        reinterpret_cast<const void *>(k_decode<D, GQ, false, false, true>),
+        reinterpret_cast<const void *>(k_decode<D, GQ, false, true, true>),
+    };
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int D, int GQ>
 cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
-    if (c->cold >= 0) return launch_decode_t<D, GQ, false, true>(c, q, out, part, s);
-    return c->ragged ? launch_decode_t<D, GQ, true, false>(c, q, out, part, s)
-                     : launch_decode_t<D, GQ, false, false>(c, q, out, part, s);
+    if (c->cold >= 0) return launch_decode_t<D, GQ, false, true, false>(c, q, out, part, s);
+    return c->ragged ? launch_decode_t<D, GQ, true, false, false>(c, q, out, part, s)
+                     : launch_decode_t<D, GQ, false, false, false>(c, q, out, part, s);
+}
+
+template <int D, int GQ>
+cudaError_t launch_decode_topk_t(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s) {
+    return c->cold >= 0 ? launch_decode_t<D, GQ, false, true, true>(c, q, out, c->part, s, Kc)
+                        : launch_decode_t<D, GQ, false, false, true>(c, q, out, c->part, s, Kc);
 }
 
 }  // namespace
@@ -1098,6 +1131,14 @@ cudaError_t set_kernel_attributes(int d, int gq, int smem_max) {
     if (d == D_ && gq == G_) return set_decode_attr<D_, G_>(smem_max);
     OTT_ATTR(128, 1) OTT_ATTR(128, 2) OTT_ATTR(128, 4) OTT_ATTR(64, 1) OTT_ATTR(64, 2) OTT_ATTR(64, 4)
 #undef OTT_ATTR
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s) {
+#define OTT_DECK(D_, G_) \
+    if (c->d == D_ && c->gq == G_) return launch_decode_topk_t<D_, G_>(c, q, out, Kc, s);
+    OTT_DECK(128, 1) OTT_DECK(128, 2) OTT_DECK(128, 4) OTT_DECK(64, 1) OTT_DECK(64, 2) OTT_DECK(64, 4)
+#undef OTT_DECK
     return cudaErrorInvalidValue;
 }
 

@@ -139,6 +139,10 @@ struct ott_cache {
     int32_t *cidx;          // [U][C]
     int *cmeta;             // [U][2]: tokens in the cold pool, slot of the oldest
     int32_t *bcnt;          // [U][NB] valid tokens of each block
+    // Top-K sparse decode (ott_decode_attn_topk)
+    int32_t *sel;           // [U][Kc] the blocks selected by the last call
+    float *bound;           // [U][NB] scratch: the blocks' score bounds
+    int topk_ok;            // the selection kernel's shared memory fits for NB blocks
 };
 
 namespace ott {
@@ -172,6 +176,10 @@ cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *
 cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
                                    int Lstride, long long t_begin, long long t_end, cudaStream_t s);
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
+cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s);
+cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s);
+int topk_smem_bytes(int d, int gq, int nf);
+cudaError_t set_topk_attributes(int d, int gq, int smem_max);
 cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *stage, cudaStream_t s);
 size_t export_stage_bytes(const ott_cache *c, int nu, int nf);
 int flush_smem_bytes(int d, int G, int P);

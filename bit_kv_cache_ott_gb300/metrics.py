@@ -59,6 +59,26 @@ def cold_unit_bytes(bcount, ncold: int, d: int) -> int:
     return 2 * nq * d // 4 + nonempty * d * 4 + nq * (d // 32) * 4 + int(ncold) * d * 4
 
 
+def topk_bytes_per_unit(T: int, d: int, g: int, G: int, R: int, P: int, K: int) -> int:
+    """Top-K sparse decode of one unit: the bound pass reads every non-empty
+    block's K scale/zero header and the queries; the decode reads the K
+    selected blocks, the residual and pool tokens, the queries, and writes the
+    output. Which blocks are selected depends on the data; they are counted
+    as the K smallest non-empty blocks, so this is a lower bound."""
+    nf = flush_count(T, G, R)
+    npool = pool_size(T, G, R, P)
+    sizes = sorted(n for n in (block_count(j, G, P) for j in range(nf)) if n > 0)
+    kc = min(K, len(sizes))
+    nq = sum(sizes[:kc])
+    bound_pass = len(sizes) * d * 4 + g * d * 2
+    return (bound_pass + 2 * nq * d // 4 + kc * d * 4 + nq * (d // 32) * 4
+            + (T - nf * G + npool) * d * 4 + g * d * 4)
+
+
+def topk_bytes(T: int, B: int, Hq: int, Hkv: int, d: int, G: int, R: int, P: int, K: int) -> int:
+    return B * Hkv * topk_bytes_per_unit(T, d, Hq // Hkv, G, R, P, K)
+
+
 def fp16_cache_bytes(T: int, B: int, Hkv: int, d: int) -> int:
     """The same cache held entirely in fp16 (K and V)."""
     return B * Hkv * T * d * 4

@@ -48,6 +48,7 @@ class Workload:
     seed: int = 1000
     len_lo: int = 0   # > 0: sequence b's prefill length is drawn uniformly from [len_lo, L]
     cold: int = -1    # >= 0: the cold-pool eviction policy with this capacity
+    topk: int = 0     # > 0: decode with ott_decode_attn_topk, this many blocks per (sequence, kv head)
 
     @property
     def g(self) -> int:
@@ -87,6 +88,12 @@ WORKLOADS = {
     "batch_b32_ragged": Workload("batch_b32_ragged", B=32, Hq=32, Hkv=32, d=128, L=7168, steps=512,
                                  G=128, R=32, P=32, seed=1005, len_lo=1024),
     # the headline batch under the cold-pool policy with the pages' 32 slots
+    # long contexts decoded with Top-K sparse access (1/8 and 1/16 of the blocks)
+    "mistral_gqa_g128_topk32": Workload("mistral_gqa_g128_topk32", B=4, Hq=32, Hkv=8, d=128, L=32768,
+                                        steps=256, G=128, R=32, P=32, seed=1003, topk=32),
+    "llama31_8b_131k_topk64": Workload("llama31_8b_131k_topk64", B=1, Hq=32, Hkv=8, d=128, L=131072,
+                                       steps=128, G=128, R=32, P=64, outlier_rate=0.002,
+                                       layers=32, seed=1004, topk=64),
     "batch_b32_cold": Workload("batch_b32_cold", B=32, Hq=32, Hkv=32, d=128, L=4096, steps=512,
                                G=128, R=32, P=32, seed=1002, cold=32),
 }

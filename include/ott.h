@@ -176,6 +176,28 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
  */
 int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream);
 
+/*
+ * Top-K sparse decode (zijie-tian.site sec. 6: OTT combined with sparse access
+ * to the quantized KV). As ott_decode_attn, but each (sequence, kv head)
+ * attends only K of its quantized blocks, next to all its residual and pool
+ * tokens (and cold-pool tokens under that policy): the non-empty blocks with
+ * the largest score bound, ties to the lower block index. The bound of a
+ * block for query head h is the largest q.k that a key dequantized from the
+ * block's per-channel scale s and zero z can reach, sum over channels of
+ * max(q*z, q*(z + 3*s)), in fp32 (round-to-nearest products and sums, channel
+ * order); the block's bound is the largest over the query heads that share
+ * the kv head. A selected block is attended whole. The bound reads only each
+ * block's 4d-byte scale/zero header, so with K well below the block count
+ * the call reads far fewer bytes than ott_decode_attn.
+ * K >= 1 (K >= the block count attends every block). sel: NULL, or a DEVICE
+ * int32 [B*Hkv][min(K, nf)] that receives the selected block indices of each
+ * unit in ascending order (-1 where fewer blocks are non-empty), written on
+ * the stream. Not for a cache after ott_prefill_lens (OTT_ERR_STATE).
+ * OTT_ERR_INVALID also if the selection's shared memory (about 8 bytes per
+ * block slot) does not fit for this max_tokens.
+ */
+int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t *sel, void *stream);
+
 /* Counts (same for every sequence and kv head): tokens seen, blocks (flushes),
  * residual tokens, pool tokens. Host-side, no device access. After
  * ott_prefill_lens the counts differ per sequence; this then reports
