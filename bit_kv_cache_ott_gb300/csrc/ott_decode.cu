@@ -844,6 +844,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
     // fewer active warps than slots every SM still gets its share
     const int gw = warp * gridDim.x + blockIdx.x;
     if (gw >= a.NWp) return;
+    // Top-K: launched as a programmatic dependent of the block selection;
+    // the selected blocks are that grid's results
+    if constexpr (TK) asm volatile("griddepcontrol.wait;" ::: "memory");
     long long x = range_start(a.W, a.NWp, gw);
     const long long x1 = range_start(a.W, a.NWp, gw + 1);
     const int u_first = unit_at<RG>(a, st, x).u;
@@ -1073,8 +1076,23 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     // CTAs only as wide as the active warps need: with few items, the SMs keep
     // room for the combine's CTAs, which then start while the decode drains
     const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
-    k_decode<D, GQ, RG, CO, TK><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if constexpr (TK) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)c->sm_count);
+        cfg.blockDim = dim3((unsigned)(wpc * 32));
+        cfg.dynamicSmemBytes = (size_t)Cfg<D, GQ>::WARP_SMEM * wpc;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k_decode<D, GQ, RG, CO, TK>, a, st);
+    } else {
+        k_decode<D, GQ, RG, CO, TK><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ, RG>(a, st, c->B, s);
 }

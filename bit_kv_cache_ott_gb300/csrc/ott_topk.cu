@@ -12,17 +12,20 @@
 // sums in channel order, so that it is reproducible bit for bit; a block's
 // bound is the largest over the query heads of its kv head.
 //
-// Two kernels:
-//   k_topk_bounds: a CTA per (unit, 32 blocks). The 32 blocks' K scale/zero
-//     headers (4d bytes each, the only part of a block read here) are staged
-//     into shared memory with coalesced loads, in rows padded by one word so
-//     that the threads of a warp, each reading one channel of its own block,
-//     hit different banks. Thread (block, head) then sums its bound in
-//     channel order; the block's bound is the largest over its heads.
-//   k_topk_sort: a CTA per unit. The blocks' (bound, index) keys are sorted
-//     by a bitonic network in shared memory (bound descending, then index);
-//     the first min(K, non-empty blocks) are selected and sorted again by
-//     index, and written to sel[u][0..Kc) (-1 in the slots left over).
+// Two kernels, then the decode, chained by programmatic dependent launches
+// (each starts while the previous one drains and waits for its results):
+//   k_topk_bounds: a CTA of 128 threads per (unit, 32 blocks). The 32
+//     blocks' K scale/zero headers (4d bytes each, the only part of a block
+//     read here) are staged into shared memory, every thread with all its
+//     16-byte loads in flight at once, in rows padded by one word so that the
+//     threads of a warp, each reading one channel of its own block, hit
+//     different banks. Thread (block, head) then sums its bound in channel
+//     order; the block's bound is the largest over its heads.
+//   k_topk_sort: a CTA per unit, one thread per compare-exchange. The blocks'
+//     (bound, index) keys are sorted by a bitonic network in shared memory
+//     (bound descending, then index); the first min(K, non-empty blocks) are
+//     selected and sorted again by index, and written to sel[u][0..Kc) (-1 in
+//     the slots left over).
 #include <math_constants.h>
 
 #include "ott_internal.cuh"
@@ -31,7 +34,8 @@ namespace ott {
 namespace {
 
 constexpr int BND_BLOCKS = 32;      // blocks per bounds CTA
-constexpr int SORT_THREADS = 512;
+constexpr int BND_THREADS = 128;
+constexpr int SORT_THREADS = 512;   // at most
 
 struct TopkArgs {
     const uint8_t *blk;
@@ -47,24 +51,43 @@ struct TopkArgs {
 };
 
 template <int D, int GQ>
-__global__ void __launch_bounds__(BND_BLOCKS * GQ) k_topk_bounds(TopkArgs a) {
+__global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a) {
     constexpr int RW = D + 1;                    // padded row (words)
+    constexpr int V4 = D / 4;                    // 16-byte pieces per header
+    constexpr int PER = BND_BLOCKS * V4 / BND_THREADS;
+    static_assert(BND_BLOCKS * GQ <= BND_THREADS, "one thread per (block, head)");
+    static_assert(BND_BLOCKS * V4 % BND_THREADS == 0, "whole pieces per thread");
     __shared__ uint32_t hdr[BND_BLOCKS * RW];
     __shared__ float qs[GQ * D];
     __shared__ float part[GQ][BND_BLOCKS];
+    // the sort may be scheduled now; it waits for these bounds
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int u = blockIdx.y, j0 = blockIdx.x * BND_BLOCKS, tid = threadIdx.x, nth = blockDim.x;
     const int nb = min(BND_BLOCKS, a.nf - j0);
     const int b = u / a.Hkv, hk = u % a.Hkv;
     const __half *qp = a.q + ((size_t)b * a.Hq + hk * GQ) * D;
     for (int e = tid; e < GQ * D; e += nth) qs[e] = __half2float(qp[e]);
     const uint8_t *base = a.blk + ((size_t)u * a.NB + j0) * a.blk_bytes;
-    for (int e = tid; e < nb * D; e += nth) {
-        const int r = e / D, c = e % D;
-        hdr[r * RW + c] = __ldg(reinterpret_cast<const uint32_t *>(base + (size_t)r * a.blk_bytes) + c);
+    uint4 buf[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = tid + i * BND_THREADS, r = e / V4, v = e % V4;
+        if (r < nb) buf[i] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)r * a.blk_bytes) + v);
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = tid + i * BND_THREADS, r = e / V4, v = e % V4;
+        if (r < nb) {
+            uint32_t *dst = hdr + r * RW + 4 * v;
+            dst[0] = buf[i].x;
+            dst[1] = buf[i].y;
+            dst[2] = buf[i].z;
+            dst[3] = buf[i].w;
+        }
     }
     __syncthreads();
     const int r = tid % BND_BLOCKS, h = tid / BND_BLOCKS;
-    if (r < nb) {
+    if (h < GQ && r < nb) {
         float acc = 0.0f;
         const uint32_t *row = hdr + r * RW;
         const float *qh = qs + h * D;
@@ -118,8 +141,12 @@ __device__ void bitonic_sort(T *k, int n) {
 __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(TopkArgs a, int n2) {
     extern __shared__ unsigned long long keys[];   // [n2]
     int *idx = reinterpret_cast<int *>(keys + n2);  // [n2]: the selected blocks, then in index order
+    // the decode may be scheduled now; it waits for the selection
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
     const float *bd = a.bound + (size_t)u * a.NB;
+    // the bounds are the previous grid's results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // key: (bound descending, index ascending) as one ascending 64-bit key;
     // empty blocks (bound -inf) and padding sort last
     for (int j = tid; j < n2; j += nth) {
@@ -181,7 +208,7 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     bool found = false;
 #define OTT_BND(D_, G_)                                                       \
     if (c->d == D_ && c->gq == G_) {                                          \
-        k_topk_bounds<D_, G_><<<grid, BND_BLOCKS * G_, 0, s>>>(a);            \
+        k_topk_bounds<D_, G_><<<grid, BND_THREADS, 0, s>>>(a);                \
         found = true;                                                         \
     }
     OTT_BND(128, 1) OTT_BND(128, 2) OTT_BND(128, 4) OTT_BND(64, 1) OTT_BND(64, 2) OTT_BND(64, 4)
@@ -190,8 +217,19 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n2 = pow2_at_least(c->nf > 1 ? c->nf : 1);
-    k_topk_sort<<<c->U, SORT_THREADS, topk_smem_bytes(c->d, c->gq, c->nf), s>>>(a, n2);
-    return cudaGetLastError();
+    // one thread per compare-exchange (n2 / 2), whole warps, at most SORT_THREADS
+    const int th = n2 / 2 < 32 ? 32 : (n2 / 2 > SORT_THREADS ? SORT_THREADS : n2 / 2);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)c->U);
+    cfg.blockDim = dim3((unsigned)th);
+    cfg.dynamicSmemBytes = (size_t)topk_smem_bytes(c->d, c->gq, c->nf);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_topk_sort, a, n2);
 }
 
 cudaError_t set_topk_attributes(int d, int gq, int smem_max) {
