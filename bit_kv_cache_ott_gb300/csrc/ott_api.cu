@@ -193,7 +193,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->bcnt = sz_bcnt ? reinterpret_cast<int32_t *>(base + o_bc) : nullptr;
     c->sel = reinterpret_cast<int32_t *>(base + o_sel);
     c->bound = reinterpret_cast<float *>(base + o_bnd);
-    c->topk_ok = topk_smem_bytes(d, gq, c->NB) <= smem_optin;
+    c->topk_ok = topk_smem_bytes(d, gq, c->NB) <= smem_optin - 2048;
     e = cudaMemset(mem, 0, c->mem_bytes);
     if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
     if (e == cudaSuccess) e = set_topk_attributes(d, gq, smem_optin);

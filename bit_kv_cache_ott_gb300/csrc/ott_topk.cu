@@ -21,11 +21,10 @@
 //     threads of a warp, each reading one channel of its own block, hit
 //     different banks. Thread (block, head) then sums its bound in channel
 //     order; the block's bound is the largest over its heads.
-//   k_topk_sort: a CTA per unit, one thread per compare-exchange. The blocks'
-//     (bound, index) keys are sorted by a bitonic network in shared memory
-//     (bound descending, then index); the first min(K, non-empty blocks) are
-//     selected and sorted again by index, and written to sel[u][0..Kc) (-1 in
-//     the slots left over).
+//   k_topk_pick: a CTA per unit. An exact radix select over the bounds (four
+//     8-bit histogram rounds) finds the first min(K, non-empty blocks) under
+//     (bound descending, index ascending); a prefix count writes them to
+//     sel[u][0..Kc) in ascending block order (-1 in the slots left over).
 #include <math_constants.h>
 
 #include "ott_internal.cuh"
@@ -35,7 +34,7 @@ namespace {
 
 constexpr int BND_BLOCKS = 32;      // blocks per bounds CTA
 constexpr int BND_THREADS = 128;
-constexpr int SORT_THREADS = 512;   // at most
+constexpr int SORT_THREADS = 512;   // selection CTA: at most
 
 struct TopkArgs {
     const uint8_t *blk;
@@ -120,62 +119,132 @@ __device__ __forceinline__ uint32_t ordered(float f) {
     return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
 }
 
-// Ascending bitonic sort of n (a power of two) keys in shared memory.
-template <typename T>
-__device__ void bitonic_sort(T *k, int n) {
-    for (int size = 2; size <= n; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-                const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const T x = k[lo], y = k[hi];
-                if ((x > y) == up) {
-                    k[lo] = y;
-                    k[hi] = x;
-                }
-            }
-            __syncthreads();
+// Exclusive prefix sum of v over the threads of the CTA (in thread order);
+// `total` receives the sum over all threads. ws: 32 ints of shared memory.
+__device__ __forceinline__ int block_exscan(int v, int *ws, int &total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int t = lane < nw ? ws[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
         }
+        ws[lane] = t;
+    }
+    __syncthreads();
+    total = ws[nw - 1];
+    const int r = (wid > 0 ? ws[wid - 1] : 0) + x - v;
+    __syncthreads();   // ws is reused by the next call
+    return r;
 }
 
-__global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(TopkArgs a, int n2) {
-    extern __shared__ unsigned long long keys[];   // [n2]
-    int *idx = reinterpret_cast<int *>(keys + n2);  // [n2]: the selected blocks, then in index order
+// The selection, by an exact radix select: key_j = the bit-inverted ordered
+// bound (smallest key = largest bound). Four rounds over 8-bit digits, most
+// significant first, each a histogram of the keys that still match the
+// digits found so far, give the key tau of the need-th smallest key and the
+// number `take` of keys equal to tau that belong to the selection. The
+// selection is every key below tau and the `take` lowest-indexed keys equal
+// to tau: exactly the first min(K, non-empty) blocks under (bound
+// descending, index ascending). A prefix count gives each its slot in
+// ascending block order.
+constexpr uint32_t EMPTY = 0xffffffffu;           // key of an empty block
+
+__global__ void __launch_bounds__(SORT_THREADS) k_topk_pick(TopkArgs a) {
+    extern __shared__ uint32_t key[];              // [nf]
+    __shared__ int hist[256];
+    __shared__ int ws[32];
+    __shared__ int s_digit, s_below;
     // the decode may be scheduled now; it waits for the selection
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
+    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x, n = a.nf;
     const float *bd = a.bound + (size_t)u * a.NB;
+    // a contiguous chunk of blocks per thread, so that prefix counts follow block order
+    const int chunk = (n + nth - 1) / nth, jb = min(n, tid * chunk), je = min(n, jb + chunk);
     // the bounds are the previous grid's results
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // key: (bound descending, index ascending) as one ascending 64-bit key;
-    // empty blocks (bound -inf) and padding sort last
-    for (int j = tid; j < n2; j += nth) {
-        unsigned long long key = ~0ull;
-        if (j < a.nf) {
-            const float f = bd[j];
-            if (f != -CUDART_INF_F) key = ((unsigned long long)(~ordered(f)) << 32) | (unsigned)j;
+    int ne_local = 0;
+    for (int j = jb; j < je; ++j) {
+        const float f = bd[j];
+        const bool nonempty = f != -CUDART_INF_F;
+        key[j] = nonempty ? ~ordered(f) : EMPTY;   // a finite bound never maps to EMPTY
+        ne_local += nonempty;
+    }
+    int ne;
+    block_exscan(ne_local, ws, ne);
+    const int want = min(a.K, ne);
+    uint32_t prefix = 0, mask = 0;
+    int need = want;
+    for (int shift = 24; shift >= 0 && want > 0; shift -= 8) {
+        for (int i = tid; i < 256; i += nth) hist[i] = 0;
+        __syncthreads();
+        for (int j = jb; j < je; ++j) {
+            const uint32_t k = key[j];
+            if (k != EMPTY && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
         }
-        keys[j] = key;
+        __syncthreads();
+        if (tid < 32) {
+            // lane l owns digits 8l .. 8l+7
+            int cnt[8], sum = 0;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                cnt[x] = hist[8 * tid + x];
+                sum += cnt[x];
+            }
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const int excl = incl - sum;
+            if (excl < need && need <= incl) {   // exactly one lane
+                int c = excl, dg = 8 * tid;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    if (c + cnt[x] >= need) {
+                        dg = 8 * tid + x;
+                        break;
+                    }
+                    c += cnt[x];
+                }
+                s_digit = dg;
+                s_below = c;
+            }
+        }
+        __syncthreads();
+        prefix |= (uint32_t)s_digit << shift;
+        mask |= 255u << shift;
+        need -= s_below;
+        __syncthreads();
     }
-    __syncthreads();
-    bitonic_sort(keys, n2);
-    // the selected blocks, then in ascending order (m2: a power of two >= Kc, <= n2)
-    int m2 = 1;
-    while (m2 < a.Kc) m2 <<= 1;
-    for (int i = tid; i < m2; i += nth) {
-        const unsigned long long key = i < a.Kc ? keys[i] : ~0ull;
-        idx[i] = key == ~0ull ? 0x7fffffff : (int)(unsigned)(key & 0xffffffffull);
+    // keys equal to tau = prefix: the `need` lowest-indexed ones are taken
+    int eq_local = 0;
+    for (int j = jb; j < je; ++j) eq_local += want > 0 && key[j] != EMPTY && key[j] == prefix;
+    int eq_total;
+    int eq_before = block_exscan(eq_local, ws, eq_total);
+    int sel_local = 0;
+    for (int j = jb; j < je; ++j) {
+        const uint32_t k = key[j];
+        const bool ok = want > 0 && k != EMPTY;
+        const bool take = ok && (k < prefix || (k == prefix && eq_before++ < need));
+        key[j] = take ? 1u : 0u;                   // reused as the selection mark
+        sel_local += take;
     }
-    __syncthreads();
-    bitonic_sort(idx, m2);
+    int nsel;
+    int pos = block_exscan(sel_local, ws, nsel);
     int32_t *out = a.sel + (size_t)u * a.Kc;
-    for (int i = tid; i < a.Kc; i += nth) out[i] = idx[i] == 0x7fffffff ? -1 : idx[i];
-}
-
-int pow2_at_least(int n) {
-    int p = 1;
-    while (p < n) p <<= 1;
-    return p;
+    for (int j = jb; j < je; ++j)
+        if (key[j]) out[pos++] = j;
+    for (int i = nsel + tid; i < a.Kc; i += nth) out[i] = -1;
 }
 
 }  // namespace
@@ -183,8 +252,7 @@ int pow2_at_least(int n) {
 int topk_smem_bytes(int d, int gq, int nf) {
     (void)d;
     (void)gq;
-    const int n2 = pow2_at_least(nf > 1 ? nf : 1);
-    return n2 * 8 + n2 * 4;
+    return (nf > 1 ? nf : 1) * 4;
 }
 
 cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s) {
@@ -216,9 +284,9 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     if (!found) return cudaErrorInvalidValue;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int n2 = pow2_at_least(c->nf > 1 ? c->nf : 1);
-    // one thread per compare-exchange (n2 / 2), whole warps, at most SORT_THREADS
-    const int th = n2 / 2 < 32 ? 32 : (n2 / 2 > SORT_THREADS ? SORT_THREADS : n2 / 2);
+    // whole warps, up to SORT_THREADS, about two blocks per thread
+    int th = ((c->nf + 1) / 2 + 31) / 32 * 32;
+    th = th < 32 ? 32 : (th > SORT_THREADS ? SORT_THREADS : th);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c->U);
     cfg.blockDim = dim3((unsigned)th);
@@ -229,13 +297,13 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_topk_sort, a, n2);
+    return cudaLaunchKernelEx(&cfg, k_topk_pick, a);
 }
 
 cudaError_t set_topk_attributes(int d, int gq, int smem_max) {
     (void)d;
     (void)gq;
-    return cudaFuncSetAttribute(k_topk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    return cudaFuncSetAttribute(k_topk_pick, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max - 2048);
 }
 
 }  // namespace ott
