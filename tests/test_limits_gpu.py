@@ -1,6 +1,7 @@
 """GPU parity at the limits the library accepts: the largest outlier pool
 whose flush staging fits one CTA's shared memory, a batch with more
-(sequence, kv head) units than the decode grid has warps, and a ragged batch
+(sequence, kv head) units than the decode grid has warps, one or two units
+long enough that every decode warp holds a piece of them, and a ragged batch
 of the maximum 256 sequences. Same bar as the other parity tests: state
 bit-exact against the CPU oracle, outputs within max |d| <= 2e-3 and mean
 |d| <= 2e-4 of its double result.
@@ -45,3 +46,13 @@ def test_ragged_at_the_sequence_limit(oracle_mod, ott):
     rng = np.random.default_rng(256)
     lens = [int(x) for x in rng.integers(1, 70, size=256)]
     _run_ragged(oracle_mod, ott, 256, 2, 1, 64, 16, 2, 3, lens, 20, seed=256, every=10)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,G,R,P,L", [
+    (1, 2, 1, 4, 1, 2, 10000),     # one unit of 2,500 blocks: every decode warp holds a piece of it
+    (1, 8, 2, 8, 2, 5, 12000),     # two GQA units of 1,500 blocks
+])
+def test_one_long_unit(oracle_mod, ott, B, Hq, Hkv, G, R, P, L):
+    """Thousands of blocks in one or two units: every decode warp holds a
+    piece of a unit, and the combine merges thousands of partials per head."""
+    _run_small(oracle_mod, ott, B, Hq, Hkv, 128, G, R, P, L, 3, seed=L + G, check_every_step=False)
