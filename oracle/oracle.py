@@ -55,6 +55,8 @@ def lib():
             L.orc_create_policy.argtypes = [i32] * 8
             L.orc_export_cold.argtypes = [P, i32, P, P, P]
             L.orc_topk_select.argtypes = [P, i32, i32, P, i32, P, P]
+            L.orc_release_seq.argtypes = [P, i32]
+            L.orc_prefill_seq.argtypes = [P, i32, P, P, i32]
             L.orc_decode_topk.argtypes = [P, P, i32, P]
             L.orc_destroy.argtypes = [P]
             L.orc_append.argtypes = [P, P, P]
@@ -176,7 +178,20 @@ class OracleCache:
     def append(self, k, v):
         """k, v: fp16 [B][Hkv][d]."""
         kb, vb = _bits(k), _bits(v)
-        lib().orc_append(self._h, _ptr(kb), _ptr(vb))
+        if lib().orc_append(self._h, _ptr(kb), _ptr(vb)):
+            raise RuntimeError("append while a sequence is empty")
+
+    def release_seq(self, b: int):
+        """Sequence b drops every token; it must be refilled before the next append or decode."""
+        if lib().orc_release_seq(self._h, int(b)):
+            raise ValueError("bad sequence index")
+
+    def prefill_seq(self, b: int, K, V):
+        """Fill the empty sequence b: K, V fp16 [Hkv][L][d]."""
+        Kb, Vb = _bits(K), _bits(V)
+        rc = lib().orc_prefill_seq(self._h, int(b), _ptr(Kb), _ptr(Vb), Kb.shape[1])
+        if rc:
+            raise RuntimeError("prefill_seq rejected (sequence not empty or bad length)")
 
     def decode(self, q) -> np.ndarray:
         """q: fp16 [B][Hq][d] -> float64 [B][Hq][d]."""

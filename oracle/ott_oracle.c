@@ -57,6 +57,11 @@
  *      and no store holds them any more. The new block is the group's
  *      tokens that did not enter the pool. Decode attends the cold pool like
  *      the outlier pool; discarded tokens are not attended.
+ *  R13 A sequence of a batch can be released (it then holds no token) and
+ *      refilled with a new prompt; from then on it is a fresh sequence of
+ *      its own (R10): its tokens are numbered from 0, and no state of the
+ *      released one remains. Appends and decodes need every sequence to
+ *      hold at least one token.
  *  R12 Top-K sparse access ([blog] sec. 6, combining OTT with sparse KV
  *      access): a decode call may attend only K of a unit's quantized
  *      blocks, plus every residual, pool and cold token. The K blocks are
@@ -468,6 +473,9 @@ int orc_append(void *hp, const uint16_t *k, const uint16_t *v)
 {
     orc_cache *h = (orc_cache *)hp;
     const int U = h->B * h->Hkv;
+    for (int b = 0; b < h->B; ++b)     /* R13: every sequence holds a token */
+        if (h->T > 0 && h->Tb[b] == 0)
+            return -2;
     for (int i = 0; i < U; ++i)
         append_unit(h, &h->u[i], h->Tb[i / h->Hkv], k + (size_t)i * h->d, v + (size_t)i * h->d);
     for (int b = 0; b < h->B; ++b)
@@ -516,6 +524,50 @@ int orc_prefill_lens(void *hp, const uint16_t *K, const uint16_t *V, const int32
         longest = lens[b] > longest ? lens[b] : longest;
     }
     h->T = longest;
+    return 0;
+}
+
+/* R13: release sequence b: its units drop every token and block. */
+static void clear_unit(orc_unit *u)
+{
+    for (int j = 0; j < u->nb; ++j) {
+        orc_block *b = &u->blk[j];
+        free(b->idx); free(b->kcode); free(b->ks); free(b->kz);
+        free(b->vcode); free(b->vs); free(b->vz);
+    }
+    u->nb = 0;
+    u->tail_n = 0;
+    u->pool_n = 0;
+    u->cold_n = 0;
+}
+
+int orc_release_seq(void *hp, int b)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (b < 0 || b >= h->B)
+        return -1;
+    for (int x = 0; x < h->Hkv; ++x)
+        clear_unit(&h->u[b * h->Hkv + x]);
+    h->Tb[b] = 0;
+    return 0;
+}
+
+/* R13: fill the empty sequence b with a prompt of L tokens.
+ * K, V: fp16 bits [Hkv][L][d]. */
+int orc_prefill_seq(void *hp, int b, const uint16_t *K, const uint16_t *V, int L)
+{
+    orc_cache *h = (orc_cache *)hp;
+    if (b < 0 || b >= h->B || L < 1)
+        return -1;
+    if (h->Tb[b] != 0)
+        return -2;
+    const int d = h->d;
+    for (int x = 0; x < h->Hkv; ++x)
+        for (int t = 0; t < L; ++t)
+            append_unit(h, &h->u[b * h->Hkv + x], t, K + ((size_t)x * L + t) * d, V + ((size_t)x * L + t) * d);
+    h->Tb[b] = L;
+    if (L > h->T)
+        h->T = L;
     return 0;
 }
 

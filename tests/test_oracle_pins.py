@@ -353,3 +353,44 @@ def test_ragged_batch_is_independent_sequences(oracle_mod):
     bad = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
     with pytest.raises(RuntimeError):
         bad.prefill_lens(K, V, [1, 2, 3, Lmax + 1])       # a length beyond the staged tokens
+
+
+def test_released_and_refilled_sequence_is_a_fresh_one(oracle_mod):
+    """A released sequence refilled with a new prompt equals a one-sequence
+    cache that only ever saw that prompt (state bit for bit, outputs exactly),
+    and the other sequences are untouched by the release."""
+    B, Hq, Hkv, d, G, R, P = 3, 4, 2, 64, 8, 2, 3
+    g = torch.Generator().manual_seed(9)
+    K = torch.randn(B, Hkv, 90, d, generator=g).half()
+    V = torch.randn(B, Hkv, 90, d, generator=g).half()
+    K2 = torch.randn(Hkv, 37, d, generator=g).half()
+    V2 = torch.randn(Hkv, 37, d, generator=g).half()
+    steps = [(torch.randn(B, Hkv, d, generator=g).half(), torch.randn(B, Hkv, d, generator=g).half())
+             for _ in range(20)]
+    lens = [90, 60, 75]
+    big = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    big.prefill_lens(K, V, lens)
+    for k, v in steps[:5]:
+        big.append(k, v)
+    before = [big.export_unit(u) for u in range(B * Hkv)]
+    big.release_seq(1)
+    with pytest.raises(RuntimeError):
+        big.append(*steps[5])                  # an empty sequence blocks appends
+    big.prefill_seq(1, K2, V2)
+    fresh = oracle_mod.OracleCache(1, Hq, Hkv, d, G, R, P)
+    fresh.prefill(K2[None], V2[None])
+    for u in (0, 1, 4, 5):                     # sequences 0 and 2 untouched
+        e = big.export_unit(u)
+        for key in ("bidx", "kcode", "ks", "vcode", "tidx", "tk", "pidx", "pk"):
+            assert np.array_equal(e[key], before[u][key]), (u, key)
+    for k, v in steps[5:]:
+        big.append(k, v)
+        fresh.append(k[1:2], v[1:2])
+    for x in range(Hkv):
+        a, f = big.export_unit(1 * Hkv + x), fresh.export_unit(x)
+        assert (a["T"], a["nf"], a["tail"], a["npool"]) == (f["T"], f["nf"], f["tail"], f["npool"]) == (52, 6, 4, 3)
+        for key in ("bcount", "bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tidx", "tk", "tv", "pidx", "pnorm",
+                    "pk", "pv"):
+            assert np.array_equal(a[key], f[key]), (x, key)
+    q = torch.randn(B, Hq, d, generator=g).half()
+    assert np.array_equal(big.decode(q)[1], fresh.decode(q[1:2])[0])
