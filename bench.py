@@ -330,8 +330,11 @@ def run_ours(args, w):
     caches = []
     lens = synth.seq_lens(wr)
     for layer in range(w.layers):
+        pool = None
+        if w.paged:   # the blocks the run fills, from one pool
+            pool = sum(metrics.flush_count(t + total_steps, w.G, w.R) for t in lens) * w.Hkv + 1
         c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged,
-                         cold=cold_of(w))
+                         cold=cold_of(w), pool_blocks=pool)
         K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
         if w.ragged:
             c.prefill_lens(K, V, lens)
@@ -499,6 +502,8 @@ def run_ours(args, w):
                        "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
                        **({"topk": w.topk, "topk_bytes": "bound pass over every non-empty block's scale/zero "
                            "header, plus the K smallest non-empty blocks (a lower bound)"} if w.topk > 0 else {}),
+                       **({"paged": "blocks from one pool of the blocks the run fills, through a block table"}
+                          if w.paged else {}),
                        **({"cold": w.cold, "cold_bytes": "block and cold-pool sizes read from the device "
                            "before and after the timed region, linear in between"} if w.cold >= 0 else {}),
                        **({"ragged_lens": {"min": min(lens), "max": max(lens),

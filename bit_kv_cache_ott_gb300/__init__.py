@@ -37,7 +37,8 @@ class StateExport(C.Structure):
                 ("bidx", "kcode", "ks", "kz", "vcode", "vs", "vz", "tk", "tv", "pidx", "pnorm", "pk", "pv")]
 
 
-SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
+SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_paged", "ott_release_seq", "ott_prefill_seq",
+           "ott_free_blocks", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
            "ott_decode_attn", "ott_decode_attn_static", "ott_decode_attn_topk", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
            "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str")
 
@@ -61,6 +62,11 @@ def load(build_if_missing: bool = False):
     L.ott_create.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_create_ragged.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_create_cold.argtypes = [i32] * 9 + [C.POINTER(P)]
+    L.ott_create_paged.argtypes = [i32] * 8 + [i64, C.POINTER(P)]
+    L.ott_release_seq.argtypes = [P, i32, P]
+    L.ott_prefill_seq.argtypes = [P, i32, P, P, i32, P]
+    L.ott_free_blocks.argtypes = [P]
+    L.ott_free_blocks.restype = i64
     L.ott_export_cold.argtypes = [P, i32, i32, P, P, P, P, P]
     L.ott_destroy.argtypes = [P]
     L.ott_prefill.argtypes = [P, P, P, i32, P]
@@ -111,14 +117,19 @@ class OTTCache:
     ``ott_create_cold``: displaced pool tokens go to a first-in-first-out
     fp16 cold pool of C slots instead of the new block."""
 
-    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False, cold=None):
+    def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False, cold=None,
+                 pool_blocks=None):
         L = load()
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
         self.max_tokens = max_tokens
         self.ragged = ragged
         self.cold = cold
         h = C.c_void_p()
-        if cold is not None:
+        if pool_blocks is not None:
+            self.ragged = True
+            _check(L.ott_create_paged(B, Hq, Hkv, d, G, R, P, max_tokens, int(pool_blocks), C.byref(h)),
+                   "ott_create_paged")
+        elif cold is not None:
             if ragged:
                 raise ValueError("the cold-pool policy takes sequences of one length")
             _check(L.ott_create_cold(B, Hq, Hkv, d, G, R, P, int(cold), max_tokens, C.byref(h)), "ott_create_cold")
@@ -208,6 +219,21 @@ class OTTCache:
         _check(load().ott_get_seq_counts(self._h, b, C.byref(T), C.byref(nf), C.byref(tail), C.byref(npool)),
                "ott_get_seq_counts")
         return T.value, nf.value, tail.value, npool.value
+
+    def release_seq(self, b: int, stream=None):
+        """Sequence b finishes: it drops its tokens (and its pool blocks)."""
+        _check(load().ott_release_seq(self._h, int(b), _stream(stream)), "ott_release_seq")
+
+    def prefill_seq(self, b: int, K: torch.Tensor, V: torch.Tensor, stream=None):
+        """Fill the empty sequence b with a prompt: K, V fp16 [Hkv][L][d] on the device."""
+        L = K.shape[1] if K.dim() == 3 else -1
+        shp = (self.Hkv, L, self.d)
+        _check(load().ott_prefill_seq(self._h, int(b), _dev_ptr(K, shp, "K"), _dev_ptr(V, shp, "V"), L,
+                                      _stream(stream)), "ott_prefill_seq")
+
+    def free_blocks(self) -> int:
+        """Free blocks of the paged pool (-1 without one)."""
+        return int(load().ott_free_blocks(self._h))
 
     def cold_sizes(self):
         """Cold-pool policy: (block sizes [U][nf], cold-pool sizes [U]) from the device."""

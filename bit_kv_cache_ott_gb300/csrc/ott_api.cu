@@ -35,7 +35,19 @@ bool flush_due_seq(const ott_cache *c, int b) {
 int flushes_after(const ott_cache *c, long long T) { return T >= c->G + c->R ? (int)((T - c->R) / c->G) : 0; }
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 int cold, ott_cache **out);
+                 int cold, ott_cache **out, long long pool_blocks = 0);
+
+// Paged pool: blocks that flushes of these sequences (group j of sequence b
+// for j in [nf_from[b], nf_to[b])) need. 0 for a cache without the pool.
+long long blocks_needed(const ott_cache *c, long long n_unit_flushes) { return c->paged ? n_unit_flushes : 0; }
+
+// Ragged caches: every sequence must hold a token for appends and decodes.
+bool some_sequence_empty(const ott_cache *c) {
+    if (!c->ragged) return false;
+    for (int b = 0; b < c->B; ++b)
+        if (c->Tb[b] == 0) return true;
+    return false;
+}
 
 }  // namespace
 
@@ -66,6 +78,15 @@ int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C, i
     return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, C, out);
 }
 
+int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, long long pool_blocks,
+                     ott_cache **out) {
+    if (B > RAGGED_MAX || pool_blocks < 1 || pool_blocks > 0x7fffffffLL) {
+        if (out) *out = nullptr;
+        return OTT_ERR_INVALID;
+    }
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 1, -1, out, pool_blocks);
+}
+
 int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, ott_cache **out) {
     if (B > RAGGED_MAX) {
         if (out) *out = nullptr;
@@ -79,7 +100,7 @@ int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int ma
 namespace {
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 int cold, ott_cache **out) {
+                 int cold, ott_cache **out, long long pool_blocks) {
     if (!out) return OTT_ERR_INVALID;
     *out = nullptr;
     if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
@@ -129,7 +150,11 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const int maxu_alloc = c->maxu > c->maxu_r ? c->maxu : c->maxu_r;
 
     const size_t U = (size_t)c->U;
-    const size_t sz_blk = U * c->NB * (size_t)c->blk_bytes;
+    c->paged = pool_blocks > 0;
+    c->pool_blocks = (int)pool_blocks;
+    c->free_blocks = pool_blocks;
+    const size_t sz_blk = (c->paged ? (size_t)pool_blocks : U * c->NB) * (size_t)c->blk_bytes;
+    const size_t sz_bt = c->paged ? U * c->NB * 4 : 0, sz_fs = c->paged ? (size_t)pool_blocks * 4 : 0;
     const size_t sz_bidx = U * c->NB * (size_t)G * 4;
     const size_t sz_ring = U * c->ring * (size_t)d * 2;
     const size_t sz_pool = U * (size_t)P * d * 2;
@@ -157,6 +182,9 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t o_cm = off; off = round_up(off + sz_cmeta, 256);
     const size_t o_bc = off; off = round_up(off + sz_bcnt, 256);
     const size_t o_sel = off; off = round_up(off + sz_sel, 256);
+    const size_t o_bt = off; off = round_up(off + sz_bt, 256);
+    const size_t o_fs = off; off = round_up(off + sz_fs, 256);
+    const size_t o_ft = off; off = round_up(off + 16, 256);
     const size_t o_bnd = off; off = round_up(off + sz_sel, 256);
     c->mem_bytes = off;
 
@@ -192,11 +220,22 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->cmeta = sz_cmeta ? reinterpret_cast<int *>(base + o_cm) : nullptr;
     c->bcnt = sz_bcnt ? reinterpret_cast<int32_t *>(base + o_bc) : nullptr;
     c->sel = reinterpret_cast<int32_t *>(base + o_sel);
+    c->bt = sz_bt ? reinterpret_cast<int32_t *>(base + o_bt) : nullptr;
+    c->fstack = sz_fs ? reinterpret_cast<int32_t *>(base + o_fs) : nullptr;
+    c->ftop = reinterpret_cast<int *>(base + o_ft);
     c->bound = reinterpret_cast<float *>(base + o_bnd);
     c->topk_ok = topk_smem_bytes(d, gq, c->NB) <= smem_optin - 2048;
     e = cudaMemset(mem, 0, c->mem_bytes);
     if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
     if (e == cudaSuccess) e = set_topk_attributes(d, gq, smem_optin);
+    if (e == cudaSuccess && c->paged) {
+        // every pool slot free
+        std::vector<int32_t> slots((size_t)pool_blocks);
+        for (long long i = 0; i < pool_blocks; ++i) slots[(size_t)i] = (int32_t)i;
+        const int top = (int)pool_blocks;
+        e = cudaMemcpy(c->fstack, slots.data(), slots.size() * 4, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaMemcpy(c->ftop, &top, sizeof(int), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(mem);
@@ -232,6 +271,8 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     const int nf = L >= c->G + c->R ? (L - c->R) / c->G : 0;
+    if (blocks_needed(c, (long long)nf * c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
+    c->free_blocks -= blocks_needed(c, (long long)nf * c->U);
     for (int j = 0; j < nf; ++j) {
         cudaError_t e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
         if (e != cudaSuccess) return fail_cuda(c, e);
@@ -249,11 +290,15 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
     if (!lens || Lmax < 1 || !K || !V || !aligned16(K) || !aligned16(V)) return OTT_ERR_INVALID;
     if (Lmax > c->max_tokens) return OTT_ERR_CAPACITY;
     int nf_max = 0;
+    long long unit_flushes = 0;
     for (int b = 0; b < c->B; ++b) {
         if (lens[b] < 1 || lens[b] > Lmax) return OTT_ERR_INVALID;
         const int nf = flushes_after(c, lens[b]);
         nf_max = nf > nf_max ? nf : nf_max;
+        unit_flushes += (long long)nf * c->Hkv;
     }
+    if (blocks_needed(c, unit_flushes) > c->free_blocks) return OTT_ERR_CAPACITY;
+    c->free_blocks -= blocks_needed(c, unit_flushes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     // group j of every sequence that has one, in token order
@@ -288,6 +333,11 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
 namespace {
 
 int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+    long long due = 0;   // sequences whose residual window fills with this token
+    for (int b = 0; b < c->B; ++b)
+        due += c->Tb[b] + 1 - (long long)c->nfb[b] * c->G >= (long long)c->G + c->R;
+    if (blocks_needed(c, due * c->Hkv) > c->free_blocks) return OTT_ERR_CAPACITY;
+    c->free_blocks -= blocks_needed(c, due * c->Hkv);
     cudaError_t e = launch_append_ragged(c, k, v, s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     FlushList fl;
@@ -314,9 +364,13 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     if (c->poisoned) return OTT_ERR_STATE;
     if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
     if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
+    if (some_sequence_empty(c)) return OTT_ERR_STATE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (c->ragged)
         return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
+    const bool due = c->T + 1 - (long long)c->nf * c->G >= (long long)c->G + c->R;
+    if (due && blocks_needed(c, c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
+    if (due) c->free_blocks -= blocks_needed(c, c->U);
     cudaError_t e = launch_append(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T += 1;
@@ -330,7 +384,7 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
 
 int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
     if (!c) return OTT_ERR_INVALID;
-    if (c->poisoned || c->T < 1) return OTT_ERR_STATE;
+    if (c->poisoned || c->T < 1 || some_sequence_empty(c)) return OTT_ERR_STATE;
     if (!q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
     cudaError_t e = launch_decode(c, static_cast<const __half *>(q), static_cast<__half *>(out),
                                   static_cast<cudaStream_t>(stream));
@@ -339,7 +393,7 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
 
 int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t *sel, void *stream) {
     if (!c) return OTT_ERR_INVALID;
-    if (c->poisoned || c->T < 1 || c->ragged) return OTT_ERR_STATE;
+    if (c->poisoned || c->T < 1 || c->ragged || c->paged) return OTT_ERR_STATE;
     if (K < 1 || !c->topk_ok || !q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *qh = static_cast<const __half *>(q);
@@ -350,6 +404,57 @@ int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t 
     if (e == cudaSuccess && sel && Kc > 0)
         e = cudaMemcpyAsync(sel, c->sel, (size_t)c->U * Kc * 4, cudaMemcpyDeviceToDevice, s);
     return fail_cuda(c, e);
+}
+
+int ott_release_seq(ott_cache *c, int b, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || !c->ragged_capable || c->T < 1) return OTT_ERR_STATE;
+    if (b < 0 || b >= c->B) return OTT_ERR_INVALID;
+    if (!c->ragged) {   // a uniform prefill so far: switch to per-sequence counts
+        c->Tb.assign(c->B, c->T);
+        c->nfb.assign(c->B, c->nf);
+        c->ragged = 1;
+        c->nf = 0;
+    }
+    cudaError_t e = launch_release(c, b, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    c->free_blocks += blocks_needed(c, (long long)c->nfb[b] * c->Hkv);
+    c->Tb[b] = 0;
+    c->nfb[b] = 0;
+    return OTT_OK;
+}
+
+int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned || !c->ragged) return OTT_ERR_STATE;
+    if (b < 0 || b >= c->B || L < 1 || !K || !V || !aligned16(K) || !aligned16(V)) return OTT_ERR_INVALID;
+    if (c->Tb[b] != 0) return OTT_ERR_STATE;   // release the sequence first
+    if (L > c->max_tokens) return OTT_ERR_CAPACITY;
+    const int nf = flushes_after(c, L);
+    if (blocks_needed(c, (long long)nf * c->Hkv) > c->free_blocks) return OTT_ERR_CAPACITY;
+    c->free_blocks -= blocks_needed(c, (long long)nf * c->Hkv);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
+    for (int j = 0; j < nf; ++j) {
+        FlushList fl;
+        fl.n = 1;
+        fl.lb[0] = b;
+        fl.lj[0] = j;
+        cudaError_t e = launch_flush_list_src(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, b * c->Hkv, fl, s);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
+    cudaError_t e = launch_copy_tail_units(c, Kh, Vh, b * c->Hkv, c->Hkv, L, (long long)nf * c->G, L, s,
+                                           b * c->Hkv);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    c->Tb[b] = L;
+    c->nfb[b] = nf;
+    if (L > c->T) c->T = L;
+    return OTT_OK;
+}
+
+long long ott_free_blocks(const ott_cache *c) {
+    if (!c) return OTT_ERR_INVALID;
+    return c->paged ? c->free_blocks : -1;
 }
 
 int ott_get_seq_counts(const ott_cache *c, int b, long long *T, int *nf, int *tail, int *n_pool) {

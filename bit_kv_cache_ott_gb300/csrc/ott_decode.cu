@@ -136,6 +136,9 @@ struct DecodeArgs {
     // sel[u][0..Ksel) (ascending, -1 for none) instead of blocks 0..nf-1
     const int32_t *sel;
     int Ksel;
+    // paged pool (ragged caches from ott_create_paged): block j of unit u is
+    // pool slot bt[u*NB + j]; null otherwise
+    const int32_t *bt;
 };
 
 template <int D, int GQ>
@@ -257,7 +260,7 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 // ---------------------------------------------------------------- quantized segment
 // Blocks [j0, j1) of unit u (Top-K: the blocks listed at positions [j0, j1)
 // of the unit's selection); the partial goes to part[slot].
-template <int D, int GQ, bool CO, bool TK>
+template <int D, int GQ, bool CO, bool TK, bool RG>
 __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
                               int lane) {
@@ -286,7 +289,11 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
         if (lane == 0) {
             const int vt = (cnt_of(j) + TILE - 1) / TILE;
             const int t0 = k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
-            const uint8_t *bsrc = a.blk + ((size_t)u * a.NB + blk_of(j)) * a.blk_bytes;
+            size_t bslot = (size_t)u * a.NB + blk_of(j);
+            if constexpr (RG) {
+                if (a.bt) bslot = (size_t)__ldg(a.bt + bslot);
+            }
+            const uint8_t *bsrc = a.blk + bslot * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
             if (k == 0)
                 bulk_load(dst, bsrc, (uint32_t)(KSZ + nt * TB), &bars[st]);
@@ -863,7 +870,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
             x = ubase + end;
         } else {
             const int end = (int)min(x1 - ubase, (long long)ui.Iu);
-            if (!quant_segment<D, GQ, CO, TK>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
+            if (!quant_segment<D, GQ, CO, TK, RG>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
                                       stg1, bars, phase, qsm, qhl, lane))
                 return;
             x = ubase + end;
@@ -1023,6 +1030,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     DecodeArgs a;
     a.sel = c->sel;
     a.Ksel = Kc;
+    a.bt = c->paged ? c->bt : nullptr;
     a.bcnt = c->bcnt;
     a.ck = c->ck;
     a.cv = c->cv;
@@ -1217,6 +1225,9 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
     using namespace ott;
     if (!c) return OTT_ERR_INVALID;
     if (c->poisoned || c->T < 1) return OTT_ERR_STATE;
+    if (c->ragged)
+        for (int b = 0; b < c->B; ++b)
+            if (c->Tb[b] == 0) return OTT_ERR_STATE;   // a released sequence not refilled yet
     if (!q || !out || q == out || (reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u))
         return OTT_ERR_INVALID;
     int dev = -1;

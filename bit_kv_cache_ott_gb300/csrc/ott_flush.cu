@@ -57,6 +57,11 @@ struct FlushArgs {
     int *cmeta;                  // [U][2]: tokens in the cold pool, slot of the oldest
     int32_t *bcnt;               // [U][NB] valid tokens of each block (cold-pool policy)
     int C;                       // cold-pool capacity; -1: displaced tokens are written back
+    int32_t *bt;                 // paged pool: [U][NB] slot of each block (null: slot u*NB + j)
+    int32_t *fstack;             // paged pool: free slots
+    int *ftop;                   // paged pool: number of free slots
+    int *ctl;                    // status word: [1] set when the pool had no free slot
+    int src_u0;                  // the source holds units src_u0, src_u0 + 1, ...
     long long src_unit_stride;   // elements between units in the source
     long long src_mod;           // slot = token mod src_mod
     long long t0;                // first token of the group
@@ -108,7 +113,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
             sv = a.pv + off;
         } else {
             const long long t = t0 + (row - np0);
-            const size_t off = (size_t)u * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
+            const size_t off = (size_t)(u - a.src_u0) * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
             sk = a.srcK + off;
             sv = a.srcV + off;
         }
@@ -216,7 +221,23 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         }
     }
 
-    uint8_t *bb = a.blk + ((size_t)u * a.NB + jj) * a.blk_bytes;
+    // the block's slot: its own, or (paged pool) one taken from the free
+    // slots; the host has checked that enough are free
+    size_t slot = (size_t)u * a.NB + jj;
+    if (a.bt) {
+        if (tid == 0) {
+            const int top = atomicSub(a.ftop, 1) - 1;
+            if (top >= 0) {
+                a.bt[slot] = a.fstack[top];
+            } else {   // never with the host's count; recorded instead of reading out of bounds
+                a.bt[slot] = 0;
+                atomicExch(a.ctl + 1, 1);
+            }
+        }
+        __syncthreads();
+        slot = (size_t)__ldcg(a.bt + slot);
+    }
+    uint8_t *bb = a.blk + slot * a.blk_bytes;
     uint8_t *tiles = bb + ksz_bytes(D);
     for (int t = tid; t < G; t += nth)
         a.bidx[((size_t)u * a.NB + jj) * G + t] = t < cnt ? (int32_t)(uint32_t)key[bmap[t]] : -1;
@@ -324,7 +345,7 @@ __global__ void k_append_ragged(const uint4 *__restrict__ k, const uint4 *__rest
 
 // tokens [t_begin, t_end) of units [u0, u0+nu) of K, V [U][Lstride][d] -> their ring slots
 __global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half *rv, int u0, int nu, int d,
-                            int ring, int Lstride, long long t_begin, long long t_end) {
+                            int ring, int Lstride, long long t_begin, long long t_end, int src_u0) {
     const int vpr = d / 8;
     const long long ntok = t_end - t_begin;
     const long long total = (long long)nu * ntok * vpr;
@@ -334,7 +355,7 @@ __global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half
         const long long tt = (e / vpr) % ntok;
         const int u = u0 + (int)(e / vpr / ntok);
         const long long t = t_begin + tt;
-        const size_t src = ((size_t)u * Lstride + t) * d;
+        const size_t src = ((size_t)(u - src_u0) * Lstride + t) * d;
         const size_t dst = ((size_t)u * ring + (size_t)(t % ring)) * d;
         reinterpret_cast<uint4 *>(rk + dst)[x] = reinterpret_cast<const uint4 *>(K + src)[x];
         reinterpret_cast<uint4 *>(rv + dst)[x] = reinterpret_cast<const uint4 *>(V + src)[x];
@@ -345,11 +366,17 @@ __global__ void k_copy_tail(const __half *K, const __half *V, __half *rk, __half
 //   kcode/vcode [nu][nf][G][d/4] bytes, ks/kz [nu][nf][d], vs/vz [nu][nf][G][d/32]
 struct ExportArgs {
     const uint8_t *blk;
+    const int32_t *bt;       // paged pool: slot of each block (null: u*NB + j)
     long long blk_bytes;
     int NB, nf, G, d, u0, nu;
     uint8_t *kcode, *vcode;
     uint16_t *ks, *kz, *vs, *vz;
 };
+
+__device__ __forceinline__ size_t export_slot(const ExportArgs &a, int u, int j) {
+    const size_t own = (size_t)u * a.NB + j;
+    return a.bt ? (size_t)a.bt[own] : own;
+}
 
 __global__ void k_export(ExportArgs a) {
     const int d = a.d, rb = d / 4, NG = d / 32;
@@ -363,7 +390,7 @@ __global__ void k_export(ExportArgs a) {
         const int t = (int)((e / rb) % a.G);
         const long long bj = e / rb / a.G;
         const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
-        const uint8_t *tb = a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes + ksz_bytes(d) +
+        const uint8_t *tb = a.blk + export_slot(a, a.u0 + uu, j) * a.blk_bytes + ksz_bytes(d) +
                             (size_t)(t / TILE) * tile_bytes(d);
         const uint32_t *kw = reinterpret_cast<const uint32_t *>(tb + tile_k_off(d));
         const uint32_t *vw = reinterpret_cast<const uint32_t *>(tb + tile_v_off(d));
@@ -383,8 +410,7 @@ __global__ void k_export(ExportArgs a) {
         const int ch = (int)(e % d);
         const long long bj = e / d;
         const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
-        const uint32_t sz = reinterpret_cast<const uint32_t *>(
-            a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes)[ch];
+        const uint32_t sz = reinterpret_cast<const uint32_t *>(a.blk + export_slot(a, a.u0 + uu, j) * a.blk_bytes)[ch];
         a.ks[e] = (uint16_t)(sz & 0xffffu);
         a.kz[e] = (uint16_t)(sz >> 16);
     }
@@ -393,7 +419,7 @@ __global__ void k_export(ExportArgs a) {
         const int t = (int)((e / NG) % a.G);
         const long long bj = e / NG / a.G;
         const int j = (int)(bj % a.nf), uu = (int)(bj / a.nf);
-        const uint8_t *tb = a.blk + ((size_t)(a.u0 + uu) * a.NB + j) * a.blk_bytes + ksz_bytes(d) +
+        const uint8_t *tb = a.blk + export_slot(a, a.u0 + uu, j) * a.blk_bytes + ksz_bytes(d) +
                             (size_t)(t / TILE) * tile_bytes(d);
         const uint32_t sz = reinterpret_cast<const uint32_t *>(tb + tile_sz_off(d))[vsz_index(t, gm)];
         a.vs[e] = (uint16_t)(sz & 0xffffu);
@@ -442,6 +468,11 @@ FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV,
     a.cmeta = c->cmeta;
     a.bcnt = c->bcnt;
     a.C = c->cold;
+    a.bt = c->paged ? c->bt : nullptr;
+    a.fstack = c->fstack;
+    a.ftop = c->ftop;
+    a.ctl = c->ctl;
+    a.src_u0 = 0;
     a.src_unit_stride = src_unit_stride;
     a.src_mod = src_mod;
     a.t0 = t0;
@@ -482,6 +513,35 @@ cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __ha
     return run_flush(c, flush_args(c, srcK, srcV, src_unit_stride, src_mod, 0, 0), fl, fl.n * c->Hkv, s);
 }
 
+cudaError_t launch_flush_list_src(const ott_cache *c, const __half *srcK, const __half *srcV,
+                                  long long src_unit_stride, long long src_mod, int src_u0, const FlushList &fl,
+                                  cudaStream_t s) {
+    if (fl.n <= 0) return cudaSuccess;
+    FlushArgs a = flush_args(c, srcK, srcV, src_unit_stride, src_mod, 0, 0);
+    a.src_u0 = src_u0;
+    return run_flush(c, a, fl, fl.n * c->Hkv, s);
+}
+
+// Paged pool: the blocks of sequence b's units go back to the free slots.
+__global__ void k_release(int32_t *fstack, int *ftop, const int32_t *bt, int u0, int NB, int nf, int pool,
+                          int *ctl) {
+    const int u = u0 + blockIdx.x;
+    for (int j = threadIdx.x; j < nf; j += blockDim.x) {
+        const int top = atomicAdd(ftop, 1);
+        if (top < pool)
+            fstack[top] = bt[(size_t)u * NB + j];
+        else   // never with the host's count; recorded instead of writing out of bounds
+            atomicExch(ctl + 1, 1);
+    }
+}
+
+cudaError_t launch_release(const ott_cache *c, int b, cudaStream_t s) {
+    const int nf = c->nfb[b];
+    if (!c->paged || nf == 0) return cudaSuccess;
+    k_release<<<c->Hkv, 256, 0, s>>>(c->fstack, c->ftop, c->bt, b * c->Hkv, c->NB, nf, c->pool_blocks, c->ctl);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
     SlotTable st;
     for (int b = 0; b < c->B; ++b) st.slot[b] = (int)(c->Tb[b] % c->ring);
@@ -493,13 +553,13 @@ cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __ha
 }
 
 cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
-                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s) {
+                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s, int src_u0) {
     if (t_begin >= t_end || nu <= 0) return cudaSuccess;
     const long long total = (long long)nu * (t_end - t_begin) * (c->d / 8);
     const int th = 256;
     const long long bl = (total + th - 1) / th;
     k_copy_tail<<<(int)(bl < 65535 ? bl : 65535), th, 0, s>>>(K, V, c->rk, c->rv, u0, nu, c->d, c->ring,
-                                                               Lstride, t_begin, t_end);
+                                                               Lstride, t_begin, t_end, src_u0);
     return cudaGetLastError();
 }
 
@@ -517,6 +577,7 @@ cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *s
     const size_t nblk = (size_t)nu * nf;
     ExportArgs a;
     a.blk = c->blk;
+    a.bt = c->paged ? c->bt : nullptr;
     a.blk_bytes = c->blk_bytes;
     a.NB = c->NB;
     a.nf = nf;

@@ -35,6 +35,8 @@
 // Residual ring: rk, rv [U][G+R][d], token t in slot t mod (G+R).
 // Outlier pool:  pk, pv [U][P][d], pnorm [U][P], pidx [U][P], kept sorted by
 // (norm, token index) ascending; n_pool = min(P, nf*G) for every unit.
+// Paged pool (ott_create_paged): block j of unit u lives at pool slot
+// bt[u][j] instead of u*NB + j.
 // Cold pool (cold-pool policy only): ck, cv [U][C][d], cidx [U][C], a ring
 // used first in, first out, with (count, slot of the oldest) in cmeta [U][2];
 // block sizes then depend on the data and are kept in bcnt [U][NB].
@@ -139,6 +141,15 @@ struct ott_cache {
     int32_t *cidx;          // [U][C]
     int *cmeta;             // [U][2]: tokens in the cold pool, slot of the oldest
     int32_t *bcnt;          // [U][NB] valid tokens of each block
+    // paged block pool (ott_create_paged): the quantized blocks of all units
+    // come from one pool; a flush takes a free slot, a released sequence
+    // returns its slots
+    int paged;
+    int pool_blocks;
+    int32_t *bt;            // [U][NB] pool slot of block j of unit u
+    int32_t *fstack;        // [pool_blocks] free slots
+    int *ftop;              // [1] number of free slots on the stack
+    long long free_blocks;  // host mirror of *ftop
     // Top-K sparse decode (ott_decode_attn_topk)
     int32_t *sel;           // [U][Kc] the blocks selected by the last call
     float *bound;           // [U][NB] scratch: the blocks' score bounds
@@ -174,7 +185,12 @@ cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __ha
 cudaError_t launch_copy_tail(const ott_cache *c, const __half *K, const __half *V, int L,
                              long long t_begin, cudaStream_t s);
 cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
-                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s);
+                                   int Lstride, long long t_begin, long long t_end, cudaStream_t s,
+                                   int src_u0 = 0);
+cudaError_t launch_flush_list_src(const ott_cache *c, const __half *srcK, const __half *srcV,
+                                  long long src_unit_stride, long long src_mod, int src_u0, const FlushList &fl,
+                                  cudaStream_t s);
+cudaError_t launch_release(const ott_cache *c, int b, cudaStream_t s);
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
 cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s);
 cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s);

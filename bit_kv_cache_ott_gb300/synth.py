@@ -49,6 +49,7 @@ class Workload:
     len_lo: int = 0   # > 0: sequence b's prefill length is drawn uniformly from [len_lo, L]
     cold: int = -1    # >= 0: the cold-pool eviction policy with this capacity
     topk: int = 0     # > 0: decode with ott_decode_attn_topk, this many blocks per (sequence, kv head)
+    paged: bool = False   # ragged workloads: the blocks come from one pool (ott_create_paged)
 
     @property
     def g(self) -> int:
@@ -87,6 +88,9 @@ WORKLOADS = {
     # a serving batch whose sequences differ in length (mean ~4096 tokens)
     "batch_b32_ragged": Workload("batch_b32_ragged", B=32, Hq=32, Hkv=32, d=128, L=7168, steps=512,
                                  G=128, R=32, P=32, seed=1005, len_lo=1024),
+    # the ragged serving batch with its blocks drawn from one pool through a block table
+    "batch_b32_paged": Workload("batch_b32_paged", B=32, Hq=32, Hkv=32, d=128, L=7168, steps=512,
+                                G=128, R=32, P=32, seed=1005, len_lo=1024, paged=True),
     # the headline batch under the cold-pool policy with the pages' 32 slots
     # long contexts decoded with Top-K sparse access (1/8 and 1/16 of the blocks)
     "mistral_gqa_g128_topk32": Workload("mistral_gqa_g128_topk32", B=4, Hq=32, Hkv=8, d=128, L=32768,

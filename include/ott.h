@@ -110,6 +110,40 @@ int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P,
 int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C,
                     int max_tokens, ott_cache **out);
 
+/*
+ * As ott_create_ragged, with the quantized blocks of all (sequence, kv head)
+ * units drawn from one pool of pool_blocks blocks (a paged block table)
+ * instead of max_tokens worth of blocks per unit: a serving batch whose
+ * sequences differ in length needs only the blocks its tokens fill. Each
+ * flush takes one free block per flushed unit; ott_release_seq returns a
+ * sequence's blocks. A call whose flushes would need more blocks than are
+ * free returns OTT_ERR_CAPACITY before anything is queued. The decode reads
+ * every block through the table. Not for ott_decode_attn_topk.
+ */
+int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens,
+                     long long pool_blocks, ott_cache **out);
+
+/*
+ * Serving (caches from ott_create_ragged or ott_create_paged): sequence b
+ * finishes. It drops all its tokens and (paged pool) returns its blocks; the
+ * slot must be refilled with ott_prefill_seq before the next ott_append or
+ * decode (which return OTT_ERR_STATE while a sequence is empty). stream: the
+ * stream of the cache's other calls.
+ */
+int ott_release_seq(ott_cache *c, int b, void *stream);
+
+/*
+ * Serving: fill the empty sequence b with a new prompt of L tokens; from then
+ * on it is a fresh sequence of its own (token indices from 0), flushed and
+ * attended as in ott_prefill_lens. K, V: DEVICE fp16 [Hkv][L][d], contiguous.
+ * OTT_ERR_STATE if b holds tokens; OTT_ERR_CAPACITY if L > max_tokens or the
+ * paged pool lacks free blocks.
+ */
+int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, void *stream);
+
+/* Free blocks of a paged pool (host-side count), or -1 for a cache without one. */
+long long ott_free_blocks(const ott_cache *c);
+
 /* Free everything. NULL-safe. Waits for the device to finish. */
 int ott_destroy(ott_cache *c);
 
