@@ -31,18 +31,26 @@
  *   - Decode attends to every token seen, scale 1/sqrt(d); query head h
  *     reads kv head h / (Hq/Hkv). Output fp16 (round to nearest).
  *
+ * Variants, each declared below with its own rules: batches whose sequences
+ * differ in length (ott_create_ragged), a paged block pool with sequences
+ * that finish and are replaced (ott_create_paged, ott_release_seq,
+ * ott_prefill_seq), the cold-pool eviction policy (ott_create_cold), Top-K
+ * sparse decode (ott_decode_attn_topk) and an allocation-free decode
+ * (ott_decode_attn_static).
+ *
  * Conventions for every call:
  *   - Device pointers are CUDA device addresses of fp16 data (IEEE binary16),
  *     contiguous, 16-byte aligned. The caller owns them and keeps them alive
  *     until the work queued on `stream` completes.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream). All
- *     work is queued on it; no call synchronizes except ott_export_state and
- *     ott_check_device.
+ *     work is queued on it; no call synchronizes except the create and
+ *     destroy calls, ott_export_state, ott_export_cold and ott_check_device.
  *   - Arguments and state are checked before anything is queued: a call that
  *     returns an error other than OTT_ERR_CUDA leaves the cache unchanged.
  *     A CUDA error poisons the handle: later calls return OTT_ERR_STATE.
  *   - A handle is not thread-safe. Distinct handles are independent.
- *   - Every sequence of the batch has the same length T.
+ *   - Every sequence of the batch has the same length T, except in the
+ *     ragged and paged variants.
  */
 #ifndef OTT_H
 #define OTT_H
