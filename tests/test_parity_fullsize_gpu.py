@@ -68,6 +68,14 @@ def test_batch_b32_headline(oracle_mod, ott):
     run_fullsize(oracle_mod, ott, "batch_b32", 300, {0, 31, 32, 160, 299}, heads=12, unit_limit=48)
 
 
+@pytest.mark.parametrize("name", ["batch_b1", "batch_b8", "batch_b16"])
+def test_batch_sweep(oracle_mod, ott, name):
+    """The rest of the batch sweep (B = 1, 8, 16; B = 32 is the headline
+    test): 140 steps across the flush after step 31, state at every flush,
+    sampled outputs before and after it."""
+    run_fullsize(oracle_mod, ott, name, 140, {0, 31, 32, 139}, heads=10, unit_limit=40)
+
+
 @pytest.mark.parametrize("name", ["mistral_gqa_g128", "mistral_gqa_g256"])
 def test_mistral_gqa(oracle_mod, ott, name):
     run_fullsize(oracle_mod, ott, name, 256, {0, 63, 64, 200, 255}, heads=10)
