@@ -281,6 +281,12 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T = L;
     c->nf = nf;
+    if (c->paged) {   // blocks are read through the table: per-sequence counts from now on
+        c->Tb.assign(c->B, L);
+        c->nfb.assign(c->B, nf);
+        c->ragged = 1;
+        c->nf = 0;
+    }
     return OTT_OK;
 }
 

@@ -126,7 +126,9 @@ int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C,
  * flush takes one free block per flushed unit; ott_release_seq returns a
  * sequence's blocks. A call whose flushes would need more blocks than are
  * free returns OTT_ERR_CAPACITY before anything is queued. The decode reads
- * every block through the table. Not for ott_decode_attn_topk.
+ * every block through the table, so the cache keeps per-sequence counts even
+ * after ott_prefill (ott_get_counts then reports sequence 0). Not for
+ * ott_decode_attn_topk.
  */
 int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens,
                      long long pool_blocks, ott_cache **out);

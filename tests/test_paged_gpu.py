@@ -150,3 +150,32 @@ def test_paged_argument_errors(ott):
             plain.release_seq(0)           # not created for per-sequence lengths
         assert ei.value.code == ott.OTT_ERR_STATE
         assert plain.free_blocks() == -1
+
+
+@pytest.mark.parametrize("paged", [True, False])
+def test_release_after_a_uniform_prefill(oracle_mod, ott, paged):
+    """A cache filled by ott_prefill (one length for all) switches to
+    per-sequence counts at its first release; it then serves like the others."""
+    B, Hq, Hkv, d, G, R, P, L, steps = 3, 6, 3, 128, 16, 2, 4, 70, 24
+    K, V = _gen(21, B, Hkv, L + steps, d)
+    kk, vv = _gen(22, 1, Hkv, 45, d)
+    q_all = torch.randn(steps, B, Hq, d, generator=torch.Generator().manual_seed(23)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    orc.prefill(K[:, :, :L].contiguous(), V[:, :, :L].contiguous())
+    dev = torch.device("cuda")
+    kw = dict(pool_blocks=_blocks([L + steps] * B, G, R, Hkv) + 1) if paged else dict(ragged=True)
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=L + steps + 1, **kw) as c:
+        c.prefill(K[:, :, :L].contiguous().to(dev), V[:, :, :L].contiguous().to(dev))
+        for s in range(steps):
+            if s == 9:
+                c.release_seq(2)
+                orc.release_seq(2)
+                c.prefill_seq(2, kk[0].contiguous().to(dev), vv[0].contiguous().to(dev))
+                orc.prefill_seq(2, kk[0].contiguous(), vv[0].contiguous())
+            compare_out(c.decode_attn(q_all[s].to(dev)), orc.decode(q_all[s]), f"step {s}")
+            k, v = K[:, :, L + s].contiguous(), V[:, :, L + s].contiguous()
+            c.append(k.to(dev), v.to(dev))
+            orc.append(k, v)
+        for b in range(B):
+            _compare_seq(c, orc, b, Hkv)
+        c.check_device()
