@@ -411,8 +411,8 @@ def run_ours(args, w):
         dec_bytes = sum(metrics.hot_bytes(ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
                         + cold_q0[li] + (cold_q1[li] - cold_q0[li]) * f / nfl
                         for ts, f in step_log for li in range(w.layers))
-    # append + decode + combine (+ the Top-K selection), plus flushes
-    launches = K_steps * w.layers * (4 if w.topk > 0 else 3) + flushes
+    # append + decode + combine (+ the Top-K bounds and pick), plus flushes
+    launches = K_steps * w.layers * (5 if w.topk > 0 else 3) + flushes
     ms = max_over_ranks(ms, dev)
     for c in caches:
         c.check_device()
@@ -518,7 +518,7 @@ def run_ours(args, w):
             "cache_bytes": cache_bytes, "fp16_cache_bytes": fp16_bytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
-                         "kernel": ("k_topk_select + k_decode + k_combine (ott_decode_attn_topk)" if w.topk > 0
+                         "kernel": ("k_topk_bounds + k_topk_pick + k_decode + k_combine (ott_decode_attn_topk)" if w.topk > 0
                                     else "k_decode + k_combine (ott_decode_attn)"),
                          "algorithmic_bytes_per_launch": dec_bytes / n_launch,
                          "traffic": recorded_traffic(w.name)},
