@@ -129,3 +129,24 @@ def test_cold_changes_nothing_without_evictions(oracle_mod):
     assert eb["ncold"] == 0
     q = torch.randn(1, 1, d, generator=torch.Generator().manual_seed(0)).half()
     assert np.array_equal(a.decode(q), b.decode(q))
+
+
+def test_cold_golden_hand_worked(oracle_mod):
+    """tests/golden/cold_pool_tiny.json: membership worked out by hand."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "cold_pool_tiny.json")))
+    sh = g["shape"]
+    d = sh["d"]
+    K = np.stack([np.full(d, a, np.float16) for a in g["inputs"]["key_level"]])
+    V = np.zeros_like(K)
+    orc = oracle_mod.OracleCache(1, 1, 1, d, sh["G"], sh["R"], sh["P"], cold=sh["C"])
+    for t in range(len(K)):
+        orc.append(K[t][None, None], V[t][None, None])
+    e = orc.export_unit(0)
+    ex = g["expect"]
+    blocks = [e["bidx"][j][: e["bcount"][j]].tolist() for j in range(e["nf"])]
+    assert blocks == ex["blocks"]
+    assert [x for x in e["pidx"].tolist() if x >= 0] == ex["pool"]
+    assert e["cidx"][: e["ncold"]].tolist() == ex["cold"]
+    assert e["tail"] == len(ex["tail"])

@@ -175,3 +175,29 @@ def test_topk_with_the_cold_pool(oracle_mod):
     vals = np.concatenate([e["tv"], e["pv"][: e["npool"]], e["cv"][: e["ncold"]]]).view(np.float16).astype(np.float64)
     for h in range(Hq):
         assert np.allclose(out[0, h], _attend(q[0, h].double().numpy(), keys, vals), rtol=1e-10, atol=1e-12)
+
+
+def test_topk_golden_hand_worked(oracle_mod):
+    """tests/golden/topk_tiny.json: bounds and selections worked out by hand."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "topk_tiny.json")))
+    sh = g["shape"]
+    d = sh["d"]
+    rows = []
+    for lo, hi in g["inputs"]["block_levels"]:
+        rows += [np.full(d, lo, np.float16), np.full(d, hi, np.float16)]
+    K = np.stack(rows)
+    V = np.zeros_like(K)
+    orc = oracle_mod.OracleCache(1, 1, 1, d, sh["G"], sh["R"], sh["P"])
+    for t in range(len(K)):
+        orc.append(K[t][None, None], V[t][None, None])
+    for name, sign in (("q_plus", 1.0), ("q_minus", -1.0)):
+        q = np.full((1, 1, d), sign, np.float16)
+        ex = g["expect"][name]
+        sel, bounds = orc.topk_select(q, 2)
+        assert bounds[0].tolist() == ex["bounds"], name
+        assert sel[0].tolist() == ex["top2"], name
+        if "top3" in ex:
+            sel3, _ = orc.topk_select(q, 3)
+            assert sel3[0].tolist() == ex["top3"], name
