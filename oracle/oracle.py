@@ -215,15 +215,17 @@ class OracleCache:
         -1 padded; bounds float32 [B*Hkv][nf], -inf for empty blocks)."""
         qb = _bits(q)
         U = self.B * self.Hkv
-        nf = self.counts(0)[1]
+        nf = max(self.counts(u)[1] for u in range(U))   # units may differ (ragged batches)
         sel = np.full((U, max(K, 1)), -1, np.int32)
-        bounds = np.zeros((U, max(nf, 1)), np.float32)
+        bounds = np.full((U, max(nf, 1)), -np.inf, np.float32)
         for u in range(U):
             b, hk = divmod(u, self.Hkv)
             row = np.zeros(max(nf, 1), np.int32)
             qrow = np.ascontiguousarray(qb[b])
-            m = lib().orc_topk_select(self._h, b, hk, _ptr(qrow), int(K), _ptr(row), _ptr(bounds[u]))
+            brow = np.full(max(nf, 1), -np.inf, np.float32)
+            m = lib().orc_topk_select(self._h, b, hk, _ptr(qrow), int(K), _ptr(row), _ptr(brow))
             sel[u, :m] = row[:m]
+            bounds[u] = brow
         return sel[:, :K], bounds[:, :nf]
 
     def decode_head(self, b, hq, qv) -> np.ndarray:
