@@ -193,13 +193,15 @@ class OTTCache:
                          sel: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """Top-K sparse decode: each (sequence, kv head) attends its K blocks
         with the largest score bound plus all fp16 tokens. ``sel``, if given,
-        is a CUDA int32 tensor [B*Hkv][min(K, nf)] that receives the blocks."""
+        is a CUDA int32 tensor [B*Hkv][min(K, nf)] that receives the blocks
+        (nf: the largest block count of any sequence)."""
         shp = (self.B, self.Hq, self.d)
         if out is None:
             out = torch.empty(shp, dtype=torch.float16, device=q.device)
         sp = None
         if sel is not None:
-            kc = min(int(K), self.counts()[1])
+            nf = max(self.seq_counts(b)[1] for b in range(self.B)) if self.ragged else self.counts()[1]
+            kc = min(int(K), nf)
             if (not sel.is_cuda or sel.dtype != torch.int32 or not sel.is_contiguous()
                     or tuple(sel.shape) != (self.B * self.Hkv, kc)):
                 raise ValueError(f"sel: expected a contiguous CUDA int32 tensor {(self.B * self.Hkv, kc)}")

@@ -399,11 +399,14 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
 
 int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t *sel, void *stream) {
     if (!c) return OTT_ERR_INVALID;
-    if (c->poisoned || c->T < 1 || c->ragged || c->paged) return OTT_ERR_STATE;
+    if (c->poisoned || c->T < 1 || some_sequence_empty(c)) return OTT_ERR_STATE;
     if (K < 1 || !c->topk_ok || !q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *qh = static_cast<const __half *>(q);
-    const int Kc = K < c->nf ? K : c->nf;
+    int nf_max = c->nf;
+    if (c->ragged)
+        for (int b = 0; b < c->B; ++b) nf_max = c->nfb[b] > nf_max ? c->nfb[b] : nf_max;
+    const int Kc = K < nf_max ? K : nf_max;
     cudaError_t e = cudaSuccess;
     if (Kc > 0) e = launch_topk_select(c, qh, K, Kc, s);
     if (e == cudaSuccess) e = launch_decode_topk(c, qh, static_cast<__half *>(out), Kc, s);

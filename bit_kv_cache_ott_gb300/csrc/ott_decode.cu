@@ -1058,7 +1058,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     if constexpr (RG) {
         long long base = 0;
         for (int b = 0; b < c->B; ++b) {
-            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], c->nfb[b]);
+            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b]);
             st.e[b].base = base;
             base += (long long)c->Hkv * st.e[b].Iu;
         }
@@ -1113,6 +1113,7 @@ cudaError_t set_decode_attr(int smem_max) {
         reinterpret_cast<const void *>(k_decode<D, GQ, true, false, false>),
         reinterpret_cast<const void *>(k_decode<D, GQ, false, false, true>),
         reinterpret_cast<const void *>(k_decode<D, GQ, false, true, true>),
+        reinterpret_cast<const void *>(k_decode<D, GQ, true, false, true>),
     };
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
@@ -1130,6 +1131,7 @@ cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, 
 
 template <int D, int GQ>
 cudaError_t launch_decode_topk_t(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s) {
+    if (c->ragged) return launch_decode_t<D, GQ, true, false, true>(c, q, out, c->part, s, Kc);
     return c->cold >= 0 ? launch_decode_t<D, GQ, false, true, true>(c, q, out, c->part, s, Kc)
                         : launch_decode_t<D, GQ, false, false, true>(c, q, out, c->part, s, Kc);
 }

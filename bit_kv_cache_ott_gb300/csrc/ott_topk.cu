@@ -47,10 +47,21 @@ struct TopkArgs {
     int Kc;                  // slots per unit in sel: min(K, nf)
     float *bound;            // [U][NB] scratch: block bounds
     int32_t *sel;            // [U][Kc]
+    const int32_t *bt;       // paged pool: slot of each block (null: u*NB + j)
+    int ragged;              // 1: sequence b has nfb.nf[b] blocks (else nf for all)
 };
 
+// Blocks of each sequence of a ragged batch (a kernel parameter).
+struct NfTable {
+    int nf[RAGGED_MAX];
+};
+
+__device__ __forceinline__ int unit_nf(const TopkArgs &a, const NfTable &t, int u) {
+    return a.ragged ? t.nf[u / a.Hkv] : a.nf;
+}
+
 template <int D, int GQ>
-__global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a) {
+__global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a, const __grid_constant__ NfTable nt) {
     constexpr int RW = D + 1;                    // padded row (words)
     constexpr int V4 = D / 4;                    // 16-byte pieces per header
     constexpr int PER = BND_BLOCKS * V4 / BND_THREADS;
@@ -62,16 +73,21 @@ __global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a) {
     // the sort may be scheduled now; it waits for these bounds
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int u = blockIdx.y, j0 = blockIdx.x * BND_BLOCKS, tid = threadIdx.x, nth = blockDim.x;
-    const int nb = min(BND_BLOCKS, a.nf - j0);
+    const int nf_u = unit_nf(a, nt, u);
+    if (j0 >= nf_u) return;   // the whole CTA: this unit has fewer blocks
+    const int nb = min(BND_BLOCKS, nf_u - j0);
     const int b = u / a.Hkv, hk = u % a.Hkv;
     const __half *qp = a.q + ((size_t)b * a.Hq + hk * GQ) * D;
     for (int e = tid; e < GQ * D; e += nth) qs[e] = __half2float(qp[e]);
-    const uint8_t *base = a.blk + ((size_t)u * a.NB + j0) * a.blk_bytes;
     uint4 buf[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int e = tid + i * BND_THREADS, r = e / V4, v = e % V4;
-        if (r < nb) buf[i] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)r * a.blk_bytes) + v);
+        if (r < nb) {
+            const size_t own = (size_t)u * a.NB + j0 + r;
+            const size_t slot = a.bt ? (size_t)__ldg(a.bt + own) : own;
+            buf[i] = __ldg(reinterpret_cast<const uint4 *>(a.blk + slot * a.blk_bytes) + v);
+        }
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -158,14 +174,14 @@ __device__ __forceinline__ int block_exscan(int v, int *ws, int &total) {
 // ascending block order.
 constexpr uint32_t EMPTY = 0xffffffffu;           // key of an empty block
 
-__global__ void __launch_bounds__(SORT_THREADS) k_topk_pick(TopkArgs a) {
+__global__ void __launch_bounds__(SORT_THREADS) k_topk_pick(TopkArgs a, const __grid_constant__ NfTable nt) {
     extern __shared__ uint32_t key[];              // [nf]
     __shared__ int hist[256];
     __shared__ int ws[32];
     __shared__ int s_digit, s_below;
     // the decode may be scheduled now; it waits for the selection
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x, n = a.nf;
+    const int u = blockIdx.x, tid = threadIdx.x, nth = blockDim.x, n = unit_nf(a, nt, u);
     const float *bd = a.bound + (size_t)u * a.NB;
     // a contiguous chunk of blocks per thread, so that prefix counts follow block order
     const int chunk = (n + nth - 1) / nth, jb = min(n, tid * chunk), je = min(n, jb + chunk);
@@ -257,10 +273,21 @@ int topk_smem_bytes(int d, int gq, int nf) {
 
 cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s) {
     TopkArgs a;
+    NfTable nt;
+    int nf_max = c->nf;
+    a.ragged = c->ragged;
+    if (c->ragged) {
+        nf_max = 0;
+        for (int b = 0; b < c->B; ++b) {
+            nt.nf[b] = c->nfb[b];
+            nf_max = c->nfb[b] > nf_max ? c->nfb[b] : nf_max;
+        }
+    }
+    a.bt = c->paged ? c->bt : nullptr;
     a.blk = c->blk;
     a.blk_bytes = c->blk_bytes;
     a.NB = c->NB;
-    a.nf = c->nf;
+    a.nf = nf_max;
     a.G = c->G;
     a.P = c->P;
     a.jfull = (c->P + c->G - 1) / c->G;
@@ -272,11 +299,11 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     a.Kc = Kc;
     a.bound = c->bound;
     a.sel = c->sel;
-    const dim3 grid((unsigned)((c->nf + BND_BLOCKS - 1) / BND_BLOCKS), (unsigned)c->U);
+    const dim3 grid((unsigned)((nf_max + BND_BLOCKS - 1) / BND_BLOCKS), (unsigned)c->U);
     bool found = false;
 #define OTT_BND(D_, G_)                                                       \
     if (c->d == D_ && c->gq == G_) {                                          \
-        k_topk_bounds<D_, G_><<<grid, BND_THREADS, 0, s>>>(a);                \
+        k_topk_bounds<D_, G_><<<grid, BND_THREADS, 0, s>>>(a, nt);            \
         found = true;                                                         \
     }
     OTT_BND(128, 1) OTT_BND(128, 2) OTT_BND(128, 4) OTT_BND(64, 1) OTT_BND(64, 2) OTT_BND(64, 4)
@@ -285,19 +312,19 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // whole warps, up to SORT_THREADS, about two blocks per thread
-    int th = ((c->nf + 1) / 2 + 31) / 32 * 32;
+    int th = ((nf_max + 1) / 2 + 31) / 32 * 32;
     th = th < 32 ? 32 : (th > SORT_THREADS ? SORT_THREADS : th);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)c->U);
     cfg.blockDim = dim3((unsigned)th);
-    cfg.dynamicSmemBytes = (size_t)topk_smem_bytes(c->d, c->gq, c->nf);
+    cfg.dynamicSmemBytes = (size_t)topk_smem_bytes(c->d, c->gq, nf_max);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_topk_pick, a);
+    return cudaLaunchKernelEx(&cfg, k_topk_pick, a, nt);
 }
 
 cudaError_t set_topk_attributes(int d, int gq, int smem_max) {

@@ -127,8 +127,7 @@ int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C,
  * sequence's blocks. A call whose flushes would need more blocks than are
  * free returns OTT_ERR_CAPACITY before anything is queued. The decode reads
  * every block through the table, so the cache keeps per-sequence counts even
- * after ott_prefill (ott_get_counts then reports sequence 0). Not for
- * ott_decode_attn_topk.
+ * after ott_prefill (ott_get_counts then reports sequence 0).
  */
 int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens,
                      long long pool_blocks, ott_cache **out);
@@ -234,9 +233,10 @@ int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream)
  * block's 4d-byte scale/zero header, so with K well below the block count
  * the call reads far fewer bytes than ott_decode_attn.
  * K >= 1 (K >= the block count attends every block). sel: NULL, or a DEVICE
- * int32 [B*Hkv][min(K, nf)] that receives the selected block indices of each
- * unit in ascending order (-1 where fewer blocks are non-empty), written on
- * the stream. Not for a cache after ott_prefill_lens (OTT_ERR_STATE).
+ * int32 [B*Hkv][min(K, nf)] (nf: the largest block count of any sequence)
+ * that receives the selected block indices of each unit in ascending order
+ * (-1 where a unit has fewer non-empty blocks), written on the stream. Works
+ * on ragged and paged batches: each unit selects among its own blocks.
  * OTT_ERR_INVALID also if the selection's shared memory (about 8 bytes per
  * block slot) does not fit for this max_tokens.
  */

@@ -141,9 +141,6 @@ def test_paged_argument_errors(ott):
         with pytest.raises(ott.OTTError) as ei:
             c.prefill_seq(0, K[0].contiguous(), K[0].contiguous())   # sequence 0 is not empty
         assert ei.value.code == ott.OTT_ERR_STATE
-        with pytest.raises(ott.OTTError) as ei:
-            c.decode_attn_topk(torch.zeros(2, 1, 128, device=dev, dtype=torch.float16), 1)
-        assert ei.value.code == ott.OTT_ERR_STATE
     with ott.OTTCache(2, 1, 1, 128, 16, 2, 4, max_tokens=64) as plain:
         plain.prefill(K, K.clone())
         with pytest.raises(ott.OTTError) as ei:

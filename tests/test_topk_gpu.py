@@ -33,7 +33,7 @@ def _gen(seed, B, Hkv, T, d, falling=False):
 
 def _check(c, orc, q, Kb, where):
     dev = torch.device("cuda")
-    nf = c.counts()[1]
+    nf = max(c.seq_counts(b)[1] for b in range(c.B)) if c.ragged else c.counts()[1]
     kc = min(Kb, nf)
     sel = torch.full((c.B * c.Hkv, kc), -7, dtype=torch.int32, device=dev)
     out = c.decode_attn_topk(q.to(dev), Kb, sel=sel if kc > 0 else None)
@@ -113,8 +113,9 @@ def test_topk_argument_errors(ott):
                                           C.c_void_p(out.data_ptr()), Kb, None, st) == ott.OTT_ERR_INVALID
     with ott.OTTCache(2, 1, 1, 128, 16, 2, 4, max_tokens=64, ragged=True) as r:
         r.prefill_lens(K, K.clone(), [20, 40])
+        r.release_seq(0)
         with pytest.raises(ott.OTTError) as ei:
-            r.decode_attn_topk(q, 2)
+            r.decode_attn_topk(q, 2)              # a released sequence must be refilled first
         assert ei.value.code == ott.OTT_ERR_STATE
 
 
@@ -136,4 +137,35 @@ def test_topk_fullsize(oracle_mod, ott, name, Kb):
             orc.append(k, v)
             if s in (0, 33, 39):
                 _check(c, orc, q, Kb, f"{name} step {s}")
+        c.check_device()
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_topk_ragged_and_paged(oracle_mod, ott, paged):
+    """Sequences of different lengths (and, paged, blocks from one pool):
+    each unit selects among its own blocks; selection bit-exact, outputs
+    within tolerance, through flushes, a release and a refill."""
+    from tests.test_ragged_gpu import _gen as _rgen
+    B, Hq, Hkv, d, G, R, P = 4, 8, 2, 128, 16, 3, 5
+    lens, steps, Kb = [300, 40, 170, 95], 30, 4
+    Lmax = max(lens)
+    K, V = _rgen(31, B, Hkv, Lmax + steps, d)
+    kk, vv = _rgen(32, 1, Hkv, 120, d)
+    q_all = torch.randn(steps, B, Hq, d, generator=torch.Generator().manual_seed(33)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    orc.prefill_lens(K[:, :, :Lmax].contiguous(), V[:, :, :Lmax].contiguous(), lens)
+    dev = torch.device("cuda")
+    kw = dict(pool_blocks=2 * (Lmax + steps) // G * B * Hkv) if paged else dict(ragged=True)
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=Lmax + steps + 1, **kw) as c:
+        c.prefill_lens(K[:, :, :Lmax].contiguous().to(dev), V[:, :, :Lmax].contiguous().to(dev), lens)
+        for s in range(steps):
+            if s == 12:
+                c.release_seq(1)
+                orc.release_seq(1)
+                c.prefill_seq(1, kk[0].contiguous().to(dev), vv[0].contiguous().to(dev))
+                orc.prefill_seq(1, kk[0].contiguous(), vv[0].contiguous())
+            _check(c, orc, q_all[s], Kb, f"step {s}")
+            k, v = K[:, :, Lmax + s].contiguous(), V[:, :, Lmax + s].contiguous()
+            c.append(k.to(dev), v.to(dev))
+            orc.append(k, v)
         c.check_device()
