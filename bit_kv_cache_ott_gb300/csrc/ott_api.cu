@@ -41,9 +41,10 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
 // for j in [nf_from[b], nf_to[b])) need. 0 for a cache without the pool.
 long long blocks_needed(const ott_cache *c, long long n_unit_flushes) { return c->paged ? n_unit_flushes : 0; }
 
-// Ragged caches: every sequence must hold a token for appends and decodes.
+// Ragged caches: every sequence must hold a token for appends and decodes
+// (except at the very start, T = 0, when all sequences grow together).
 bool some_sequence_empty(const ott_cache *c) {
-    if (!c->ragged) return false;
+    if (!c->ragged || c->T == 0) return false;
     for (int b = 0; b < c->B; ++b)
         if (c->Tb[b] == 0) return true;
     return false;
@@ -371,6 +372,12 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
     if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
     if (some_sequence_empty(c)) return OTT_ERR_STATE;
+    if (c->paged && !c->ragged) {   // blocks are read through the table: per-sequence counts
+        c->Tb.assign(c->B, c->T);
+        c->nfb.assign(c->B, c->nf);
+        c->ragged = 1;
+        c->nf = 0;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (c->ragged)
         return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);

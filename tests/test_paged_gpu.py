@@ -176,3 +176,23 @@ def test_release_after_a_uniform_prefill(oracle_mod, ott, paged):
         for b in range(B):
             _compare_seq(c, orc, b, Hkv)
         c.check_device()
+
+
+def test_paged_cache_filled_by_appends(oracle_mod, ott):
+    """No prefill: every token arrives through ott_append, from an empty cache."""
+    B, Hq, Hkv, d, G, R, P, T = 2, 4, 2, 128, 16, 3, 5, 90
+    K, V = _gen(41, B, Hkv, T, d)
+    q = torch.randn(B, Hq, d, generator=torch.Generator().manual_seed(42)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    dev = torch.device("cuda")
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=T + 1, pool_blocks=_blocks([T] * B, G, R, Hkv)) as c:
+        for t in range(T):
+            k, v = K[:, :, t].contiguous(), V[:, :, t].contiguous()
+            c.append(k.to(dev), v.to(dev))
+            orc.append(k, v)
+            if t % 23 == 0 or t == T - 1:
+                compare_out(c.decode_attn(q.to(dev)), orc.decode(q), f"T={t + 1}")
+        assert c.free_blocks() == 0
+        for b in range(B):
+            _compare_seq(c, orc, b, Hkv)
+        c.check_device()
