@@ -196,3 +196,22 @@ def test_paged_cache_filled_by_appends(oracle_mod, ott):
         for b in range(B):
             _compare_seq(c, orc, b, Hkv)
         c.check_device()
+
+
+def test_paged_static_decode_matches(ott):
+    """The allocation-free entry point reads the pool through the table too."""
+    B, Hq, Hkv, d, G, R, P = 3, 4, 2, 128, 16, 3, 5
+    lens = [40, 97, 18]
+    K, V = _gen(51, B, Hkv, max(lens), d)
+    dev = torch.device("cuda")
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=128, pool_blocks=_blocks(lens, G, R, Hkv) + 2) as c:
+        c.prefill_lens(K.contiguous().to(dev), V.contiguous().to(dev), lens)
+        q = torch.randn(B, Hq, d, generator=torch.Generator().manual_seed(5)).half().to(dev)
+        ref = c.decode_attn(q)
+        out = torch.full_like(ref, float("nan"))
+        rc = ott.load().ott_decode_attn_static(C.c_void_p(c.handle), C.c_void_p(q.data_ptr()),
+                                               C.c_void_p(out.data_ptr()),
+                                               C.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == ott.OTT_OK
+        torch.cuda.synchronize()
+        assert float((out.float() - ref.float()).abs().max()) <= 2e-3
