@@ -260,6 +260,12 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 // ---------------------------------------------------------------- quantized segment
 // Blocks [j0, j1) of unit u (Top-K: the blocks listed at positions [j0, j1)
 // of the unit's selection); the partial goes to part[slot].
+//
+// The chunks of the segment (up to CHUNK_TILES tiles of one block each) are
+// walked by two cursors: one issues the bulk copies two chunks ahead, the
+// other consumes them. A chunk whose tiles are all full (the common case:
+// every block after the pool fills holds G tokens) runs a body without any
+// masking; the ragged last chunk of a short block takes the masked body.
 template <int D, int GQ, bool CO, bool TK, bool RG>
 __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
@@ -267,52 +273,81 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     using C = Cfg<D, GQ>;
     constexpr int NKT = C::NKT, NW = C::NW, NG = C::NG, GPV = C::GPV, NV = C::NV;
     constexpr int KSZ = ksz_bytes(D), TB = tile_bytes(D);
+    constexpr int CT = CHUNK_TILES * TILE;   // token slots per chunk
     const int r = lane >> 2, i = lane & 3;
 
-    // position j -> block index; a position without a block holds no token
-    auto blk_of = [&](int j) -> int {
-        if constexpr (TK) return __ldg(a.sel + (size_t)u * a.Ksel + j);
-        return j;
-    };
-    auto cnt_of = [&](int j) -> int {
+    // tokens of the block at position j of the segment (0: no block there)
+    auto cnt_at = [&](int j) -> int {
         if constexpr (TK) {
-            const int bj = blk_of(j);
+            const int bj = __ldg(a.sel + (size_t)u * a.Ksel + j);
             return bj < 0 ? 0 : block_cnt<CO>(a, u, bj);
         }
         return block_cnt<CO>(a, u, j);
     };
-    auto active = [&](int j, int k) { return 16 * CHUNK_TILES * k < cnt_of(j); };
-    int lj = j0, lk = 0;
-    while (lj < j1 && !active(lj, lk)) { ++lj; lk = 0; }
-    int cj_ = lj, ck_ = lk;   // next chunk to consume
-    auto issue = [&](int j, int k, int st) {
+    // chunk cursor: position j, chunk k of that block, the block's tokens
+    struct Cursor {
+        int j, k, cnt;
+    };
+    auto skip_empty = [&](Cursor &c) {
+        while (c.j < j1 && c.cnt == 0) {
+            ++c.j;
+            c.cnt = c.j < j1 ? cnt_at(c.j) : 0;
+        }
+    };
+    auto advance = [&](Cursor &c) {
+        ++c.k;
+        if (CT * c.k >= c.cnt) {
+            c.k = 0;
+            ++c.j;
+            c.cnt = c.j < j1 ? cnt_at(c.j) : 0;
+            skip_empty(c);
+        }
+    };
+    auto issue = [&](const Cursor &c, int st) {
         if (lane == 0) {
-            const int vt = (cnt_of(j) + TILE - 1) / TILE;
-            const int t0 = k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
-            size_t bslot = (size_t)u * a.NB + blk_of(j);
+            const int vt = (c.cnt + TILE - 1) / TILE;
+            const int t0 = c.k * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
+            int bj = c.j;
+            if constexpr (TK) bj = __ldg(a.sel + (size_t)u * a.Ksel + c.j);
+            size_t bslot = (size_t)u * a.NB + bj;
             if constexpr (RG) {
                 if (a.bt) bslot = (size_t)__ldg(a.bt + bslot);
             }
             const uint8_t *bsrc = a.blk + bslot * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
-            if (k == 0)
+            if (c.k == 0)
                 bulk_load(dst, bsrc, (uint32_t)(KSZ + nt * TB), &bars[st]);
             else
                 bulk_load(dst + KSZ, bsrc + KSZ + (size_t)t0 * TB, (uint32_t)(nt * TB), &bars[st]);
         }
     };
-    auto next = [&](int &j, int &k) {
-        ++k;
-        while (j < j1 && !active(j, k)) { ++j; k = 0; }
-    };
     // start the copies first, then stage the queries while they fly
+    Cursor ic{j0, 0, j0 < j1 ? cnt_at(j0) : 0};
+    skip_empty(ic);
+    Cursor cc = ic;
     int st_issue = 0;
-    for (int n = 0; n < 2 && lj < j1; ++n) {
-        issue(lj, lk, st_issue);
+    for (int n = 0; n < 2 && ic.j < j1; ++n) {
+        issue(ic, st_issue);
         st_issue ^= 1;
-        next(lj, lk);
+        advance(ic);
     }
     load_queries<D, GQ>(a, u, qsm, lane);
+
+    // Cooperative per-block constants: lane L handles channel pairs
+    // (2L + 64m, 2L + 64m + 1); the channels' class scales stay in registers
+    // for the whole segment.
+    constexpr int NPAIR = D / 64;
+    float clsf[NPAIR];
+    if constexpr (C::COOP) {
+#pragma unroll
+        for (int m = 0; m < NPAIR; ++m) {
+            const int ch = 2 * lane + 64 * m;
+            // a channel's slot q = o*NKT + kt (o = bit 3, kt = ch / 16) fixes
+            // its class; ch and ch + 1 share the slot
+            const int q0 = ((ch >> 3) & 1) * NKT + (ch >> 4);
+            clsf[m] = pow2i(-2 * cls_of_pos(q0 & 7));
+        }
+    }
 
     float acc[NKT][4];
 #pragma unroll
@@ -330,19 +365,32 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     float zs[NZ];
 #pragma unroll
     for (int v = 0; v < NZ; ++v) zs[v] = 0.0f;
-    float m_run = -CUDART_INF_F, l_run = 0.0f;   // head i
+    // running max and sum of the head this lane's score columns hold
+    float m_run = -CUDART_INF_F, l_run = 0.0f;
     uint32_t Bk[NKT][2];
     float c1 = 0.0f, c0 = 0.0f;
 
-    const int hB = r >> 1;               // score-MMA B column of this lane: head r/2,
-    const bool piece = (r & 1) != 0;     // piece r&1 (hi or lo)
+    // Score-MMA B column of this lane: head (r/2) mod GQ, piece r&1 (hi or
+    // lo). With fewer than four heads the heads repeat across the columns, so
+    // that every lane's score columns hold a real head: lane i scores head
+    // i mod GQ.
+    const int hB = (r >> 1) % GQ;
+    const bool piece = (r & 1) != 0;
     const float pm = piece ? 1.0f : 0.0f;
+    const int hS = i % GQ;
     // PV B column of this lane: head hV, value-group offset glow, piece
     const int hV = (r >> 1) / GPV, glow = (r >> 1) % GPV;
     const int src0 = 4 * (2 * i) + hV, src1 = 4 * (2 * i + 1) + hV;
+    const bool lo_lane = (r & 1) != 0;
+    // One B variant (GQ <= 2): lane (r, i) holds the weights of tokens r and
+    // r+8 of head i mod GQ; lanes i with odd i / GQ send the second, so that a
+    // hi lane gathers tokens 2i, 2i+1 of head hV and a lo lane tokens 2i+8,
+    // 2i+9 with two shuffles
+    const int srcA = 4 * (2 * i) + hV + (lo_lane ? GQ : 0), srcB = srcA + 4;
+    const bool send_second = ((i / GQ) & 1) != 0;
 
     int st = 0;
-    while (cj_ < j1) {
+    while (cc.j < j1) {
         uint8_t *stage = st ? stg1 : stg0;
         if (!mbar_wait(&bars[st], (phase >> st) & 1u)) {
             if (lane == 0) atomicExch(&a.ctl[1], 1);
@@ -351,29 +399,31 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
             return false;
         }
         phase ^= 1u << st;
-        const int cj = cnt_of(cj_), vt = (cj + TILE - 1) / TILE;
-        const int t0 = ck_ * CHUNK_TILES, nt = min(CHUNK_TILES, vt - t0);
+        const int cj = cc.cnt;
+        const int t0 = cc.k * CHUNK_TILES;
 
-        if (ck_ == 0) {
+        if (cc.k == 0) {
             // per-block constants: B = q*s split in hi/lo at a per-block
             // exponent E and a per-channel class scale; qz = q.z
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(stage);
             int Eh[GQ];
             float qzh[GQ];
             if constexpr (C::COOP) {
-                // each lane: channels lane + 32m of every head, staged as hi/lo rows
-                float xs[GQ][D / 32];
+                float2 xs[GQ][NPAIR];
 #pragma unroll
                 for (int h = 0; h < GQ; ++h) {
                     float amax = 0.0f, qz = 0.0f;
 #pragma unroll
-                    for (int m = 0; m < D / 32; ++m) {
-                        const int ch = lane + 32 * m;
-                        const float2 sz = __half22float2(*reinterpret_cast<const __half2 *>(ksz + ch));
-                        const float qv = qsm[h * D + ch];
-                        xs[h][m] = qv * sz.x;
-                        qz = fmaf(qv, sz.y, qz);
-                        amax = fmaxf(amax, fabsf(xs[h][m]));
+                    for (int m = 0; m < NPAIR; ++m) {
+                        const uint2 sz2 = *reinterpret_cast<const uint2 *>(ksz + 2 * lane + 64 * m);
+                        const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.x));
+                        const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.y));
+                        const float2 qv = *reinterpret_cast<const float2 *>(qsm + h * D + 2 * lane + 64 * m);
+                        xs[h][m].x = qv.x * e0.x;
+                        xs[h][m].y = qv.y * e1.x;
+                        qz = fmaf(qv.x, e0.y, qz);
+                        qz = fmaf(qv.y, e1.y, qz);
+                        amax = fmaxf(amax, fmaxf(fabsf(xs[h][m].x), fabsf(xs[h][m].y)));
                     }
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
@@ -383,26 +433,26 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                     const int E = amax > 0.0f ? min(max(14 - (((__float_as_int(amax) >> 23) & 0xff) - 127), -100), 100) : 0;
                     Eh[h] = E;
                     qzh[h] = qz;
+                    const float sE = pow2i(E);
 #pragma unroll
-                    for (int m = 0; m < D / 32; ++m) {
-                        const int ch = lane + 32 * m;
-                        const int slotq = ((ch >> 3) & 1) * NKT + (ch >> 4);
-                        const float x = xs[h][m] * pow2i(E - 2 * cls_of_pos(slotq & 7));
-                        const __half hi = __float2half_rn(x);
-                        const __half lo = __float2half_rn(x - __half2float(hi));
-                        qhl[(h * 2 + 0) * (D + 8) + ch] = hi;
-                        qhl[(h * 2 + 1) * (D + 8) + ch] = lo;
+                    for (int m = 0; m < NPAIR; ++m) {
+                        const float sc = sE * clsf[m];
+                        const float x0 = xs[h][m].x * sc, x1 = xs[h][m].y * sc;
+                        const __half2 hi = __floats2half2_rn(x0, x1);
+                        const float2 hf = __half22float2(hi);
+                        const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                        const int ch = 2 * lane + 64 * m;
+                        *reinterpret_cast<__half2 *>(qhl + (h * 2 + 0) * (D + 8) + ch) = hi;
+                        *reinterpret_cast<__half2 *>(qhl + (h * 2 + 1) * (D + 8) + ch) = lo;
                     }
                 }
                 __syncwarp();
-                const __half *row = qhl + ((hB < GQ ? hB : 0) * 2 + (piece ? 1 : 0)) * (D + 8);
+                const __half *row = qhl + (hB * 2 + (piece ? 1 : 0)) * (D + 8);
 #pragma unroll
                 for (int kt = 0; kt < NKT; ++kt)
 #pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const uint32_t v = *reinterpret_cast<const uint32_t *>(row + 16 * kt + 2 * i + 8 * o);
-                        Bk[kt][o] = hB < GQ ? v : 0u;
-                    }
+                    for (int o = 0; o < 2; ++o)
+                        Bk[kt][o] = *reinterpret_cast<const uint32_t *>(row + 16 * kt + 2 * i + 8 * o);
                 __syncwarp();
             } else {
                 // every lane computes its own 32 values (all columns are live)
@@ -445,168 +495,176 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
                     qzh[h] = __shfl_sync(0xffffffffu, qz, 8 * h);
                 }
             }
-            // score constants of head i
+            // score constants of head hS: logit = raw * c1 + c0 (c1 > 0)
             int Ei = Eh[0];
             float qzi = qzh[0];
 #pragma unroll
             for (int h = 1; h < GQ; ++h)
-                if (i == h) { Ei = Eh[h]; qzi = qzh[h]; }
+                if (hS == h) { Ei = Eh[h]; qzi = qzh[h]; }
             c1 = pow2i(24 - Ei) * a.sl2;
             c0 = qzi * a.sl2;
         }
 
-        const bool partial = 16 * (t0 + nt) > cj;   // chunk reaches past the valid tokens
-        // phase 1: scores of every tile of the chunk (head i, tokens r and r+8);
-        // all tiles' key words are read first so their unpacking and MMAs interleave
-        float lg[CHUNK_TILES][2];
-        uint32_t kw[CHUNK_TILES][NW];
+        auto body = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            const int nt = FULL ? CHUNK_TILES : min(CHUNK_TILES, (cj + TILE - 1) / TILE - t0);
+            // phase 1: raw scores of every tile of the chunk (tokens r and
+            // r+8, head hS); all tiles' key words are read first so that
+            // their unpacking and MMAs interleave
+            float sc[CHUNK_TILES][2];
+            uint32_t kw[CHUNK_TILES][NW];
 #pragma unroll
-        for (int tau = 0; tau < CHUNK_TILES; ++tau)
-            if (tau < nt) lds_words<NW>(stage + KSZ + tau * TB + tile_k_off(D) + lane * NW * 4, kw[tau]);
+            for (int tau = 0; tau < CHUNK_TILES; ++tau)
+                if (FULL || tau < nt) lds_words<NW>(stage + KSZ + tau * TB + tile_k_off(D) + lane * NW * 4, kw[tau]);
 #pragma unroll
-        for (int tau = 0; tau < CHUNK_TILES; ++tau) {
-            lg[tau][0] = lg[tau][1] = -CUDART_INF_F;
-            if (tau < nt) {
-                uint32_t k10[NW];
+            for (int tau = 0; tau < CHUNK_TILES; ++tau) {
+                sc[tau][0] = sc[tau][1] = -CUDART_INF_F;
+                if (FULL || tau < nt) {
+                    uint32_t k10[NW];
 #pragma unroll
-                for (int w = 0; w < NW; ++w) k10[w] = kw[tau][w] >> 10;
-                float da[4] = {0.0f, 0.0f, 0.0f, 0.0f}, db[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    for (int w = 0; w < NW; ++w) k10[w] = kw[tau][w] >> 10;
+                    float d4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int kt = 0; kt < NKT; ++kt) {
-                    const int q0 = kt, q1 = NKT + kt;
-                    const int w0 = 2 * (q0 >> 3), p0 = q0 & 7, w1 = 2 * (q1 >> 3), p1 = q1 & 7;
-                    mma16816((kt & 1) ? db : da, ext_rt(kw[tau][w0], k10[w0], p0),
-                             ext_rt(kw[tau][w0 + 1], k10[w0 + 1], p0), ext_rt(kw[tau][w1], k10[w1], p1),
-                             ext_rt(kw[tau][w1 + 1], k10[w1 + 1], p1), Bk[kt][0], Bk[kt][1]);
-                }
-                lg[tau][0] = fmaf((da[0] + db[0]) + (da[1] + db[1]), c1, c0);
-                lg[tau][1] = fmaf((da[2] + db[2]) + (da[3] + db[3]), c1, c0);
-                if (partial) {
-                    const int slotk = 16 * (t0 + tau) + r;
-                    if (slotk >= cj) lg[tau][0] = -CUDART_INF_F;
-                    if (slotk + 8 >= cj) lg[tau][1] = -CUDART_INF_F;
-                }
-                if (i >= GQ) lg[tau][0] = lg[tau][1] = -CUDART_INF_F;
-            }
-        }
-
-        // phase 2: running max per head, rescale on increase
-        float mloc = -CUDART_INF_F;
-#pragma unroll
-        for (int tau = 0; tau < CHUNK_TILES; ++tau) mloc = fmaxf(mloc, fmaxf(lg[tau][0], lg[tau][1]));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-        const float m_new = fmaxf(m_run, mloc);
-        if (__any_sync(0xffffffffu, m_new > m_run)) {
-            const float alpha = m_new > m_run ? ex2(m_run - m_new) : 1.0f;
-            l_run *= alpha;
-            const float aD = __shfl_sync(0xffffffffu, alpha, 4 * r + i / GPV);
-#pragma unroll
-            for (int mt = 0; mt < NKT; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[mt][e] *= aD;
-            const float aZ = __shfl_sync(0xffffffffu, alpha, hV);
-#pragma unroll
-            for (int v = 0; v < NZ; ++v) zs[v] *= aZ;
-            m_run = m_new;
-        }
-        const float m_use = m_run == -CUDART_INF_F ? 0.0f : m_run;
-
-        // phase 3a: weights and P' = p*s (hi/lo) for every tile of the chunk
-        uint32_t bv[CHUNK_TILES][NV][2];
-#pragma unroll
-        for (int tau = 0; tau < CHUNK_TILES; ++tau) {
-#pragma unroll
-            for (int v = 0; v < NV; ++v) bv[tau][v][0] = bv[tau][v][1] = 0u;
-            if (tau < nt) {
-                const uint8_t *tb = stage + KSZ + tau * TB;
-                const float p0 = ex2(lg[tau][0] - m_use), p1 = ex2(lg[tau][1] - m_use);
-                l_run += p0 + p1;
-                const float pa = __shfl_sync(0xffffffffu, p0, src0);
-                const float pb = __shfl_sync(0xffffffffu, p0, src1);
-                const float pc = __shfl_sync(0xffffffffu, p1, src0);
-                const float pd = __shfl_sync(0xffffffffu, p1, src1);
-                if constexpr (SPLIT) {
-                    const bool lo_lane = (r & 1) != 0;
-#pragma unroll
-                    for (int k = 0; k < NV / 2; ++k) {
-                        // this lane's variant 2k + piece, both pieces; the partner's piece goes across
-                        const int gamma = (2 * k + (lo_lane ? 1 : 0)) * GPV + glow;
-                        const uint4 sz =
-                            *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
-                        const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
-                        const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                        const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
-                        const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
-                        const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
-                        zs[k] = fmaf(pa, e0.y, zs[k]);
-                        zs[k] = fmaf(pb, e1.y, zs[k]);
-                        zs[k] = fmaf(pc, e2.y, zs[k]);
-                        zs[k] = fmaf(pd, e3.y, zs[k]);
-                        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-                        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                        const uint32_t hi0 = h2bits(h01), hi1 = h2bits(h23);
-                        const uint32_t lo0 = h2bits(__floats2half2_rn(x0 - f01.x, x1 - f01.y));
-                        const uint32_t lo1 = h2bits(__floats2half2_rn(x2 - f23.x, x3 - f23.y));
-                        const uint32_t own0 = lo_lane ? lo0 : hi0, own1 = lo_lane ? lo1 : hi1;
-                        const uint32_t got0 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi0 : lo0, 4);
-                        const uint32_t got1 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi1 : lo1, 4);
-                        bv[tau][2 * k][0] = lo_lane ? got0 : own0;
-                        bv[tau][2 * k][1] = lo_lane ? got1 : own1;
-                        bv[tau][2 * k + 1][0] = lo_lane ? own0 : got0;
-                        bv[tau][2 * k + 1][1] = lo_lane ? own1 : got1;
+                    for (int kt = 0; kt < NKT; ++kt) {
+                        const int q0 = kt, q1 = NKT + kt;
+                        const int w0 = 2 * (q0 >> 3), p0 = q0 & 7, w1 = 2 * (q1 >> 3), p1 = q1 & 7;
+                        mma16816(d4, ext_rt(kw[tau][w0], k10[w0], p0), ext_rt(kw[tau][w0 + 1], k10[w0 + 1], p0),
+                                 ext_rt(kw[tau][w1], k10[w1], p1), ext_rt(kw[tau][w1 + 1], k10[w1 + 1], p1), Bk[kt][0],
+                                 Bk[kt][1]);
                     }
-                } else {
-                    // one variant: this lane takes tokens 2i, 2i+1 (hi lane) or 2i+8, 2i+9 (lo lane)
-                    const bool lo_lane = (r & 1) != 0;
-                    const bool gv = glow < NG;           // columns past the value groups stay zero
-                    const int gamma = gv ? glow : 0;
-                    const uint2 sz = *reinterpret_cast<const uint2 *>(
-                        tb + tile_sz_off(D) + (((gamma * 4 + i) * 4) + (lo_lane ? 2 : 0)) * 4);
-                    const float2 ea = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
-                    const float2 eb = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                    const float pA = lo_lane ? pc : pa, pB = lo_lane ? pd : pb;
-                    const float xA = pA * ea.x, xB = pB * eb.x;
-                    if (gv) zs[0] = fmaf(pB, eb.y, fmaf(pA, ea.y, zs[0]));
-                    const __half2 h = __floats2half2_rn(xA, xB);
-                    const float2 f = __half22float2(h);
-                    const uint32_t hi = h2bits(h), lo = h2bits(__floats2half2_rn(xA - f.x, xB - f.y));
-                    // hi lane: keeps hi of (2i, 2i+1), gets hi of (2i+8, 2i+9); lo lane the lo pieces
-                    const uint32_t got = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 4);
-                    bv[tau][0][0] = gv ? (lo_lane ? got : hi) : 0u;
-                    bv[tau][0][1] = gv ? (lo_lane ? lo : got) : 0u;
+                    sc[tau][0] = d4[0] + d4[1];
+                    sc[tau][1] = d4[2] + d4[3];
+                    if (!FULL) {
+                        const int slotk = 16 * (t0 + tau) + r;
+                        if (slotk >= cj) sc[tau][0] = -CUDART_INF_F;
+                        if (slotk + 8 >= cj) sc[tau][1] = -CUDART_INF_F;
+                    }
                 }
             }
-        }
-        // phase 3b: the PV products
+
+            // phase 2: running max per head (c1 > 0, so the largest raw
+            // score gives the largest logit), rescale on increase
+            float mraw = -CUDART_INF_F;
 #pragma unroll
-        for (int tau = 0; tau < CHUNK_TILES; ++tau) {
-            if (tau < nt) {
-                uint32_t vw[NW], v10[NW];
-                lds_words<NW>(stage + KSZ + tau * TB + tile_v_off(D) + lane * NW * 4, vw);
+            for (int tau = 0; tau < CHUNK_TILES; ++tau) mraw = fmaxf(mraw, fmaxf(sc[tau][0], sc[tau][1]));
+            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 4));
+            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 8));
+            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
+            const float m_new = fmaxf(m_run, fmaf(mraw, c1, c0));
+            if (__any_sync(0xffffffffu, m_new > m_run)) {
+                const float alpha = m_new > m_run ? ex2(m_run - m_new) : 1.0f;
+                l_run *= alpha;
+                const float aD = __shfl_sync(0xffffffffu, alpha, 4 * r + i / GPV);
 #pragma unroll
-                for (int w = 0; w < NW; ++w) v10[w] = vw[w] >> 10;
+                for (int mt = 0; mt < NKT; ++mt)
 #pragma unroll
-                for (int mt = 0; mt < NKT; ++mt) {
-                    const int q0 = mt, q1 = NKT + mt;
-                    const int w0 = 2 * (q0 >> 3), p0_ = q0 & 7, w1 = 2 * (q1 >> 3), p1_ = q1 & 7;
-                    const int v = (mt >> 1) / GPV;
-                    mma16816(acc[mt], ext_rt(vw[w0], v10[w0], p0_), ext_rt(vw[w1], v10[w1], p1_),
-                             ext_rt(vw[w0 + 1], v10[w0 + 1], p0_), ext_rt(vw[w1 + 1], v10[w1 + 1], p1_),
-                             bv[tau][v][0], bv[tau][v][1]);
+                    for (int e = 0; e < 4; ++e) acc[mt][e] *= aD;
+                const float aZ = __shfl_sync(0xffffffffu, alpha, hV);
+#pragma unroll
+                for (int v = 0; v < NZ; ++v) zs[v] *= aZ;
+                m_run = m_new;
+            }
+            const float c0m = c0 - (m_run == -CUDART_INF_F ? 0.0f : m_run);
+
+            // phase 3a: weights and P' = p*s (hi/lo) for every tile of the chunk
+            uint32_t bv[CHUNK_TILES][NV][2];
+#pragma unroll
+            for (int tau = 0; tau < CHUNK_TILES; ++tau) {
+#pragma unroll
+                for (int v = 0; v < NV; ++v) bv[tau][v][0] = bv[tau][v][1] = 0u;
+                if (FULL || tau < nt) {
+                    const uint8_t *tb = stage + KSZ + tau * TB;
+                    const float p0 = ex2(fmaf(sc[tau][0], c1, c0m)), p1 = ex2(fmaf(sc[tau][1], c1, c0m));
+                    l_run += p0 + p1;
+                    if constexpr (SPLIT) {
+                        const float pa = __shfl_sync(0xffffffffu, p0, src0);
+                        const float pb = __shfl_sync(0xffffffffu, p0, src1);
+                        const float pc = __shfl_sync(0xffffffffu, p1, src0);
+                        const float pd = __shfl_sync(0xffffffffu, p1, src1);
+#pragma unroll
+                        for (int k = 0; k < NV / 2; ++k) {
+                            // this lane's variant 2k + piece, both pieces; the partner's piece goes across
+                            const int gamma = (2 * k + (lo_lane ? 1 : 0)) * GPV + glow;
+                            const uint4 sz =
+                                *reinterpret_cast<const uint4 *>(tb + tile_sz_off(D) + ((gamma * 4 + i) * 4) * 4);
+                            const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
+                            const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
+                            const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
+                            const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
+                            const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
+                            zs[k] = fmaf(pa, e0.y, zs[k]);
+                            zs[k] = fmaf(pb, e1.y, zs[k]);
+                            zs[k] = fmaf(pc, e2.y, zs[k]);
+                            zs[k] = fmaf(pd, e3.y, zs[k]);
+                            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+                            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                            const uint32_t hi0 = h2bits(h01), hi1 = h2bits(h23);
+                            const uint32_t lo0 = h2bits(__floats2half2_rn(x0 - f01.x, x1 - f01.y));
+                            const uint32_t lo1 = h2bits(__floats2half2_rn(x2 - f23.x, x3 - f23.y));
+                            const uint32_t own0 = lo_lane ? lo0 : hi0, own1 = lo_lane ? lo1 : hi1;
+                            const uint32_t got0 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi0 : lo0, 4);
+                            const uint32_t got1 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi1 : lo1, 4);
+                            bv[tau][2 * k][0] = lo_lane ? got0 : own0;
+                            bv[tau][2 * k][1] = lo_lane ? got1 : own1;
+                            bv[tau][2 * k + 1][0] = lo_lane ? own0 : got0;
+                            bv[tau][2 * k + 1][1] = lo_lane ? own1 : got1;
+                        }
+                    } else {
+                        // one variant: this lane takes tokens 2i, 2i+1 (hi lane) or 2i+8, 2i+9 (lo lane)
+                        const float X = send_second ? p1 : p0;
+                        const float pA = __shfl_sync(0xffffffffu, X, srcA);
+                        const float pB = __shfl_sync(0xffffffffu, X, srcB);
+                        const bool gv = glow < NG;           // columns past the value groups stay zero
+                        const int gamma = gv ? glow : 0;
+                        const uint2 sz = *reinterpret_cast<const uint2 *>(
+                            tb + tile_sz_off(D) + (((gamma * 4 + i) * 4) + (lo_lane ? 2 : 0)) * 4);
+                        const float2 ea = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
+                        const float2 eb = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
+                        const float xA = pA * ea.x, xB = pB * eb.x;
+                        if (gv) zs[0] = fmaf(pB, eb.y, fmaf(pA, ea.y, zs[0]));
+                        const __half2 h = __floats2half2_rn(xA, xB);
+                        const float2 f = __half22float2(h);
+                        const uint32_t hi = h2bits(h), lo = h2bits(__floats2half2_rn(xA - f.x, xB - f.y));
+                        // hi lane: keeps hi of (2i, 2i+1), gets hi of (2i+8, 2i+9); lo lane the lo pieces
+                        const uint32_t got = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 4);
+                        bv[tau][0][0] = gv ? (lo_lane ? got : hi) : 0u;
+                        bv[tau][0][1] = gv ? (lo_lane ? lo : got) : 0u;
+                    }
                 }
             }
-        }
+            // phase 3b: the PV products
+#pragma unroll
+            for (int tau = 0; tau < CHUNK_TILES; ++tau) {
+                if (FULL || tau < nt) {
+                    uint32_t vw[NW], v10[NW];
+                    lds_words<NW>(stage + KSZ + tau * TB + tile_v_off(D) + lane * NW * 4, vw);
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) v10[w] = vw[w] >> 10;
+#pragma unroll
+                    for (int mt = 0; mt < NKT; ++mt) {
+                        const int q0 = mt, q1 = NKT + mt;
+                        const int w0 = 2 * (q0 >> 3), p0_ = q0 & 7, w1 = 2 * (q1 >> 3), p1_ = q1 & 7;
+                        const int v = (mt >> 1) / GPV;
+                        mma16816(acc[mt], ext_rt(vw[w0], v10[w0], p0_), ext_rt(vw[w1], v10[w1], p1_),
+                                 ext_rt(vw[w0 + 1], v10[w0 + 1], p0_), ext_rt(vw[w1 + 1], v10[w1 + 1], p1_),
+                                 bv[tau][v][0], bv[tau][v][1]);
+                    }
+                }
+            }
+        };
+        if (CT * (cc.k + 1) <= cj)
+            body(std::true_type{});
+        else
+            body(std::false_type{});
 
         // release the stage and refill it with the chunk two ahead
         __syncwarp();
         fence_async_shared();
-        if (lj < j1) {
-            issue(lj, lk, st);
-            next(lj, lk);
+        if (ic.j < j1) {
+            issue(ic, st);
+            advance(ic);
         }
-        next(cj_, ck_);
+        advance(cc);
         st ^= 1;
     }
 
