@@ -50,6 +50,23 @@ bool some_sequence_empty(const ott_cache *c) {
     return false;
 }
 
+// With per-sequence counts, T is the longest sequence: releases and refills
+// move it both ways, and the capacity checks are per sequence.
+void refresh_T(ott_cache *c) {
+    long long t = 0;
+    for (int b = 0; b < c->B; ++b) t = c->Tb[b] > t ? c->Tb[b] : t;
+    c->T = t;
+}
+
+// Switch a cache to per-sequence counts (ragged decode and flush lists),
+// every sequence at the current uniform count.
+void to_per_sequence(ott_cache *c) {
+    c->Tb.assign(c->B, c->T);
+    c->nfb.assign(c->B, c->nf);
+    c->ragged = 1;
+    c->nf = 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -282,11 +299,11 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T = L;
     c->nf = nf;
-    if (c->paged) {   // blocks are read through the table: per-sequence counts from now on
-        c->Tb.assign(c->B, L);
-        c->nfb.assign(c->B, nf);
-        c->ragged = 1;
-        c->nf = 0;
+    // a paged cache reads blocks through the table, and a cache emptied by
+    // releases keeps per-sequence counts: both continue per sequence
+    if (c->paged || c->ragged) {
+        c->ragged = 0;
+        to_per_sequence(c);
     }
     return OTT_OK;
 }
@@ -370,14 +387,11 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     if (!c) return OTT_ERR_INVALID;
     if (c->poisoned) return OTT_ERR_STATE;
     if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
+    // with per-sequence counts T is the longest sequence, so this is each
+    // sequence's own capacity check
     if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
     if (some_sequence_empty(c)) return OTT_ERR_STATE;
-    if (c->paged && !c->ragged) {   // blocks are read through the table: per-sequence counts
-        c->Tb.assign(c->B, c->T);
-        c->nfb.assign(c->B, c->nf);
-        c->ragged = 1;
-        c->nf = 0;
-    }
+    if (c->paged && !c->ragged) to_per_sequence(c);   // blocks are read through the table
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (c->ragged)
         return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
@@ -426,24 +440,25 @@ int ott_release_seq(ott_cache *c, int b, void *stream) {
     if (!c) return OTT_ERR_INVALID;
     if (c->poisoned || !c->ragged_capable || c->T < 1) return OTT_ERR_STATE;
     if (b < 0 || b >= c->B) return OTT_ERR_INVALID;
-    if (!c->ragged) {   // a uniform prefill so far: switch to per-sequence counts
-        c->Tb.assign(c->B, c->T);
-        c->nfb.assign(c->B, c->nf);
-        c->ragged = 1;
-        c->nf = 0;
-    }
+    if (!c->ragged) to_per_sequence(c);   // a uniform prefill so far
+    if (c->Tb[b] == 0) return OTT_OK;      // already empty
     cudaError_t e = launch_release(c, b, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->free_blocks += blocks_needed(c, (long long)c->nfb[b] * c->Hkv);
     c->Tb[b] = 0;
     c->nfb[b] = 0;
+    refresh_T(c);
     return OTT_OK;
 }
 
 int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, void *stream) {
     if (!c) return OTT_ERR_INVALID;
-    if (c->poisoned || !c->ragged) return OTT_ERR_STATE;
+    if (c->poisoned || !c->ragged_capable) return OTT_ERR_STATE;
     if (b < 0 || b >= c->B || L < 1 || !K || !V || !aligned16(K) || !aligned16(V)) return OTT_ERR_INVALID;
+    if (!c->ragged) {
+        if (c->T != 0) return OTT_ERR_STATE;   // a uniform batch: release the sequence first
+        to_per_sequence(c);                    // an empty cache filled one sequence at a time
+    }
     if (c->Tb[b] != 0) return OTT_ERR_STATE;   // release the sequence first
     if (L > c->max_tokens) return OTT_ERR_CAPACITY;
     const int nf = flushes_after(c, L);
@@ -464,7 +479,7 @@ int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, vo
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->Tb[b] = L;
     c->nfb[b] = nf;
-    if (L > c->T) c->T = L;
+    refresh_T(c);
     return OTT_OK;
 }
 

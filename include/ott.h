@@ -136,8 +136,11 @@ int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max
  * Serving (caches from ott_create_ragged or ott_create_paged): sequence b
  * finishes. It drops all its tokens and (paged pool) returns its blocks; the
  * slot must be refilled with ott_prefill_seq before the next ott_append or
- * decode (which return OTT_ERR_STATE while a sequence is empty). stream: the
- * stream of the cache's other calls.
+ * decode (which return OTT_ERR_STATE while a sequence is empty). Releasing an
+ * empty sequence does nothing. With per-sequence counts, max_tokens bounds
+ * each sequence: a loop that releases and refills sequences can run for any
+ * number of steps as long as no single sequence outgrows max_tokens.
+ * stream: the stream of the cache's other calls.
  */
 int ott_release_seq(ott_cache *c, int b, void *stream);
 
@@ -145,8 +148,10 @@ int ott_release_seq(ott_cache *c, int b, void *stream);
  * Serving: fill the empty sequence b with a new prompt of L tokens; from then
  * on it is a fresh sequence of its own (token indices from 0), flushed and
  * attended as in ott_prefill_lens. K, V: DEVICE fp16 [Hkv][L][d], contiguous.
- * OTT_ERR_STATE if b holds tokens; OTT_ERR_CAPACITY if L > max_tokens or the
- * paged pool lacks free blocks.
+ * An empty cache from ott_create_ragged or ott_create_paged may be filled
+ * this way one sequence at a time (appends and decodes wait until every
+ * sequence holds a token). OTT_ERR_STATE if b holds tokens; OTT_ERR_CAPACITY
+ * if L > max_tokens or the paged pool lacks free blocks.
  */
 int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, void *stream);
 

@@ -107,7 +107,8 @@ def test_cold_static_decode_matches(ott):
                                                C.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == ott.OTT_OK
         torch.cuda.synchronize()
-        assert float((out.float() - ref.float()).abs().max()) <= 2e-3
+        # the same kernels on the same inputs: the same bits
+        assert torch.equal(out, ref)
 
 
 def test_cold_argument_errors(ott):

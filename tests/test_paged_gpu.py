@@ -214,4 +214,78 @@ def test_paged_static_decode_matches(ott):
                                                C.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == ott.OTT_OK
         torch.cuda.synchronize()
-        assert float((out.float() - ref.float()).abs().max()) <= 2e-3
+        # the same kernels on the same inputs: the same bits
+        assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("paged", [True, False])
+def test_rotation_beyond_max_tokens(oracle_mod, ott, paged):
+    """A serving loop that keeps releasing and refilling sequences runs for
+    more appends than max_tokens: the capacity is per sequence, so no call is
+    refused while every sequence stays below it."""
+    B, Hq, Hkv, d, G, R, P, M = 3, 3, 3, 64, 8, 2, 3, 40
+    steps = 3 * M
+    K, V = _gen(61, B, Hkv, steps + M, d)
+    q_all = torch.randn(steps, B, Hq, d, generator=torch.Generator().manual_seed(62)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    dev = torch.device("cuda")
+    # a pool for every sequence at its longest
+    kw = dict(pool_blocks=_blocks([M] * B, G, R, Hkv) + 1) if paged else dict(ragged=True)
+    lens = [5, 12, 20]
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=M, **kw) as c:
+        c.prefill_lens(K[:, :, :20].contiguous().to(dev), V[:, :, :20].contiguous().to(dev), lens)
+        orc.prefill_lens(K[:, :, :20].contiguous(), V[:, :, :20].contiguous(), lens)
+        T = list(lens)
+        refills = 0
+        for s in range(steps):
+            for b in range(B):
+                if T[b] + 1 > M:                # about to outgrow max_tokens: replace it
+                    c.release_seq(b)
+                    orc.release_seq(b)
+                    L = 1 + (s + 3 * b) % 7
+                    kk, vv = _gen(1000 + s * B + b, 1, Hkv, L, d)
+                    c.prefill_seq(b, kk[0].contiguous().to(dev), vv[0].contiguous().to(dev))
+                    orc.prefill_seq(b, kk[0].contiguous(), vv[0].contiguous())
+                    T[b] = L
+                    refills += 1
+            k, v = K[:, :, M + s].contiguous(), V[:, :, M + s].contiguous()
+            c.append(k.to(dev), v.to(dev))
+            orc.append(k, v)
+            T = [t + 1 for t in T]
+            if s % 11 == 0 or s == steps - 1:
+                compare_out(c.decode_attn(q_all[s].to(dev)), orc.decode(q_all[s]), f"step {s} lens {T}")
+        assert refills >= 6 and steps > M
+        for b in range(B):
+            _compare_seq(c, orc, b, Hkv)
+        c.check_device()
+
+
+@pytest.mark.parametrize("paged", [True, False])
+def test_empty_cache_filled_one_sequence_at_a_time(oracle_mod, ott, paged):
+    """An empty serving cache takes its prompts through ott_prefill_seq, one
+    sequence at a time; appends wait until every sequence holds a token."""
+    B, Hq, Hkv, d, G, R, P = 3, 6, 3, 128, 16, 2, 4
+    lens, steps = [37, 5, 60], 12
+    dev = torch.device("cuda")
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P)
+    kw = dict(pool_blocks=_blocks([L + steps for L in lens], G, R, Hkv)) if paged else dict(ragged=True)
+    K, V = _gen(71, B, Hkv, steps, d)
+    q = torch.randn(B, Hq, d, generator=torch.Generator().manual_seed(72)).half()
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=max(lens) + steps, **kw) as c:
+        for b, L in enumerate(lens):
+            kk, vv = _gen(80 + b, 1, Hkv, L, d)
+            c.prefill_seq(b, kk[0].contiguous().to(dev), vv[0].contiguous().to(dev))
+            orc.prefill_seq(b, kk[0].contiguous(), vv[0].contiguous())
+            if b < B - 1:
+                with pytest.raises(ott.OTTError) as ei:   # sequence b+1 is still empty
+                    c.append(K[:, :, 0].contiguous().to(dev), V[:, :, 0].contiguous().to(dev))
+                assert ei.value.code == ott.OTT_ERR_STATE
+        for s in range(steps):
+            k, v = K[:, :, s].contiguous(), V[:, :, s].contiguous()
+            c.append(k.to(dev), v.to(dev))
+            orc.append(k, v)
+        compare_out(c.decode_attn(q.to(dev)), orc.decode(q), "after the appends")
+        for b in range(B):
+            assert c.seq_counts(b)[0] == lens[b] + steps
+            _compare_seq(c, orc, b, Hkv)
+        c.check_device()
