@@ -292,9 +292,18 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     rate, dt, sample, nproc = oracle_rate_cores(w, args.steps, args.warmup, args.oracle_units_per_core)
+    # ms_per_step is the measured time of one step of the sampled work (what
+    # this run actually did); value is that rate scaled to the whole workload
+    # by algorithmic bytes, with the factor stated in `extrapolation`
+    sampled_ms = 1e3 * dt / args.steps
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.B / rate,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sampled_ms,
+        "extrapolation": {"sampled_ms_per_step": sampled_ms,
+                          "full_workload_ms_per_step": (1e3 * w.B / rate) if rate > 0 else None,
+                          "scale_factor": ((1e3 * w.B / rate) / sampled_ms) if rate > 0 and sampled_ms > 0 else None,
+                          "basis": "algorithmic bytes of the sampled units against the whole workload; "
+                                   "value is decode tokens/s of the whole workload at the sampled rate"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
@@ -307,6 +316,31 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ our arm
+
+def copy_peak(ott, dev, stream, gib: int = 2, reps: int = 10):
+    """HBM bandwidth of a plain streaming copy (the library's ott_hbm_copy),
+    measured in this process: `gib` GiB read and as many written per call,
+    best of `reps` event-timed calls after 3 warm-up calls."""
+    n = gib << 28   # float32 elements
+    src = torch.empty(n, dtype=torch.float32, device=dev).fill_(1.0)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        ott.hbm_copy(dst, src, stream)
+    best = None
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ott.hbm_copy(dst, src, stream)
+        b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b)
+        best = t if best is None else min(best, t)
+    nbytes = 2 * n * 4
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"gbs": nbytes / (best * 1e-3) / 1e9, "bytes_per_call": nbytes, "kernel": "ott_hbm_copy",
+            "method": f"{gib} GiB read + {gib} GiB written per call, best of {reps} CUDA-event-timed calls"}
+
 
 def run_ours(args, w):
     import bit_kv_cache_ott_gb300 as ott
@@ -326,7 +360,7 @@ def run_ours(args, w):
     # weak scaling: rank r holds its own shard of B sequences
     wr = shard(w, rank, ws)
     K_steps, W_steps, E_steps = args.steps, args.warmup, args.e2e_steps
-    total_steps = W_steps + K_steps + E_steps
+    total_steps = W_steps + K_steps + E_steps + w.G + 2   # + the flush probe
     caches = []
     lens = synth.seq_lens(wr)
     for layer in range(w.layers):
@@ -351,75 +385,123 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float16, device=dev)
 
-    def step(s, ev=None):
+    def step(s):
         k, v, q = dev_in[s % n_distinct]
         for c in caches:
             c.append(k, v, stream)
-            if ev is not None:
-                ev[0].record(stream)
             decode_call(c, w, q, out, stream)
-            if ev is not None:
-                ev[1].record(stream)
+
+    def flush_due_next(Ts):
+        """Does the next append make some sequence flush?"""
+        return any((t + 1 - w.R) % w.G == 0 and t + 1 >= w.G + w.R for t in Ts)
+
+    # caches that fit in about twice the L2 would be read from L2 by repeated
+    # calls: a buffer larger than L2 is written between the timed calls
+    cache_total = caches[0].device_bytes() * w.layers
+    l2_flush = cache_total < 2 * L2_BYTES
+    l2_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if l2_flush else None
+
+    def flush_l2(s):
+        if l2_buf is not None:
+            l2_buf.fill_(float(s))
 
     for s in range(W_steps):
         step(s)
     torch.cuda.synchronize()
 
-    # timed region: K steps, decode kernels bracketed by events on the same stream
-    launches = 0
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(K_steps * w.layers)]
-    dec_bytes = 0
-    flushes = 0
+    # the HBM copy peak of this GPU, measured in this run (2 GiB read + 2 GiB written)
+    peak_run = None
+    if not args.no_copy_peak:
+        peak_run = copy_peak(ott, dev, stream)
+
+    # timed region: K whole steps (append, with its flush when one is due,
+    # then the decode call), with no event inside the loop; with an L2 flush,
+    # each step is bracketed by events and the flush writes fall outside
     Ts = [caches[0].seq_counts(b)[0] for b in range(w.B)]
     T0 = max(Ts)
-    # cold-pool policy: the quantized and cold stores' sizes are read before
-    # and after the timed region and taken as linear in the flushes between
-    cold_q0 = [cold_quant_bytes(c) for c in caches] if w.cold >= 0 else None
-    step_log = []     # (token counts, flush steps so far) per timed step
+    cold = w.cold >= 0
     flush_steps = 0
+    step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K_steps if l2_flush else 0)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
         e0.record(stream)
         for s in range(K_steps):
-            k, v, q = dev_in[(W_steps + s) % n_distinct]
+            flush_steps += int(flush_due_next(Ts))
             Ts = [t + 1 for t in Ts]
-            flush_launch = any((t - w.R) % w.G == 0 and t >= w.G + w.R for t in Ts)   # some sequence flushes now
-            flush_steps += int(flush_launch)
-            for li, c in enumerate(caches):
-                c.append(k, v, stream)
-                flushes += int(flush_launch)
-                ev = dec_events[s * w.layers + li]
-                ev[0].record(stream)
-                decode_call(c, w, q, out, stream)
-                ev[1].record(stream)
-            # the byte count is taken after the timed region (only the
-            # per-step token counts are kept here, so the host stays ahead)
-            step_log.append((tuple(Ts), flush_steps))
+            if l2_flush:
+                flush_l2(s)
+                step_events[s][0].record(stream)
+            step(W_steps + s)
+            if l2_flush:
+                step_events[s][1].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    ms = e0.elapsed_time(e1)
-    dec_ms = sum(a.elapsed_time(b) for a, b in dec_events)
-    if cold_q0 is None:
-        dec_bytes = sum(step_bytes(w, list(ts)) for ts, _ in step_log) * w.layers
-    else:
-        cold_q1 = [cold_quant_bytes(c) for c in caches]
-        nfl = max(1, flush_steps)
-        dec_bytes = sum(metrics.hot_bytes(ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P)
-                        + cold_q0[li] + (cold_q1[li] - cold_q0[li]) * f / nfl
-                        for ts, f in step_log for li in range(w.layers))
+    ms = sum(a.elapsed_time(b) for a, b in step_events) if l2_flush else e0.elapsed_time(e1)
+    flushes = flush_steps * w.layers
     # append + decode + combine (+ the Top-K bounds and pick), plus flushes
     launches = K_steps * w.layers * (5 if w.topk > 0 else 3) + flushes
     ms = max_over_ranks(ms, dev)
+    s_next = W_steps + K_steps
+
+    # One flush cycle (G steps) after the timed region, each append and each
+    # decode call bracketed by its own events on the launch stream:
+    #  * the roofline: the decode call's bytes and time averaged over a whole
+    #    flush cycle (its bytes fall as the fp16 residual empties at a flush);
+    #  * the flush: the append that flushes against the median plain append.
+    #    The flush runs once every G steps for a batch of equal lengths, so K
+    #    timed steps rarely hold their share of it; `value` charges it at its
+    #    rate, one flush per G steps. A ragged batch flushes its sequences at
+    #    different steps, so its timed steps already hold their share.
+    n_dec = w.G
+    app_ev, dec_ev, app_due, dec_bytes_list = [], [], [], []
+    for i in range(n_dec):
+        k, v, q = dev_in[s_next % n_distinct]
+        due = flush_due_next(Ts)
+        Ts = [t + 1 for t in Ts]
+        ea = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ed = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ea[0].record(stream)
+        for c in caches:
+            c.append(k, v, stream)
+        ea[1].record(stream)
+        flush_l2(i)
+        ed[0].record(stream)
+        for c in caches:
+            decode_call(c, w, q, out, stream)
+        ed[1].record(stream)
+        app_ev.append(ea)
+        dec_ev.append(ed)
+        app_due.append(due)
+        if not cold:
+            dec_bytes_list.append(step_bytes(w, list(Ts)) * w.layers)
+        s_next += 1
+    torch.cuda.synchronize()
+    dec_ms = sum(a_.elapsed_time(b_) for a_, b_ in dec_ev)
+    if cold:   # block and cold-pool sizes (they depend on the data) read once, after the cycle
+        dec_bytes_list = [sum(metrics.hot_bytes(Ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) + cold_quant_bytes(c)
+                              for c in caches)] * n_dec
+    dec_call_bytes = sum(dec_bytes_list) / n_dec
+    flush_us = None
+    if not w.ragged:
+        adt = [a_.elapsed_time(b_) for a_, b_ in app_ev]
+        plain = [t for t, d in zip(adt, app_due) if not d]
+        with_flush = [t for t, d in zip(adt, app_due) if d]
+        if plain and with_flush:
+            flush_us = max(0.0, 1e3 * (statistics.mean(with_flush) - statistics.median(plain)))
+    ms_amortized = ms
+    if flush_us is not None:
+        ms_amortized = ms + (K_steps / w.G - flush_steps) * flush_us * 1e-3
+
     for c in caches:
         c.check_device()
 
-    value = job_tokens_per_s(w.B, K_steps, ws, ms)
-    n_launch = K_steps * w.layers
-    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    value = job_tokens_per_s(w.B, K_steps, ws, ms_amortized)
+    n_launch = n_dec * w.layers
+    achieved = dec_call_bytes * n_dec / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
 
     # end to end through the public API with host buffers (pinned), per step:
@@ -496,7 +578,7 @@ def run_ours(args, w):
         fp16_bytes = sum(metrics.fp16_cache_bytes(t, 1, w.Hkv, w.d) for t in synth.seq_lens(wr)) * w.layers
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K_steps,
-            "warmup": W_steps, "ms_per_step": ms / K_steps, "higher_is_better": True, "scaling": "weak",
+            "warmup": W_steps, "ms_per_step": ms_amortized / K_steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp16 storage, fp32 accumulation", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
                        "G": w.G, "R": w.R, "P": w.P, "layers": w.layers, "T_start": T0,
@@ -505,22 +587,36 @@ def run_ours(args, w):
                        **({"paged": "blocks from one pool of the blocks the run fills, through a block table"}
                           if w.paged else {}),
                        **({"cold": w.cold, "cold_bytes": "block and cold-pool sizes read from the device "
-                           "before and after the timed region, linear in between"} if w.cold >= 0 else {}),
+                           "after the decode timing cycle"} if w.cold >= 0 else {}),
                        **({"ragged_lens": {"min": min(lens), "max": max(lens),
                                            "mean": round(sum(lens) / len(lens), 1)}} if w.ragged else {}),
-                       "l2": (f"cache {cache_bytes / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"
-                              if cache_bytes > L2_BYTES else "cache fits L2: L2-resident numbers"),
+                       "l2": (f"cache {cache_bytes / 1e6:.0f} MB, L2 {L2_BYTES / 1e6:.0f} MB: a "
+                              f"{2 * L2_BYTES / 1e6:.0f} MB buffer is written between timed calls (outside the timing)"
+                              if l2_flush else
+                              f"cache {cache_bytes / 1e6:.0f} MB > 2 x L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"),
                        "parallelism": f"weak-scaled shards x{ws}" if ws > 1 else "1 GPU"},
+            "ms_per_step_measured": ms / K_steps,
+            "flush": {"us_per_flush": flush_us, "flush_steps_in_timed_region": flush_steps,
+                      "charged": (f"one flush per {w.G} steps: {K_steps / w.G:.3f} flushes for {K_steps} steps, "
+                                  f"{flush_steps} timed" if flush_us is not None else
+                                  "ragged batch: its timed steps hold their own flushes")},
             "decode_gbs": achieved, "decode_pct_of_hbm_peak": 100.0 * achieved / peak,
             "decode_us_per_launch": 1e3 * dec_ms / n_launch,
+            "decode_calls_timed": n_dec,
             "flushes_in_timed_region": flushes,
-            "bytes_per_decoded_token": dec_bytes / (n_launch * w.B) * w.layers,
+            "bytes_per_decoded_token": dec_call_bytes / w.B,
             "cache_bytes": cache_bytes, "fp16_cache_bytes": fp16_bytes,
+            "peak_same_run": peak_run,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
+                         "frac_same_run": (achieved / peak_run["gbs"]) if peak_run else None,
+                         "pct_of_nominal_8000": 100.0 * achieved / 8000.0,
                          "kernel": ("k_topk_bounds + k_topk_pick + k_decode + k_combine (ott_decode_attn_topk)" if w.topk > 0
                                     else "k_decode + k_combine (ott_decode_attn)"),
-                         "algorithmic_bytes_per_launch": dec_bytes / n_launch,
+                         "timing": f"{n_dec} decode calls over one flush cycle after the timed steps "
+                                   "(one per step, after that step's append), CUDA events around each call on "
+                                   "the launch stream; bytes averaged over the same calls",
+                         "algorithmic_bytes_per_launch": dec_call_bytes / w.layers,
                          "traffic": recorded_traffic(w.name)},
             "clocks": clk.summary(),
             "gpu_launches": launches,
@@ -547,6 +643,7 @@ def main(argv=None):
     ap.add_argument("--oracle-steps", type=int, default=24)
     ap.add_argument("--oracle-units-per-core", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-peak", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

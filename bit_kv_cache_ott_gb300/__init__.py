@@ -16,7 +16,7 @@ import torch
 
 from . import synth  # noqa: F401  (seeded workloads)
 
-__all__ = ["OTTCache", "OTTError", "load", "status_str", "lib_path"]
+__all__ = ["OTTCache", "OTTError", "load", "status_str", "lib_path", "hbm_copy"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libott.so")
@@ -40,7 +40,7 @@ class StateExport(C.Structure):
 SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_paged", "ott_release_seq", "ott_prefill_seq",
            "ott_free_blocks", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
            "ott_decode_attn", "ott_decode_attn_static", "ott_decode_attn_topk", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
-           "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str")
+           "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str", "ott_hbm_copy")
 
 
 def lib_path() -> str:
@@ -84,12 +84,25 @@ def load(build_if_missing: bool = False):
     L.ott_device_bytes.restype = i64
     L.ott_status_str.argtypes = [i32]
     L.ott_status_str.restype = C.c_char_p
+    L.ott_hbm_copy.argtypes = [P, P, i64, P]
     _lib = L
     return L
 
 
 def status_str(code: int) -> str:
     return load().ott_status_str(code).decode()
+
+
+def hbm_copy(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """Copy src into dst (same byte size, CUDA tensors) with the library's
+    streaming copy kernel: the bandwidth probe that times HBM in the same run
+    as the decode."""
+    if not (dst.is_cuda and src.is_cuda and dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("hbm_copy: contiguous CUDA tensors")
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("hbm_copy: sizes differ")
+    _check(load().ott_hbm_copy(dst.data_ptr(), src.data_ptr(), n, _stream(stream)), "ott_hbm_copy")
 
 
 def _check(rc: int, what: str):

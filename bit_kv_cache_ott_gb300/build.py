@@ -1,6 +1,6 @@
 """Build libott.so in-tree for sm_103a with nvcc (no cmake, no torch extension).
 
-The three translation units compile in parallel, then link into
+The translation units compile in parallel, then link into
 ``bit_kv_cache_ott_gb300/_build/libott.so``. No fast-math: the quantization
 decisions must be the plain IEEE operations.
 """
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libott.so")
-SOURCES = ["ott_api.cu", "ott_flush.cu", "ott_decode.cu", "ott_topk.cu"]
+SOURCES = ["ott_api.cu", "ott_flush.cu", "ott_decode.cu", "ott_topk.cu", "ott_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      f"-I{os.path.join(ROOT, 'include')}"]

@@ -153,13 +153,14 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const int nwarps = sms * DEC_WARPS;
     c->maxu = (int)((long long)B * Hkv / nwarps) + 2;
     // ragged batches: units differ in length, so a range of L items can touch
-    // up to L units; L <= ceil(W_max / warps) with at most NB blocks and
-    // ceil((G + R + P) / 32) fp16 items per unit
+    // up to L units; L <= ceil(W_max / warps) with at most NB blocks of
+    // chunks_per_block(G) items and ceil((G + R + P) / FP16_CHUNK) fp16 items
+    // per unit
     c->ragged_capable = ragged;
     c->ragged = 0;
     c->maxu_r = 0;
     if (ragged) {
-        const long long iu_max = (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + (long long)c->NB;
+        const long long iu_max = (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + (long long)c->NB * chunks_per_block(G);
         const long long w_max = (long long)B * Hkv * iu_max;
         c->maxu_r = (int)((w_max + nwarps - 1) / nwarps) + 2;
         c->Tb.assign(B, 0);

@@ -59,14 +59,31 @@ __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+// The KV stream is read once per call: its bulk copies carry an L2
+// evict-first policy, so that it does not push the split-K partials (read by
+// the combine right after) and the queries out of L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_only(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
             smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(evict_first_policy())
         : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    expect_tx(bar, bytes);
+    bulk_copy_only(dst, src, bytes, bar);
 }
 
 __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
@@ -120,8 +137,10 @@ struct DecodeArgs {
     int nf, jfull;      // blocks; blocks j >= jfull hold G tokens
     int ring_start;     // first residual token's ring slot
     int ntail, npool;
-    int Sf;             // fp16 chunks per unit
-    int Iu;             // work items per unit: Sf + nf
+    int Sf;             // fp16 items per unit (FP16_CHUNK tokens each)
+    int Iu;             // work items per unit: Sf + nf * CPB
+    int CPB;            // chunks (CHUNK_TILES tiles) per block
+    int IPB;            // quantized work items per block: 1 (whole blocks) or CPB (chunks)
     long long W;        // U * Iu
     int NWp;            // warps in the grid
     int MAXU;           // units a warp's range can touch
@@ -258,16 +277,20 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 }
 
 // ---------------------------------------------------------------- quantized segment
-// Blocks [j0, j1) of unit u (Top-K: the blocks listed at positions [j0, j1)
-// of the unit's selection); the partial goes to part[slot].
+// Quantized work items [q0, q1) of unit u: item q is the block at position
+// q / IPB (Top-K: the block listed there in the unit's selection), whole
+// (IPB = 1) or its chunk q % IPB (IPB = CPB: chunks of up to CHUNK_TILES
+// tiles); the partial goes to part[slot]. Chunks past a short block's tokens
+// hold no work and are skipped.
 //
-// The chunks of the segment (up to CHUNK_TILES tiles of one block each) are
-// walked by two cursors: one issues the bulk copies two chunks ahead, the
-// other consumes them. A chunk whose tiles are all full (the common case:
-// every block after the pool fills holds G tokens) runs a body without any
-// masking; the ragged last chunk of a short block takes the masked body.
+// The chunks are walked by two cursors: one issues the bulk copies two
+// chunks ahead, the other consumes them. The first chunk of each block the
+// segment meets also brings the block's K scale/zero header. A chunk whose
+// tiles are all full (the common case: every block after the pool fills holds
+// G tokens) runs a body without any masking; the ragged last chunk of a short
+// block takes the masked body.
 template <int D, int GQ, bool CO, bool TK, bool RG>
-__device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, int j1, uint8_t *stg0,
+__device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, int q1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
                               int lane) {
     using C = Cfg<D, GQ>;
@@ -284,25 +307,35 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
         }
         return block_cnt<CO>(a, u, j);
     };
-    // chunk cursor: position j, chunk k of that block, the block's tokens
+    // chunk cursor: block position j, chunk k of that block, the block's tokens
     struct Cursor {
         int j, k, cnt;
     };
-    auto skip_empty = [&](Cursor &c) {
-        while (c.j < j1 && c.cnt == 0) {
+    const int CPB = a.CPB, IPB = a.IPB, KPI = CPB / IPB;   // chunks per item
+    const int jl = (q1 - 1) / IPB, kl = ((q1 - 1) % IPB + 1) * KPI - 1;   // the segment's last chunk
+    auto past = [&](const Cursor &c) { return c.j > jl || (c.j == jl && c.k > kl); };
+    // move to the next chunk that holds tokens (or past the segment)
+    auto settle = [&](Cursor &c) {
+        while (!past(c) && CT * c.k >= c.cnt) {
             ++c.j;
-            c.cnt = c.j < j1 ? cnt_at(c.j) : 0;
+            c.k = 0;
+            c.cnt = c.j <= jl ? cnt_at(c.j) : 0;
         }
     };
     auto advance = [&](Cursor &c) {
-        ++c.k;
-        if (CT * c.k >= c.cnt) {
-            c.k = 0;
+        if (++c.k >= CPB) {
             ++c.j;
-            c.cnt = c.j < j1 ? cnt_at(c.j) : 0;
-            skip_empty(c);
+            c.k = 0;
+            c.cnt = c.j <= jl ? cnt_at(c.j) : 0;
         }
+        settle(c);
     };
+    Cursor ic{q0 / IPB, (q0 % IPB) * KPI, 0};
+    ic.cnt = cnt_at(ic.j);
+    settle(ic);
+    // a block's first chunk in this segment brings the block's header
+    const int jf = ic.j, kf = ic.k;
+    auto hdr = [&](const Cursor &c) { return c.k == 0 || (c.j == jf && c.k == kf); };
     auto issue = [&](const Cursor &c, int st) {
         if (lane == 0) {
             const int vt = (c.cnt + TILE - 1) / TILE;
@@ -315,18 +348,21 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
             }
             const uint8_t *bsrc = a.blk + bslot * a.blk_bytes;
             uint8_t *dst = st ? stg1 : stg0;
-            if (c.k == 0)
+            if (c.k == 0) {
                 bulk_load(dst, bsrc, (uint32_t)(KSZ + nt * TB), &bars[st]);
-            else
+            } else if (hdr(c)) {   // the header, then the chunk's tiles, on one barrier
+                expect_tx(&bars[st], (uint32_t)(KSZ + nt * TB));
+                bulk_copy_only(dst, bsrc, (uint32_t)KSZ, &bars[st]);
+                bulk_copy_only(dst + KSZ, bsrc + KSZ + (size_t)t0 * TB, (uint32_t)(nt * TB), &bars[st]);
+            } else {
                 bulk_load(dst + KSZ, bsrc + KSZ + (size_t)t0 * TB, (uint32_t)(nt * TB), &bars[st]);
+            }
         }
     };
     // start the copies first, then stage the queries while they fly
-    Cursor ic{j0, 0, j0 < j1 ? cnt_at(j0) : 0};
-    skip_empty(ic);
     Cursor cc = ic;
     int st_issue = 0;
-    for (int n = 0; n < 2 && ic.j < j1; ++n) {
+    for (int n = 0; n < 2 && !past(ic); ++n) {
         issue(ic, st_issue);
         st_issue ^= 1;
         advance(ic);
@@ -390,7 +426,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
     const bool send_second = ((i / GQ) & 1) != 0;
 
     int st = 0;
-    while (cc.j < j1) {
+    while (!past(cc)) {
         uint8_t *stage = st ? stg1 : stg0;
         if (!mbar_wait(&bars[st], (phase >> st) & 1u)) {
             if (lane == 0) atomicExch(&a.ctl[1], 1);
@@ -402,7 +438,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
         const int cj = cc.cnt;
         const int t0 = cc.k * CHUNK_TILES;
 
-        if (cc.k == 0) {
+        if (hdr(cc)) {
             // per-block constants: B = q*s split in hi/lo at a per-block
             // exponent E and a per-channel class scale; qz = q.z
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(stage);
@@ -660,7 +696,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int j0, i
         // release the stage and refill it with the chunk two ahead
         __syncwarp();
         fence_async_shared();
-        if (ic.j < j1) {
+        if (!past(ic)) {
             issue(ic, st);
             advance(ic);
         }
@@ -723,17 +759,6 @@ __device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1,
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(b0));
-}
-__device__ __forceinline__ void bulk_copy_only(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
 }
 
 // Under the cold-pool policy the fp16 tokens continue with the cold pool
@@ -982,19 +1007,24 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
     for (int k0 = wi * GRP; k0 < ncand; k0 += cw * GRP) {
-        const float *ps[GRP];
-        float ms[GRP];
+        // every load of the group is issued before any arithmetic (one round trip)
+        float ms[GRP], ls[GRP], vs[GRP][CPL];
 #pragma unroll
         for (int g = 0; g < GRP; ++g) {
-            ps[g] = nullptr;
             ms[g] = -CUDART_INF_F;
+            ls[g] = 0.0f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) vs[g][c] = 0.0f;
             const int k = k0 + g;
             if (k < ncand) {
                 const int type = k < n0 ? 0 : 1;
                 const int ww = type ? q0 + (k - n0) : wa + k;
                 const int uo = ww == wa ? uo_a : 0;
-                ps[g] = a.part + (part_slot(a, ww, uo, type) * GQ + h) * (D + 2);
-                ms[g] = ps[g][0];
+                const float *p = a.part + (part_slot(a, ww, uo, type) * GQ + h) * (D + 2);
+                ms[g] = p[0];
+                ls[g] = p[1];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) vs[g][c] = p[2 + lane * CPL + c];
             }
         }
         float mn = M;
@@ -1007,11 +1037,10 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
         for (int c = 0; c < CPL; ++c) acc[c] *= so;
 #pragma unroll
         for (int g = 0; g < GRP; ++g) {
-            if (ms[g] == -CUDART_INF_F) continue;
-            const float sn = ex2(ms[g] - mn);
-            L = fmaf(sn, ps[g][1], L);
+            const float sn = ex2(ms[g] - mn);   // 0 for an empty segment (m = -inf)
+            L = fmaf(sn, ls[g], L);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(sn, ps[g][2 + lane * CPL + c], acc[c]);
+            for (int c = 0; c < CPL; ++c) acc[c] = fmaf(sn, vs[g][c], acc[c]);
         }
         M = mn;
     }
@@ -1066,7 +1095,7 @@ cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cud
 }
 
 // One sequence's counts after T tokens and nf flushes.
-inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf, int nq_items) {
+inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf, int nq_blocks, int ipb) {
     SeqEntry e;
     const long long tail_start = (long long)nf * c->G;
     e.base = 0;
@@ -1077,7 +1106,7 @@ inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf, int nq_items)
     // the cold pool's size is known on the device only: items for all C slots
     const int ncold_max = c->cold > 0 ? c->cold : 0;
     e.Sf = (e.ntail + e.npool + ncold_max + FP16_CHUNK - 1) / FP16_CHUNK;
-    e.Iu = e.Sf + nq_items;
+    e.Iu = e.Sf + nq_blocks * ipb;
     return e;
 }
 
@@ -1112,11 +1141,26 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     a.G = c->G;
     a.B = c->B;
     a.jfull = (c->P + c->G - 1) / c->G;   // from this block on, the pool is full
+    a.CPB = chunks_per_block(c->G);
+    // Work items: chunks, so that equal item counts are nearly equal work
+    // (the last item of a warp is a small share of it, and per-SM speed
+    // differences even out); with fewer blocks than decode warps, whole
+    // blocks, so that each warp's fixed cost (queries, block header) is paid
+    // once per block.
+    long long nblk = 0;
+    if constexpr (RG) {
+        for (int b = 0; b < c->B; ++b)
+            nblk += (long long)c->Hkv * (TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b]);
+    } else {
+        nblk = (long long)c->U * (TK ? (c->nf < Kc ? c->nf : Kc) : c->nf);
+    }
+    const long long nwarps = (long long)c->sm_count * DEC_WARPS;
+    a.IPB = nblk >= nwarps ? a.CPB : 1;
     TableT<RG> st;
     if constexpr (RG) {
         long long base = 0;
         for (int b = 0; b < c->B; ++b) {
-            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b]);
+            st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b], a.IPB);
             st.e[b].base = base;
             base += (long long)c->Hkv * st.e[b].Iu;
         }
@@ -1126,7 +1170,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
         a.nf = a.ntail = a.npool = a.ring_start = a.Sf = a.Iu = 0;   // per sequence in the table
         a.MAXU = c->maxu_r;
     } else {
-        const SeqEntry e = seq_entry(c, c->T, c->nf, TK ? Kc : c->nf);
+        const SeqEntry e = seq_entry(c, c->T, c->nf, TK ? Kc : c->nf, a.IPB);
         a.nf = e.nf;
         a.ring_start = e.ring_start;
         a.ntail = e.ntail;

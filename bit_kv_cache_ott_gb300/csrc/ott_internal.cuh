@@ -55,7 +55,7 @@ namespace ott {
 constexpr int TILE = 16;          // token slots per tile
 constexpr int CHUNK_TILES = 4;    // tiles per staged chunk in the decode kernel
 constexpr int DEC_WARPS = 16;     // warps per decode CTA
-constexpr int FP16_CHUNK = 32;    // fp16 tokens per decode split (one per lane)
+constexpr int FP16_CHUNK = 16;    // fp16 tokens per decode work item
 constexpr int RAGGED_MAX = 256;   // sequences in a cache whose sequences may differ in length
 
 __host__ __device__ constexpr int ksz_bytes(int d) { return 4 * d; }
@@ -65,6 +65,10 @@ __host__ __device__ constexpr int tile_v_off(int d) { return 4 * d; }
 __host__ __device__ constexpr int tile_sz_off(int d) { return 8 * d; }
 __host__ __device__ constexpr int stage_bytes(int d) { return ksz_bytes(d) + CHUNK_TILES * tile_bytes(d); }
 __host__ __device__ inline int ntiles_of(int G) { return (G + TILE - 1) / TILE; }
+// quantized decode work items per block: chunks of CHUNK_TILES tiles
+__host__ __device__ inline int chunks_per_block(int G) {
+    return (G + CHUNK_TILES * TILE - 1) / (CHUNK_TILES * TILE);
+}
 __host__ __device__ inline long long block_bytes_of(int d, int G) {
     return ksz_bytes(d) + (long long)ntiles_of(G) * tile_bytes(d);
 }

@@ -318,6 +318,17 @@ long long ott_device_bytes(const ott_cache *c);
 /* Static text for a status code. */
 const char *ott_status_str(int code);
 
+/*
+ * Measurement helper (not part of the method): copy `bytes` from src to dst,
+ * both DEVICE pointers, 16-byte aligned, bytes a multiple of 16, ranges not
+ * overlapping, with a plain streaming copy kernel on `stream`. A caller times
+ * it to measure the HBM bandwidth this GPU sustains (read + write bytes over
+ * the elapsed time), the denominator of the decode kernel's roofline
+ * fraction, in the same process as the decode timing. Errors:
+ * OTT_ERR_INVALID for a bad argument, OTT_ERR_CUDA if the launch fails.
+ */
+int ott_hbm_copy(void *dst, const void *src, long long bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

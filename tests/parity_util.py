@@ -7,6 +7,9 @@ within max |d| <= 2e-3 and mean |d| <= 2e-4 of the oracle's double result.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -39,3 +42,21 @@ def compare_out(out_gpu: torch.Tensor, ref: np.ndarray, where: str = ""):
     mx, mean = float(d.max()), float(d.mean())
     assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{where}: max|d|={mx:.3e} mean|d|={mean:.3e}"
     return mx, mean
+
+
+def oracle_decode_all(orc, q, threads: int | None = None) -> np.ndarray:
+    """The oracle's decode of every (sequence, query head), [B][Hq][d] float64,
+    one head per call spread over host threads (the oracle's C call releases
+    the interpreter lock and only reads the cache)."""
+    B, Hq = q.shape[0], q.shape[1]
+    out = np.zeros((B, Hq, q.shape[2]), np.float64)
+    pairs = [(b, h) for b in range(B) for h in range(Hq)]
+
+    def one(bh):
+        b, h = bh
+        out[b, h] = orc.decode_head(b, h, q[b, h])
+
+    n = threads or min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(one, pairs))
+    return out
