@@ -447,43 +447,60 @@ def run_ours(args, w):
     ms = max_over_ranks(ms, dev)
     s_next = W_steps + K_steps
 
-    # One flush cycle (G steps) after the timed region, each append and each
-    # decode call bracketed by its own events on the launch stream:
-    #  * the roofline: the decode call's bytes and time averaged over a whole
-    #    flush cycle (its bytes fall as the fp16 residual empties at a flush);
-    #  * the flush: the append that flushes against the median plain append.
-    #    The flush runs once every G steps for a batch of equal lengths, so K
+    # One flush cycle (G steps) after the timed region:
+    #  * the flush: every append is bracketed by its own events, and the
+    #    append that flushes is compared with the median plain append. The
+    #    flush runs once every G steps for a batch of equal lengths, so K
     #    timed steps rarely hold their share of it; `value` charges it at its
     #    rate, one flush per G steps. A ragged batch flushes its sequences at
     #    different steps, so its timed steps already hold their share.
-    n_dec = w.G
-    app_ev, dec_ev, app_due, dec_bytes_list = [], [], [], []
-    for i in range(n_dec):
+    #  * the roofline: at 8 points spread over the cycle (the decode call's
+    #    bytes fall as the fp16 residual empties at a flush), 8 decode calls
+    #    back to back between one pair of events; with an L2 flush between
+    #    calls, each call has its own events. Bytes and time are summed over
+    #    every timed call.
+    n_pts, per_pt = 8, 8
+    pt_every = max(1, w.G // n_pts)
+    app_ev, app_due, dec_groups = [], [], []
+    for i in range(w.G):
         k, v, q = dev_in[s_next % n_distinct]
         due = flush_due_next(Ts)
         Ts = [t + 1 for t in Ts]
         ea = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        ed = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         ea[0].record(stream)
         for c in caches:
             c.append(k, v, stream)
         ea[1].record(stream)
-        flush_l2(i)
-        ed[0].record(stream)
-        for c in caches:
-            decode_call(c, w, q, out, stream)
-        ed[1].record(stream)
         app_ev.append(ea)
-        dec_ev.append(ed)
         app_due.append(due)
-        if not cold:
-            dec_bytes_list.append(step_bytes(w, list(Ts)) * w.layers)
         s_next += 1
+        if i % pt_every == 0 and len(dec_groups) < n_pts:
+            evs = []
+            if l2_flush:
+                for j in range(per_pt):
+                    flush_l2(j)
+                    ed = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    ed[0].record(stream)
+                    for c in caches:
+                        decode_call(c, w, q, out, stream)
+                    ed[1].record(stream)
+                    evs.append(ed)
+            else:
+                ed = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ed[0].record(stream)
+                for j in range(per_pt):
+                    for c in caches:
+                        decode_call(c, w, q, out, stream)
+                ed[1].record(stream)
+                evs.append(ed)
+            call_bytes = (step_bytes(w, list(Ts)) * w.layers if not cold else
+                          sum(metrics.hot_bytes(Ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) + cold_quant_bytes(c)
+                              for c in caches))
+            dec_groups.append((evs, call_bytes))
     torch.cuda.synchronize()
-    dec_ms = sum(a_.elapsed_time(b_) for a_, b_ in dec_ev)
-    if cold:   # block and cold-pool sizes (they depend on the data) read once, after the cycle
-        dec_bytes_list = [sum(metrics.hot_bytes(Ts[0], w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P) + cold_quant_bytes(c)
-                              for c in caches)] * n_dec
+    n_dec = n_pts * per_pt
+    dec_ms = sum(a_.elapsed_time(b_) for evs, _ in dec_groups for a_, b_ in evs)
+    dec_bytes_list = [cb for _, cb in dec_groups for _ in range(per_pt)]
     dec_call_bytes = sum(dec_bytes_list) / n_dec
     flush_us = None
     if not w.ragged:
@@ -613,9 +630,10 @@ def run_ours(args, w):
                          "pct_of_nominal_8000": 100.0 * achieved / 8000.0,
                          "kernel": ("k_topk_bounds + k_topk_pick + k_decode + k_combine (ott_decode_attn_topk)" if w.topk > 0
                                     else "k_decode + k_combine (ott_decode_attn)"),
-                         "timing": f"{n_dec} decode calls over one flush cycle after the timed steps "
-                                   "(one per step, after that step's append), CUDA events around each call on "
-                                   "the launch stream; bytes averaged over the same calls",
+                         "timing": (f"{n_dec} decode calls at 8 points of one flush cycle after the timed steps, "
+                                    f"{per_pt} back to back per point between CUDA events on the launch stream"
+                                    + (" (each call with its own events, L2 flushed between calls)" if l2_flush else "")
+                                    + "; bytes of each call by its point's token counts"),
                          "algorithmic_bytes_per_launch": dec_call_bytes / w.layers,
                          "traffic": recorded_traffic(w.name)},
             "clocks": clk.summary(),

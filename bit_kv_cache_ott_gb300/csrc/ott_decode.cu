@@ -401,6 +401,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
     float zs[NZ];
 #pragma unroll
     for (int v = 0; v < NZ; ++v) zs[v] = 0.0f;
+    float2 zs2 = make_float2(0.0f, 0.0f);   // one variant: the lane's two tokens, kept apart until the end
     // running max and sum of the head this lane's score columns hold
     float m_run = -CUDART_INF_F, l_run = 0.0f;
     uint32_t Bk[NKT][2];
@@ -448,24 +449,23 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                 float2 xs[GQ][NPAIR];
 #pragma unroll
                 for (int h = 0; h < GQ; ++h) {
-                    float amax = 0.0f, qz = 0.0f;
+                    float amax = 0.0f;
+                    float2 qz2 = make_float2(0.0f, 0.0f);
 #pragma unroll
                     for (int m = 0; m < NPAIR; ++m) {
                         const uint2 sz2 = *reinterpret_cast<const uint2 *>(ksz + 2 * lane + 64 * m);
                         const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.x));
                         const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.y));
                         const float2 qv = *reinterpret_cast<const float2 *>(qsm + h * D + 2 * lane + 64 * m);
-                        xs[h][m].x = qv.x * e0.x;
-                        xs[h][m].y = qv.y * e1.x;
-                        qz = fmaf(qv.x, e0.y, qz);
-                        qz = fmaf(qv.y, e1.y, qz);
+                        xs[h][m] = __fmul2_rn(qv, make_float2(e0.x, e1.x));
+                        qz2 = __ffma2_rn(qv, make_float2(e0.y, e1.y), qz2);
                         amax = fmaxf(amax, fmaxf(fabsf(xs[h][m].x), fabsf(xs[h][m].y)));
                     }
+                    // |x| >= 0 orders like its bits: one warp max-reduce on them
+                    amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+                    float qz = qz2.x + qz2.y;
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                        qz += __shfl_xor_sync(0xffffffffu, qz, o);
-                    }
+                    for (int o = 16; o > 0; o >>= 1) qz += __shfl_xor_sync(0xffffffffu, qz, o);
                     const int E = amax > 0.0f ? min(max(14 - (((__float_as_int(amax) >> 23) & 0xff) - 127), -100), 100) : 0;
                     Eh[h] = E;
                     qzh[h] = qz;
@@ -473,10 +473,12 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
 #pragma unroll
                     for (int m = 0; m < NPAIR; ++m) {
                         const float sc = sE * clsf[m];
-                        const float x0 = xs[h][m].x * sc, x1 = xs[h][m].y * sc;
+                        const float2 x = __fmul2_rn(xs[h][m], make_float2(sc, sc));
+                        const float x0 = x.x, x1 = x.y;
                         const __half2 hi = __floats2half2_rn(x0, x1);
                         const float2 hf = __half22float2(hi);
-                        const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                        const float2 l2 = __ffma2_rn(hf, make_float2(-1.0f, -1.0f), x);
+                        const __half2 lo = __floats2half2_rn(l2.x, l2.y);
                         const int ch = 2 * lane + 64 * m;
                         *reinterpret_cast<__half2 *>(qhl + (h * 2 + 0) * (D + 8) + ch) = hi;
                         *reinterpret_cast<__half2 *>(qhl + (h * 2 + 1) * (D + 8) + ch) = lo;
@@ -583,9 +585,17 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
             float mraw = -CUDART_INF_F;
 #pragma unroll
             for (int tau = 0; tau < CHUNK_TILES; ++tau) mraw = fmaxf(mraw, fmaxf(sc[tau][0], sc[tau][1]));
-            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 4));
-            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 8));
-            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
+            if constexpr (GQ == 1) {
+                // every lane scores the one head: a whole-warp max-reduce on
+                // order-preserving integer keys (-inf included)
+                const int kb = __float_as_int(mraw);
+                const int key = __reduce_max_sync(0xffffffffu, kb >= 0 ? kb : kb ^ 0x7fffffff);
+                mraw = __int_as_float(key >= 0 ? key : key ^ 0x7fffffff);
+            } else {
+                mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 4));
+                mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 8));
+                mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
+            }
             const float m_new = fmaxf(m_run, fmaf(mraw, c1, c0));
             if (__any_sync(0xffffffffu, m_new > m_run)) {
                 const float alpha = m_new > m_run ? ex2(m_run - m_new) : 1.0f;
@@ -598,6 +608,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                 const float aZ = __shfl_sync(0xffffffffu, alpha, hV);
 #pragma unroll
                 for (int v = 0; v < NZ; ++v) zs[v] *= aZ;
+                zs2 = __fmul2_rn(zs2, make_float2(aZ, aZ));
                 m_run = m_new;
             }
             const float c0m = c0 - (m_run == -CUDART_INF_F ? 0.0f : m_run);
@@ -610,7 +621,9 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                 for (int v = 0; v < NV; ++v) bv[tau][v][0] = bv[tau][v][1] = 0u;
                 if (FULL || tau < nt) {
                     const uint8_t *tb = stage + KSZ + tau * TB;
-                    const float p0 = ex2(fmaf(sc[tau][0], c1, c0m)), p1 = ex2(fmaf(sc[tau][1], c1, c0m));
+                    const float2 lgp = __ffma2_rn(make_float2(sc[tau][0], sc[tau][1]), make_float2(c1, c1),
+                                                  make_float2(c0m, c0m));
+                    const float p0 = ex2(lgp.x), p1 = ex2(lgp.y);
                     l_run += p0 + p1;
                     if constexpr (SPLIT) {
                         const float pa = __shfl_sync(0xffffffffu, p0, src0);
@@ -627,16 +640,19 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                             const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
                             const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.z));
                             const float2 e3 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.w));
-                            const float x0 = pa * e0.x, x1 = pb * e1.x, x2 = pc * e2.x, x3 = pd * e3.x;
-                            zs[k] = fmaf(pa, e0.y, zs[k]);
-                            zs[k] = fmaf(pb, e1.y, zs[k]);
-                            zs[k] = fmaf(pc, e2.y, zs[k]);
-                            zs[k] = fmaf(pd, e3.y, zs[k]);
-                            const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+                            const float2 pab = make_float2(pa, pb), pcd = make_float2(pc, pd);
+                            const float2 x01 = __fmul2_rn(pab, make_float2(e0.x, e1.x));
+                            const float2 x23 = __fmul2_rn(pcd, make_float2(e2.x, e3.x));
+                            float2 zk = __fmul2_rn(pab, make_float2(e0.y, e1.y));
+                            zk = __ffma2_rn(pcd, make_float2(e2.y, e3.y), zk);
+                            zs[k] += zk.x + zk.y;
+                            const __half2 h01 = __floats2half2_rn(x01.x, x01.y), h23 = __floats2half2_rn(x23.x, x23.y);
                             const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                            const float2 l01 = __ffma2_rn(f01, make_float2(-1.0f, -1.0f), x01);
+                            const float2 l23 = __ffma2_rn(f23, make_float2(-1.0f, -1.0f), x23);
                             const uint32_t hi0 = h2bits(h01), hi1 = h2bits(h23);
-                            const uint32_t lo0 = h2bits(__floats2half2_rn(x0 - f01.x, x1 - f01.y));
-                            const uint32_t lo1 = h2bits(__floats2half2_rn(x2 - f23.x, x3 - f23.y));
+                            const uint32_t lo0 = h2bits(__floats2half2_rn(l01.x, l01.y));
+                            const uint32_t lo1 = h2bits(__floats2half2_rn(l23.x, l23.y));
                             const uint32_t own0 = lo_lane ? lo0 : hi0, own1 = lo_lane ? lo1 : hi1;
                             const uint32_t got0 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi0 : lo0, 4);
                             const uint32_t got1 = __shfl_xor_sync(0xffffffffu, lo_lane ? hi1 : lo1, 4);
@@ -656,11 +672,13 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                             tb + tile_sz_off(D) + (((gamma * 4 + i) * 4) + (lo_lane ? 2 : 0)) * 4);
                         const float2 ea = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
                         const float2 eb = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                        const float xA = pA * ea.x, xB = pB * eb.x;
-                        if (gv) zs[0] = fmaf(pB, eb.y, fmaf(pA, ea.y, zs[0]));
-                        const __half2 h = __floats2half2_rn(xA, xB);
+                        const float2 pAB = make_float2(pA, pB);
+                        const float2 x = __fmul2_rn(pAB, make_float2(ea.x, eb.x));
+                        if (gv) zs2 = __ffma2_rn(pAB, make_float2(ea.y, eb.y), zs2);
+                        const __half2 h = __floats2half2_rn(x.x, x.y);
                         const float2 f = __half22float2(h);
-                        const uint32_t hi = h2bits(h), lo = h2bits(__floats2half2_rn(xA - f.x, xB - f.y));
+                        const float2 l2 = __ffma2_rn(f, make_float2(-1.0f, -1.0f), x);
+                        const uint32_t hi = h2bits(h), lo = h2bits(__floats2half2_rn(l2.x, l2.y));
                         // hi lane: keeps hi of (2i, 2i+1), gets hi of (2i+8, 2i+9); lo lane the lo pieces
                         const uint32_t got = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 4);
                         bv[tau][0][0] = gv ? (lo_lane ? got : hi) : 0u;
@@ -705,6 +723,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
     }
 
     // epilogue: reduce l over r and the z-sums over i, write the partials
+    if constexpr (!SPLIT) zs[0] += zs2.x + zs2.y;
     float l = l_run;
     l += __shfl_xor_sync(0xffffffffu, l, 4);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
