@@ -40,7 +40,7 @@ class StateExport(C.Structure):
 SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_paged", "ott_release_seq", "ott_prefill_seq",
            "ott_free_blocks", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
            "ott_decode_attn", "ott_decode_attn_static", "ott_decode_attn_topk", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
-           "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str", "ott_hbm_copy")
+           "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str", "ott_hbm_copy", "ott_ex2_probe")
 
 
 def lib_path() -> str:
@@ -85,6 +85,7 @@ def load(build_if_missing: bool = False):
     L.ott_status_str.argtypes = [i32]
     L.ott_status_str.restype = C.c_char_p
     L.ott_hbm_copy.argtypes = [P, P, i64, P]
+    L.ott_ex2_probe.argtypes = [P, P, i32, P]
     _lib = L
     return L
 

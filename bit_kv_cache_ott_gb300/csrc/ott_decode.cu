@@ -1301,6 +1301,23 @@ cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cuda
 
 }  // namespace ott
 
+// ---------------------------------------------------------------- diagnostics
+namespace ott {
+namespace {
+__global__ void k_ex2_probe(const float *x, float *y, int n) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) y[e] = ex2(x[e]);
+}
+}  // namespace
+}  // namespace ott
+
+extern "C" int ott_ex2_probe(const float *x, float *y, int n, void *stream) {
+    if (!x || !y || n < 0) return OTT_ERR_INVALID;
+    if (n == 0) return OTT_OK;
+    const int blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    ott::k_ex2_probe<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+    return cudaGetLastError() == cudaSuccess ? OTT_OK : OTT_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- allocation-free decode
 //
 // ott_decode_attn_static: the same two kernels as ott_decode_attn, but the
@@ -1309,6 +1326,8 @@ cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cuda
 // allocate device memory on their decode path: engines that hand all free HBM
 // to their own pool at start-up and forbid any later growth, or latency-
 // critical loops that cannot afford cudaMalloc's implicit synchronization.
+#include <cuda.h>
+
 #include <mutex>
 
 namespace ott {
@@ -1324,20 +1343,60 @@ static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 namespace {
 
 std::mutex g_static_mu;
-float *g_static_ptr[1024];   // host copy of the array's device address, per device ordinal
+// Host copy of the array's device address per device ordinal, with the id of
+// the context it was taken in: after a device reset the module is loaded
+// again in a new context, where the array may sit elsewhere, so the address
+// is taken again.
+struct StaticAddr {
+    float *ptr;
+    unsigned long long ctx;
+};
+StaticAddr g_static_addr[1024];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// The current context's unique id (0 if the driver cannot tell); called
+// under g_static_mu.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+            get_id = reinterpret_cast<CtxGetIdFn>(f2);
+        }
+        cudaGetLastError();
+        resolved = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 
 // The array's name is only a host-side stand-in in host code: its device
-// address is looked up once per device, with that device current.
+// address is looked up with the device current, once per device (and again
+// in a new context after a device reset).
 cudaError_t static_scratch_address(int dev, float **out) {
     if (dev < 0 || dev >= 1024) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    StaticAddr &sa = g_static_addr[dev];
+    if (!sa.ptr || sa.ctx != ctx) {
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return e;
-        g_static_ptr[dev] = static_cast<float *>(p);
+        sa.ptr = static_cast<float *>(p);
+        sa.ctx = ctx;
     }
-    *out = g_static_ptr[dev];
+    *out = sa.ptr;
     return cudaSuccess;
 }
 

@@ -213,7 +213,8 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
  * an allocation. The paper has no counterpart; this is a deployment variant.
  *   - The first call on a device looks up the array's device address (with
  *     the cache's device current); make that first call before any stream
- *     capture.
+ *     capture. After a device reset (a new context) the next call looks it
+ *     up again; caches created before the reset are gone with it.
  *   - Every call shares the array. Calls that overlap on the GPU (other
  *     streams, other handles) race on it; order them (same stream or events).
  *     Nothing in it needs clearing between calls.
@@ -328,6 +329,16 @@ const char *ott_status_str(int code);
  * OTT_ERR_INVALID for a bad argument, OTT_ERR_CUDA if the launch fails.
  */
 int ott_hbm_copy(void *dst, const void *src, long long bytes, void *stream);
+
+/*
+ * Diagnostic (not part of the method): y[i] = 2^x[i] for n DEVICE floats,
+ * computed with the same device exponential the decode kernel uses for its
+ * softmax weights (the hardware approximation, subnormal results flushed to
+ * zero), so that its error against an exact 2^x can be measured. Errors:
+ * OTT_ERR_INVALID for a NULL pointer or n < 0, OTT_ERR_CUDA if the launch
+ * fails.
+ */
+int ott_ex2_probe(const float *x, float *y, int n, void *stream);
 
 #ifdef __cplusplus
 }
