@@ -53,6 +53,8 @@ def lib():
             L.orc_create.argtypes = [i32] * 7
             L.orc_create_policy.restype = P
             L.orc_create_policy.argtypes = [i32] * 8
+            L.orc_create_pct.restype = P
+            L.orc_create_pct.argtypes = [i32] * 9
             L.orc_export_cold.argtypes = [P, i32, P, P, P]
             L.orc_topk_select.argtypes = [P, i32, i32, P, i32, P, P]
             L.orc_release_seq.argtypes = [P, i32]
@@ -135,12 +137,20 @@ class OracleCache:
     """The oracle's OTT cache: same create/prefill/append/decode calls as the library.
 
     ``cold=None`` writes displaced pool tokens back into the new block;
-    ``cold=C`` (an int >= 0) is the cold-pool policy with capacity C."""
+    ``cold=C`` (an int >= 0) is the cold-pool policy with capacity C.
+    ``pct=(p, n_oc)`` selects the channel-conditioned outlier criterion: p in
+    units of 1/10000, n_oc outlier channels per flush (written back)."""
 
-    def __init__(self, B, Hq, Hkv, d, G, R, P, cold=None):
+    def __init__(self, B, Hq, Hkv, d, G, R, P, cold=None, pct=None):
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
         self.cold = cold
-        self._h = lib().orc_create_policy(B, Hq, Hkv, d, G, R, P, -1 if cold is None else int(cold))
+        self.pct = pct
+        if pct is not None:
+            if cold is not None:
+                raise ValueError("the criterion and the cold-pool policy do not combine")
+            self._h = lib().orc_create_pct(B, Hq, Hkv, d, G, R, P, int(pct[0]), int(pct[1]))
+        else:
+            self._h = lib().orc_create_policy(B, Hq, Hkv, d, G, R, P, -1 if cold is None else int(cold))
         if not self._h:
             raise ValueError("invalid OTT shape")
 

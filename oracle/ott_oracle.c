@@ -72,6 +72,18 @@
  *      taken in fp32 (products, 3*s and z + 3*s rounded to nearest, summed
  *      in channel order); the block's bound is the largest over the query
  *      heads that share the kv head. A selected block is attended whole.
+ *  R14 The channel-conditioned criterion ([blog] sec. 3.1: a candidate is an
+ *      outlier when it lies in an outlier channel and its magnitude is among
+ *      the globally smallest p%), a policy beside R4: at a flush, over the
+ *      candidates (pool plus group), the outlier channels are the n_oc
+ *      channels with the largest max |k| over the candidates (ties to the
+ *      lower channel index); each candidate's score is its squared norm over
+ *      those channels only (fp32, ascending channel order); the smallest
+ *      m = ceil(p * ncand) scores (ties to the lower token index) are the
+ *      outliers, p given in units of 1/10000 so that m is exact; the pool
+ *      keeps the min(P, m) most outlying of them, and every other candidate
+ *      joins the new block (written back). Pool sizes, and so block sizes,
+ *      follow from p, P and G alone: the same for every unit.
  *
  * Floating point: decisions that yield integers or stored bits (norms,
  * scales, zeros, codes) are taken in fp32 exactly as the library takes them.
@@ -245,6 +257,8 @@ typedef struct {
     long long T;        /* appends plus the longest prefill (0: empty) */
     long long *Tb;      /* [B] tokens seen by each sequence (R10) */
     int C;              /* cold-pool capacity (R11); -1: displaced tokens are written back */
+    int pct;            /* R14: p in units of 1/10000; -1: the norm criterion of R4 */
+    int n_oc;           /* R14: outlier channels per flush */
     orc_unit *u;        /* [B*Hkv] */
 } orc_cache;
 
@@ -301,6 +315,8 @@ void *orc_create_policy(int B, int Hq, int Hkv, int d, int G, int R, int P, int 
     orc_cache *h = (orc_cache *)calloc(1, sizeof(orc_cache));
     h->B = B; h->Hq = Hq; h->Hkv = Hkv; h->d = d; h->G = G; h->R = R; h->P = P;
     h->C = C < 0 ? -1 : C;
+    h->pct = -1;
+    h->n_oc = 0;
     h->u = (orc_unit *)calloc((size_t)B * Hkv, sizeof(orc_unit));
     h->Tb = (long long *)calloc((size_t)B, sizeof(long long));
     for (int i = 0; i < B * Hkv; ++i) {
@@ -325,6 +341,58 @@ void *orc_create_policy(int B, int Hq, int Hkv, int d, int G, int R, int P, int 
 void *orc_create(int B, int Hq, int Hkv, int d, int G, int R, int P)
 {
     return orc_create_policy(B, Hq, Hkv, d, G, R, P, -1);
+}
+
+/* R14: the channel-conditioned outlier criterion with p = pct / 10000 and
+ * n_oc outlier channels; displaced pool tokens are written back. */
+void *orc_create_pct(int B, int Hq, int Hkv, int d, int G, int R, int P, int pct, int n_oc)
+{
+    if (pct < 0 || pct > 10000 || n_oc < 1 || n_oc > d)
+        return NULL;
+    orc_cache *h = (orc_cache *)orc_create_policy(B, Hq, Hkv, d, G, R, P, -1);
+    if (h) {
+        h->pct = pct;
+        h->n_oc = n_oc;
+    }
+    return h;
+}
+
+/* R14, step 1: the n_oc channels with the largest max |k| over the
+ * candidates, ties to the lower channel index; out[0..n_oc) ascending. */
+static void outlier_channels(const orc_cand *cand, int ncand, int d, int n_oc, int *out)
+{
+    float *amax = (float *)calloc(d, sizeof(float));
+    char *taken = (char *)calloc(d, 1);
+    for (int c = 0; c < d; ++c)
+        for (int t = 0; t < ncand; ++t) {
+            float a = fabsf(orc_h2f(cand[t].k[c]));
+            if (a > amax[c])
+                amax[c] = a;
+        }
+    for (int n = 0; n < n_oc; ++n) {     /* pick the largest remaining, lower index first */
+        int best = -1;
+        for (int c = 0; c < d; ++c)
+            if (!taken[c] && (best < 0 || amax[c] > amax[best]))
+                best = c;
+        taken[best] = 1;
+    }
+    int n = 0;
+    for (int c = 0; c < d; ++c)
+        if (taken[c])
+            out[n++] = c;
+    free(amax);
+    free(taken);
+}
+
+/* R14, step 2: squared norm over the chosen channels (fp32, ascending). */
+static float outlier_channel_norm(const uint16_t *k, const int *oc, int n_oc)
+{
+    float s = 0.0f;
+    for (int n = 0; n < n_oc; ++n) {
+        float kc = orc_h2f(k[oc[n]]);
+        s = s + kc * kc;
+    }
+    return s;
 }
 
 /* R11: the displaced pool tokens ev[0..n) (ascending token order) enter the
@@ -370,9 +438,22 @@ static void flush_unit(orc_cache *h, orc_unit *u)
         c->from_pool = 0;
         c->norm = orc_norm(c->k, d);
     }
-    /* R4: order by (norm, index); the first P stay in the pool. */
+    int keep = ncand < P ? ncand : P;
+    if (h->pct >= 0) {
+        /* R14: scores over the outlier channels for every candidate (the
+         * channels depend on this flush's candidates, so old pool tokens are
+         * scored again); the smallest ceil(p * ncand) are the outliers. */
+        int *oc = (int *)malloc(sizeof(int) * h->n_oc);
+        outlier_channels(cand, ncand, d, h->n_oc, oc);
+        for (int t = 0; t < ncand; ++t)
+            cand[t].norm = outlier_channel_norm(cand[t].k, oc, h->n_oc);
+        free(oc);
+        const int m = (int)(((long long)h->pct * ncand + 9999) / 10000);
+        if (m < keep)
+            keep = m;
+    }
+    /* R4: order by (norm, index); the first `keep` stay in the pool. */
     qsort(cand, ncand, sizeof(orc_cand), cand_cmp_norm);
-    const int keep = ncand < P ? ncand : P;
     int c = ncand - keep;
     /* R5: the rest, in token order, become the new block. */
     qsort(cand + keep, c, sizeof(orc_cand), cand_cmp_idx);

@@ -89,3 +89,43 @@ def unpack_rows(packed: np.ndarray, d: int) -> np.ndarray:
     sh = np.array([0, 2, 4, 6], np.uint8)
     codes = (packed[..., :, None] >> sh) & 3
     return codes.reshape(*packed.shape[:-1], d)
+
+
+def state_pct(keys16: np.ndarray, G: int, R: int, P: int, pct: int, n_oc: int):
+    """Membership under the channel-conditioned criterion after T appends,
+    restated with numpy (blocks, pool, tail, pool scores).
+
+    At each flush the candidates are the pool and the group; the outlier
+    channels are the n_oc channels with the largest max |k| over them (ties
+    to the lower channel); a candidate's score is its fp32 squared norm over
+    those channels in ascending channel order; the pool keeps the
+    min(P, ceil(pct * n / 10000)) smallest (score, index) pairs; every other
+    candidate joins the block, in token order."""
+    T = len(keys16)
+    nf = flush_count(T, G, R)
+    pool: list[int] = []
+    blocks = []
+    scores = {}
+    for j in range(nf):
+        cand = pool + list(range(j * G, (j + 1) * G))
+        a = np.abs(keys16[cand].astype(np.float32)).max(axis=0)
+        order = np.lexsort((np.arange(a.size), -a))          # largest first, lower channel on ties
+        oc = np.sort(order[:n_oc])
+        sq = keys16[cand][:, oc].astype(np.float32) ** 2
+        sc = np.add.accumulate(sq, axis=1, dtype=np.float32)[:, -1]
+        ranked = sorted(range(len(cand)), key=lambda x: (float(sc[x]), cand[x]))
+        m = -(-pct * len(cand) // 10000)
+        keep = min(P, m)
+        pool = [cand[x] for x in ranked[:keep]]
+        scores = {cand[x]: sc[x] for x in ranked[:keep]}
+        blocks.append(sorted(cand[x] for x in ranked[keep:]))
+    return blocks, sorted(pool), list(range(nf * G, T)), scores
+
+
+def pct_pool_sizes(nf: int, G: int, P: int, pct: int) -> list[int]:
+    """Pool size after each flush: min(P, ceil(pct * (previous + G) / 10000))."""
+    out, prev = [], 0
+    for _ in range(nf):
+        prev = min(P, -(-pct * (prev + G) // 10000))
+        out.append(prev)
+    return out
