@@ -38,7 +38,7 @@ class StateExport(C.Structure):
 
 
 SYMBOLS = ("ott_create", "ott_create_ragged", "ott_create_paged", "ott_release_seq", "ott_prefill_seq",
-           "ott_free_blocks", "ott_create_cold", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
+           "ott_free_blocks", "ott_create_cold", "ott_create_pct", "ott_export_cold", "ott_destroy", "ott_prefill", "ott_prefill_lens", "ott_append",
            "ott_decode_attn", "ott_decode_attn_static", "ott_decode_attn_topk", "ott_get_counts", "ott_get_seq_counts", "ott_block_count",
            "ott_export_state", "ott_check_device", "ott_device_bytes", "ott_status_str", "ott_hbm_copy", "ott_ex2_probe")
 
@@ -62,6 +62,7 @@ def load(build_if_missing: bool = False):
     L.ott_create.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_create_ragged.argtypes = [i32] * 8 + [C.POINTER(P)]
     L.ott_create_cold.argtypes = [i32] * 9 + [C.POINTER(P)]
+    L.ott_create_pct.argtypes = [i32] * 10 + [C.POINTER(P)]
     L.ott_create_paged.argtypes = [i32] * 8 + [i64, C.POINTER(P)]
     L.ott_release_seq.argtypes = [P, i32, P]
     L.ott_prefill_seq.argtypes = [P, i32, P, P, i32, P]
@@ -129,10 +130,12 @@ class OTTCache:
     ``ragged=True`` creates it with ``ott_create_ragged`` so that ``prefill_lens``
     can give every sequence its own length. ``cold=C`` creates it with
     ``ott_create_cold``: displaced pool tokens go to a first-in-first-out
-    fp16 cold pool of C slots instead of the new block."""
+    fp16 cold pool of C slots instead of the new block. ``pct=(p, n_oc)``
+    creates it with ``ott_create_pct``: the channel-conditioned outlier
+    criterion, p in units of 1/10000 over n_oc outlier channels."""
 
     def __init__(self, B, Hq, Hkv, d, G=128, R=32, P=32, max_tokens=8192, ragged=False, cold=None,
-                 pool_blocks=None):
+                 pool_blocks=None, pct=None):
         L = load()
         self.B, self.Hq, self.Hkv, self.d, self.G, self.R, self.P = B, Hq, Hkv, d, G, R, P
         self.max_tokens = max_tokens
@@ -143,6 +146,11 @@ class OTTCache:
             self.ragged = True
             _check(L.ott_create_paged(B, Hq, Hkv, d, G, R, P, max_tokens, int(pool_blocks), C.byref(h)),
                    "ott_create_paged")
+        elif pct is not None:
+            if ragged or cold is not None:
+                raise ValueError("the channel criterion takes sequences of one length and writes tokens back")
+            _check(L.ott_create_pct(B, Hq, Hkv, d, G, R, P, int(pct[0]), int(pct[1]), max_tokens, C.byref(h)),
+                   "ott_create_pct")
         elif cold is not None:
             if ragged:
                 raise ValueError("the cold-pool policy takes sequences of one length")

@@ -35,7 +35,7 @@ bool flush_due_seq(const ott_cache *c, int b) {
 int flushes_after(const ott_cache *c, long long T) { return T >= c->G + c->R ? (int)((T - c->R) / c->G) : 0; }
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 int cold, ott_cache **out, long long pool_blocks = 0);
+                 int cold, ott_cache **out, long long pool_blocks = 0, int pct = -1, int n_oc = 0);
 
 // Paged pool: blocks that flushes of these sequences (group j of sequence b
 // for j in [nf_from[b], nf_to[b])) need. 0 for a cache without the pool.
@@ -96,6 +96,15 @@ int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C, i
     return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, C, out);
 }
 
+int ott_create_pct(int B, int Hq, int Hkv, int d, int G, int R, int P, int pct, int n_oc, int max_tokens,
+                   ott_cache **out) {
+    if (pct < 0 || pct > 10000 || n_oc < 1 || n_oc > d) {
+        if (out) *out = nullptr;
+        return OTT_ERR_INVALID;
+    }
+    return create_cache(B, Hq, Hkv, d, G, R, P, max_tokens, 0, -1, out, 0, pct, n_oc);
+}
+
 int ott_create_paged(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, long long pool_blocks,
                      ott_cache **out) {
     if (B > RAGGED_MAX || pool_blocks < 1 || pool_blocks > 0x7fffffffLL) {
@@ -118,7 +127,7 @@ int ott_create_ragged(int B, int Hq, int Hkv, int d, int G, int R, int P, int ma
 namespace {
 
 int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tokens, int ragged,
-                 int cold, ott_cache **out, long long pool_blocks) {
+                 int cold, ott_cache **out, long long pool_blocks, int pct, int n_oc) {
     if (!out) return OTT_ERR_INVALID;
     *out = nullptr;
     if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
@@ -180,9 +189,11 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t sz_pn = U * (size_t)P * 4;
     const size_t sz_part = (size_t)nwarps * maxu_alloc * 2 * gq * (d + 2) * 4;
     c->cold = cold;
+    c->pct = pct;
+    c->n_oc = n_oc;
     const size_t Cs = cold > 0 ? (size_t)cold : 0;
     const size_t sz_cold = U * Cs * d * 2, sz_cidx = U * Cs * 4;
-    const size_t sz_cmeta = cold >= 0 ? U * 8 : 0, sz_bcnt = cold >= 0 ? U * c->NB * 4 : 0;
+    const size_t sz_cmeta = cold >= 0 ? U * 8 : 0, sz_bcnt = (cold >= 0 || pct >= 0) ? U * c->NB * 4 : 0;
     const size_t sz_sel = U * c->NB * 4;   // also the size of the bound scratch
     size_t off = 0;
     const size_t o_blk = off; off = round_up(off + sz_blk, 256);
@@ -496,7 +507,7 @@ int ott_get_seq_counts(const ott_cache *c, int b, long long *T, int *nf, int *ta
     if (T) *T = Tb;
     if (nf) *nf = nfb;
     if (tail) *tail = (int)(Tb - (long long)nfb * c->G);
-    if (n_pool) *n_pool = pool_after(c->P, c->G, nfb);
+    if (n_pool) *n_pool = pool_after(c->P, c->G, nfb, c->pct);
     return OTT_OK;
 }
 
@@ -506,7 +517,7 @@ int ott_get_counts(const ott_cache *c, long long *T, int *nf, int *tail, int *n_
     if (T) *T = c->T;
     if (nf) *nf = c->nf;
     if (tail) *tail = (int)(c->T - (long long)c->nf * c->G);
-    if (n_pool) *n_pool = pool_after(c->P, c->G, c->nf);
+    if (n_pool) *n_pool = pool_after(c->P, c->G, c->nf, c->pct);
     return OTT_OK;
 }
 
@@ -517,7 +528,7 @@ int ott_block_count(const ott_cache *c, int j) {
         for (int b = 0; b < c->B; ++b) nf = c->nfb[b] > nf ? c->nfb[b] : nf;
     if (j < 0 || j >= nf) return OTT_ERR_INVALID;
     if (c->cold >= 0) return OTT_ERR_STATE;   // sizes differ per unit: ott_export_cold
-    return block_count(c->P, c->G, j);
+    return block_count(c->P, c->G, j, c->pct);
 }
 
 long long ott_device_bytes(const ott_cache *c) { return c ? (long long)c->mem_bytes : 0; }
@@ -546,7 +557,7 @@ int ott_export_state(ott_cache *c, int u0, int nu, const ott_state_export *dst) 
     const long long Tx = c->ragged ? c->Tb[sb0] : c->T;
     const int d = c->d, G = c->G, P = c->P, nf = c->ragged ? c->nfb[sb0] : c->nf;
     const int nt = (int)(Tx - (long long)nf * G);
-    const int np = pool_after(P, G, nf);
+    const int np = pool_after(P, G, nf, c->pct);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(c, e);
 

@@ -1121,7 +1121,7 @@ inline SeqEntry seq_entry(const ott_cache *c, long long T, int nf, int nq_blocks
     e.nf = nf;
     e.ring_start = (int)(tail_start % c->ring);
     e.ntail = (int)(T - tail_start);
-    e.npool = pool_after(c->P, c->G, nf);
+    e.npool = pool_after(c->P, c->G, nf, c->pct);
     // the cold pool's size is known on the device only: items for all C slots
     const int ncold_max = c->cold > 0 ? c->cold : 0;
     e.Sf = (e.ntail + e.npool + ncold_max + FP16_CHUNK - 1) / FP16_CHUNK;
@@ -1245,7 +1245,8 @@ cudaError_t set_decode_attr(int smem_max) {
 
 template <int D, int GQ>
 cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, float *part, cudaStream_t s) {
-    if (c->cold >= 0) return launch_decode_t<D, GQ, false, true, false>(c, q, out, part, s);
+    // block sizes from the per-block counts (cold-pool or channel criterion)
+    if (c->bcnt) return launch_decode_t<D, GQ, false, true, false>(c, q, out, part, s);
     return c->ragged ? launch_decode_t<D, GQ, true, false, false>(c, q, out, part, s)
                      : launch_decode_t<D, GQ, false, false, false>(c, q, out, part, s);
 }
@@ -1253,7 +1254,7 @@ cudaError_t launch_decode_any(const ott_cache *c, const __half *q, __half *out, 
 template <int D, int GQ>
 cudaError_t launch_decode_topk_t(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s) {
     if (c->ragged) return launch_decode_t<D, GQ, true, false, true>(c, q, out, c->part, s, Kc);
-    return c->cold >= 0 ? launch_decode_t<D, GQ, false, true, true>(c, q, out, c->part, s, Kc)
+    return c->bcnt ? launch_decode_t<D, GQ, false, true, true>(c, q, out, c->part, s, Kc)
                         : launch_decode_t<D, GQ, false, false, true>(c, q, out, c->part, s, Kc);
 }
 

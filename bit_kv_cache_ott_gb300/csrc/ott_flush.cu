@@ -55,8 +55,9 @@ struct FlushArgs {
     __half *ck, *cv;             // cold pool [U][C][d] (cold-pool policy)
     int32_t *cidx;               // [U][C] token index of each cold slot
     int *cmeta;                  // [U][2]: tokens in the cold pool, slot of the oldest
-    int32_t *bcnt;               // [U][NB] valid tokens of each block (cold-pool policy)
+    int32_t *bcnt;               // [U][NB] valid tokens of each block (null: fixed by P, G, j)
     int C;                       // cold-pool capacity; -1: displaced tokens are written back
+    int pct, n_oc;               // channel-conditioned criterion: p (1/10000; -1: norm) and channels
     int32_t *bt;                 // paged pool: [U][NB] slot of each block (null: slot u*NB + j)
     int32_t *fstack;             // paged pool: free slots
     int *ftop;                   // paged pool: number of free slots
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         jj = fl.lj[e];
         t0 = (long long)jj * a.G;
     }
-    const int G = a.G, P = a.P, np0 = fl.n > 0 ? pool_after(P, G, jj) : a.np0, nc = np0 + G;
+    const int G = a.G, P = a.P, np0 = fl.n > 0 ? pool_after(P, G, jj, a.pct) : a.np0, nc = np0 + G;
 
     __half *ck = reinterpret_cast<__half *>(smem);
     __half *cv = ck + (size_t)nc * RS;
@@ -123,23 +124,58 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     __syncthreads();
 
     // 2. keys: (fp32 squared norm bits, token index); norms >= +0 order as bits
-    for (int row = tid; row < nc; row += nth) {
-        float nrm;
-        int idx;
-        if (row < np0) {
-            nrm = a.pnorm[(size_t)u * P + row];
-            idx = a.pidx[(size_t)u * P + row];
-        } else {
+    const bool chan = a.pct >= 0;
+    if (!chan) {
+        for (int row = tid; row < nc; row += nth) {
+            float nrm;
+            int idx;
+            if (row < np0) {
+                nrm = a.pnorm[(size_t)u * P + row];
+                idx = a.pidx[(size_t)u * P + row];
+            } else {
+                const __half *kr = ck + (size_t)row * RS;
+                float s = 0.0f;
+                for (int ch = 0; ch < D; ++ch) {
+                    const float x = __half2float(kr[ch]);
+                    s = __fadd_rn(s, __fmul_rn(x, x));
+                }
+                nrm = s;
+                idx = (int)(t0 + (row - np0));
+            }
+            key[row] = ((uint64_t)__float_as_uint(nrm) << 32) | (uint32_t)idx;
+        }
+    } else {
+        // channel-conditioned criterion: the outlier channels are the n_oc
+        // with the largest max |k| over all candidates (ties to the lower
+        // channel); every candidate, old pool rows included, is scored by
+        // its squared norm over them (fp32, ascending channel order).
+        // ks and kz are free until step 6.
+        float *camax = ks;
+        int *csel = reinterpret_cast<int *>(kz);
+        for (int ch = tid; ch < D; ch += nth) {
+            float m = 0.0f;
+            for (int row = 0; row < nc; ++row) m = fmaxf(m, fabsf(__half2float(ck[(size_t)row * RS + ch])));
+            camax[ch] = m;
+        }
+        __syncthreads();
+        for (int ch = tid; ch < D; ch += nth) {
+            const float m = camax[ch];
+            int rk = 0;
+            for (int c2 = 0; c2 < D; ++c2) rk += camax[c2] > m || (camax[c2] == m && c2 < ch);
+            csel[ch] = rk < a.n_oc;
+        }
+        __syncthreads();
+        for (int row = tid; row < nc; row += nth) {
             const __half *kr = ck + (size_t)row * RS;
             float s = 0.0f;
             for (int ch = 0; ch < D; ++ch) {
+                if (!csel[ch]) continue;
                 const float x = __half2float(kr[ch]);
                 s = __fadd_rn(s, __fmul_rn(x, x));
             }
-            nrm = s;
-            idx = (int)(t0 + (row - np0));
+            const int idx = row < np0 ? a.pidx[(size_t)u * P + row] : (int)(t0 + (row - np0));
+            key[row] = ((uint64_t)__float_as_uint(s) << 32) | (uint32_t)idx;
         }
-        key[row] = ((uint64_t)__float_as_uint(nrm) << 32) | (uint32_t)idx;
     }
     __syncthreads();
 
@@ -151,7 +187,10 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         rank[r] = rk;
     }
     __syncthreads();
-    const int keep = min(P, nc);
+    // the pool keeps the P best, or under the channel criterion at most the
+    // ceil(p * nc) smallest scores
+    int keep = min(P, nc);
+    if (chan) keep = min(keep, (int)(((long long)a.pct * nc + 9999) / 10000));
     const bool cold = a.C >= 0;
     // displaced pool tokens; under the cold-pool policy they leave the block
     int ev = 0;
@@ -202,8 +241,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
 
     // the displaced tokens enter the cold pool in token order; of the
     // cn0 + ev tokens, the last min(C, cn0 + ev) stay
+    if (a.bcnt && tid == 0) a.bcnt[(size_t)u * a.NB + jj] = cnt;
     if (cold) {
-        if (tid == 0) a.bcnt[(size_t)u * a.NB + jj] = cnt;
         if (a.C > 0 && ev > 0) {
             const int n1 = min(a.C, cn0 + ev), skip = ev - min(ev, n1);
             for (int e = tid; e < (ev - skip) * VPR; e += nth) {
@@ -482,7 +521,9 @@ FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV,
     a.NB = c->NB;
     a.ntile = c->ntile;
     a.j = j;
-    a.np0 = pool_after(c->P, c->G, j);
+    a.np0 = pool_after(c->P, c->G, j, c->pct);
+    a.pct = c->pct;
+    a.n_oc = c->n_oc;
     a.Hkv = c->Hkv;
     return a;
 }

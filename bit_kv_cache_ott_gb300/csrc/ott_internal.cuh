@@ -75,12 +75,26 @@ __host__ __device__ inline long long block_bytes_of(int d, int G) {
 __host__ __device__ constexpr int cls_of_pos(int p) { return p < 5 ? p : p - 5; }
 
 // Pool size after nf flushes and valid tokens of block j (same for all units).
-__host__ __device__ inline int pool_after(int P, int G, long long nf) {
-    long long x = nf * (long long)G;
-    return (int)(x < P ? x : P);
+// Norm criterion (pct < 0): min(nf * G, P). Channel-conditioned criterion
+// (pct = p in units of 1/10000): x_j = min(P, ceil(p * (x_{j-1} + G))); the
+// map is nondecreasing and x_1 >= x_0 = 0, so the sizes never shrink and stay
+// fixed from the first repeat on (at most P + 1 steps).
+__host__ __device__ inline int pool_after(int P, int G, long long nf, int pct = -1) {
+    if (pct < 0) {
+        long long x = nf * (long long)G;
+        return (int)(x < P ? x : P);
+    }
+    int x = 0;
+    for (long long j = 0; j < nf; ++j) {
+        const long long m = ((long long)pct * (x + G) + 9999) / 10000;
+        const int y = (int)(m < P ? m : P);
+        if (y == x) break;
+        x = y;
+    }
+    return x;
 }
-__host__ __device__ inline int block_count(int P, int G, int j) {
-    return pool_after(P, G, j) + G - pool_after(P, G, j + 1);
+__host__ __device__ inline int block_count(int P, int G, int j, int pct = -1) {
+    return pool_after(P, G, j, pct) + G - pool_after(P, G, j + 1, pct);
 }
 
 // (token slot t, channel ch) -> (word index lane*(d/32)+w within the tile's
@@ -144,7 +158,10 @@ struct ott_cache {
     __half *ck, *cv;        // [U][C][d]
     int32_t *cidx;          // [U][C]
     int *cmeta;             // [U][2]: tokens in the cold pool, slot of the oldest
-    int32_t *bcnt;          // [U][NB] valid tokens of each block
+    int32_t *bcnt;          // [U][NB] valid tokens of each block (cold-pool or channel criterion)
+    // channel-conditioned outlier criterion (ott_create_pct): p in units of
+    // 1/10000 (-1: the norm criterion) and the outlier channels per flush
+    int pct, n_oc;
     // paged block pool (ott_create_paged): the quantized blocks of all units
     // come from one pool; a flush takes a free slot, a released sequence
     // returns its slots

@@ -291,7 +291,7 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     a.G = c->G;
     a.P = c->P;
     a.jfull = (c->P + c->G - 1) / c->G;
-    a.bcnt = c->cold >= 0 ? c->bcnt : nullptr;
+    a.bcnt = c->bcnt;   // null unless block sizes differ from the norm criterion's
     a.q = q;
     a.Hq = c->Hq;
     a.Hkv = c->Hkv;

@@ -119,6 +119,27 @@ int ott_create_cold(int B, int Hq, int Hkv, int d, int G, int R, int P, int C,
                     int max_tokens, ott_cache **out);
 
 /*
+ * As ott_create, with the channel-conditioned outlier criterion of
+ * zijie-tian.site sec. 3.1 (an outlier token lies in an outlier channel and
+ * its magnitude is among the globally smallest p%) in place of the norm
+ * ranking. At each flush, over the candidates (the pool plus the group):
+ * the outlier channels are the n_oc channels with the largest max |k| (ties
+ * to the lower channel index); each candidate's score is its squared key
+ * norm over those channels only (fp32, ascending channel order; old pool
+ * tokens are scored again, since the channels change from flush to flush);
+ * the m = ceil(pct * candidates / 10000) smallest scores (ties to the lower
+ * token index) are the outliers, and the pool keeps the min(P, m) most
+ * outlying of them. Every other candidate joins the new block (written
+ * back). Pool and block sizes follow from (P, G, pct) alone, the same for
+ * every unit: pool_j = min(P, ceil(pct * (pool_{j-1} + G) / 10000)), as
+ * ott_get_counts and ott_block_count report. pct = 10000 with n_oc = d is the
+ * norm criterion of ott_create; pct = 0 keeps no pool. 0 <= pct <= 10000,
+ * 1 <= n_oc <= d, else OTT_ERR_INVALID. All sequences have one length.
+ */
+int ott_create_pct(int B, int Hq, int Hkv, int d, int G, int R, int P, int pct, int n_oc,
+                   int max_tokens, ott_cache **out);
+
+/*
  * As ott_create_ragged, with the quantized blocks of all (sequence, kv head)
  * units drawn from one pool of pool_blocks blocks (a paged block table)
  * instead of max_tokens worth of blocks per unit: a serving batch whose

@@ -1,0 +1,154 @@
+"""GPU parity for the channel-conditioned outlier criterion (ott_create_pct;
+zijie-tian.site sec. 3.1: an outlier token lies in an outlier channel and its
+magnitude is among the globally smallest p%). The CUDA path through the C ABI
+against the CPU oracle's same criterion on the same seeded inputs: block
+sizes, block indices, codes, scales, residual, pool (indices, scores, keys,
+values) bit-exact; outputs within max |d| <= 2e-3 and mean |d| <= 2e-4 of the
+oracle's double result. With p = 100% over all d channels the criterion is
+the norm ranking, and the device state and outputs equal those of
+ott_create bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_ott_gb300 import synth
+from tests.parity_util import STATE_KEYS, compare_out, compare_state, oracle_decode_all
+
+pytestmark = pytest.mark.gpu
+
+
+def _gen(seed, B, Hkv, T, d):
+    """The workloads' key recipe (outlier channels, low-norm tokens) plus
+    exact duplicates for ties and a few tokens large in one extra channel,
+    so that the chosen channels move from flush to flush."""
+    g = torch.Generator().manual_seed(seed)
+    K = torch.randn(B, Hkv, T, d, generator=g)
+    ch = torch.randint(0, d, (4,), generator=g)
+    K[..., ch] *= 15
+    low = torch.rand(B, Hkv, T, generator=g) < 0.05
+    K[low] *= 0.03
+    spike = torch.rand(B, Hkv, T, generator=g) < 0.01
+    K[..., 0][spike] = 60.0
+    if T > 12:
+        K[:, :, 9::11] = K[:, :, 4:5]
+    V = torch.randn(B, Hkv, T, d, generator=g)
+    return K.half(), V.half()
+
+
+def _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps, seed, every=1):
+    K, V = _gen(seed, B, Hkv, L + steps, d)
+    q_all = torch.randn(steps + 1, B, Hq, d, generator=torch.Generator().manual_seed(seed + 1)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P, pct=(pct, n_oc))
+    orc.prefill(K[:, :, :L].contiguous(), V[:, :, :L].contiguous())
+    dev = torch.device("cuda")
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=L + steps + 1, pct=(pct, n_oc)) as c:
+        c.prefill(K[:, :, :L].contiguous().to(dev), V[:, :, :L].contiguous().to(dev))
+        nf_prev = -1
+        for s in range(steps + 1):
+            nf = c.counts()[1]
+            if s % every == 0 or s == steps or nf != nf_prev:
+                compare_state(c.export_state(), orc)
+                nf_prev = nf
+            compare_out(c.decode_attn(q_all[s].to(dev)), orc.decode(q_all[s]), f"step {s}")
+            if s < steps:
+                k, v = K[:, :, L + s].contiguous(), V[:, :, L + s].contiguous()
+                c.append(k.to(dev), v.to(dev))
+                orc.append(k, v)
+        c.check_device()
+        return c.counts()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,G,R,P,pct,n_oc,L,steps", [
+    (1, 1, 1, 128, 16, 4, 5, 2000, 4, 300, 40),       # pool below P: min(5, ceil(0.2 (x + 16)))
+    (2, 4, 2, 128, 32, 8, 32, 1000, 8, 500, 70),      # GQA 2, the pages' P = 32, 10%
+    (2, 8, 2, 64, 16, 0, 7, 5000, 3, 260, 40),        # GQA 4, d = 64, R = 0
+    (3, 3, 3, 128, 20, 5, 10, 100, 1, 200, 25),       # 1%: one outlier per flush; G not a multiple of 16
+    (1, 4, 1, 128, 16, 2, 40, 3000, 128, 150, 40),    # GQA 4, P above the fixed point, every channel
+    (1, 2, 1, 128, 8, 2, 3, 0, 2, 40, 30),            # p = 0: no pool; the first flushes during the steps
+])
+def test_pct_small(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps):
+    T, nf, tail, npool = _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps, seed=B + G + pct)
+    want = 0
+    for _ in range(nf):
+        want = min(P, -(-pct * (want + G) // 10000))
+    assert npool == want
+
+
+def test_full_percent_all_channels_equals_norm_criterion(ott):
+    """p = 100% over all d channels: the same device state and outputs as the
+    norm criterion's cache, bit for bit, through prefill, flushes and decode."""
+    B, Hq, Hkv, d, G, R, P, L, steps = 2, 4, 2, 128, 16, 4, 6, 250, 40
+    K, V = _gen(5, B, Hkv, L + steps, d)
+    q_all = torch.randn(steps, B, Hq, d, generator=torch.Generator().manual_seed(6)).half().cuda()
+    K, V = K.cuda(), V.cuda()
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=L + steps, pct=(10000, d)) as a, \
+            ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=L + steps) as b:
+        for c in (a, b):
+            c.prefill(K[:, :, :L].contiguous(), V[:, :, :L].contiguous())
+        for s in range(steps):
+            assert torch.equal(a.decode_attn(q_all[s]), b.decode_attn(q_all[s])), s
+            for c in (a, b):
+                c.append(K[:, :, L + s].contiguous(), V[:, :, L + s].contiguous())
+        ea, eb = a.export_state(), b.export_state()
+        for k in STATE_KEYS + ("bcount",):
+            assert np.array_equal(ea[k], eb[k]), k
+        assert a.counts() == b.counts()
+
+
+def test_pct_topk(oracle_mod, ott):
+    """Top-K sparse decode over the criterion's blocks (their sizes come from
+    the per-block counts): selection bit-exact, outputs within the bar."""
+    B, Hq, Hkv, d, G, R, P, pct, n_oc, L = 2, 4, 2, 128, 16, 4, 8, 2500, 6, 400
+    K, V = _gen(11, B, Hkv, L, d)
+    q = torch.randn(B, Hq, d, generator=torch.Generator().manual_seed(12)).half()
+    orc = oracle_mod.OracleCache(B, Hq, Hkv, d, G, R, P, pct=(pct, n_oc))
+    orc.prefill(K, V)
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, max_tokens=L, pct=(pct, n_oc)) as c:
+        c.prefill(K.cuda(), V.cuda())
+        nf = c.counts()[1]
+        for Kb in (1, 5, nf + 3):
+            kc = min(Kb, nf)
+            sel = torch.full((B * Hkv, kc), -7, dtype=torch.int32, device="cuda")
+            out = c.decode_attn_topk(q.cuda(), Kb, sel=sel)
+            want, _ = orc.topk_select(q, Kb)
+            assert np.array_equal(sel.cpu().numpy(), want[:, :kc]), Kb
+            compare_out(out, orc.decode_topk(q, Kb), f"K={Kb}")
+
+
+def test_pct_argument_errors(ott):
+    from bit_kv_cache_ott_gb300 import OTTError
+    for pct, n_oc in ((-1, 4), (10001, 4), (1000, 0), (1000, 129)):
+        with pytest.raises(OTTError):
+            ott.OTTCache(1, 1, 1, 128, 16, 4, 8, max_tokens=64, pct=(pct, n_oc))
+
+
+def test_pct_batch_b32_fullsize(oracle_mod, ott):
+    """The headline batch (32 sequences x 32 heads, 4K prefill, G = 128,
+    R = 32, P = 32) under p = 10% over the workload's 4 outlier channels:
+    sampled units bit-exact after the prefill and at the flush the steps
+    cross, every output at chosen steps."""
+    w = synth.WORKLOADS["batch_b32"]
+    pct, n_oc, steps, decode_steps = 1000, 4, 140, {0, 31, 32, 139}
+    K, V = synth.prefill_kv(w)
+    orc = oracle_mod.OracleCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, pct=(pct, n_oc))
+    orc.prefill(K, V)
+    rng = np.random.default_rng(3)
+    units = sorted({0, w.B * w.Hkv - 1, *rng.choice(w.B * w.Hkv, 46, replace=False).tolist()})
+    with ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + steps, pct=(pct, n_oc)) as c:
+        c.prefill(K.cuda(), V.cuda())
+        del K, V
+        compare_state(c.export_state(), orc, units)
+        nf_prev = c.counts()[1]
+        for s in range(steps):
+            k, v, q = synth.step_kvq(w, s)
+            c.append(k.cuda(), v.cuda())
+            orc.append(k, v)
+            nf = c.counts()[1]
+            if nf != nf_prev:
+                compare_state(c.export_state(), orc, units)
+                nf_prev = nf
+            if s in decode_steps:
+                compare_out(c.decode_attn(q.cuda()), oracle_decode_all(orc, q), f"pct step {s}")
+        assert c.counts()[3] == 15          # min(32, ceil(0.1 (x + 128))) settles at 15
+        c.check_device()
