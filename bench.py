@@ -342,6 +342,61 @@ def copy_peak(ott, dev, stream, gib: int = 2, reps: int = 10):
             "method": f"{gib} GiB read + {gib} GiB written per call, best of {reps} CUDA-event-timed calls"}
 
 
+def prefill_launches(w, lens) -> int:
+    """Kernel launches of one layer's prefill, as the library issues them:
+    a prompt of two or more groups takes the parallel pass (group keys, pool
+    scan, every block at once; with P = 0 the blocks alone), except under the
+    cold-pool policy, whose flushes run group by group; then the residual
+    tokens are copied (one launch, or one per sequence of a ragged batch)."""
+    nfs = [metrics.flush_count(L, w.G, w.R) for L in lens]
+    par_cost = 3 if w.P > 0 else 1
+    if not w.ragged:
+        nf = nfs[0]
+        return (par_cost if (nf >= 2 and w.cold < 0) else nf) + 1
+    par = [nf >= 2 and w.cold < 0 for nf in nfs]
+    serial = max([nf for nf, p in zip(nfs, par) if not p], default=0)
+    return par_cost * sum(par) + serial + len(lens)
+
+
+def measure_prefill(ott, w, wr, dev, stream, reps: int = 3):
+    """One layer's prefill from K, V already on the device: CUDA events on
+    the launch stream around ott_prefill (ott_prefill_lens for a ragged
+    batch) into a fresh cache, median of `reps` after one warm-up call. The
+    inputs (K and V of every prompt token) are larger than L2."""
+    lens = synth.seq_lens(wr)
+    K, V = synth.prefill_kv(wr, layer=0, device=str(dev))
+    times = []
+    for r in range(reps + 1):
+        pool = None
+        if w.paged:
+            pool = sum(metrics.flush_count(t, w.G, w.R) for t in lens) * w.Hkv + 1
+        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + 8, ragged=w.ragged,
+                         cold=cold_of(w), pool_blocks=pool)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if w.ragged:
+            c.prefill_lens(K, V, lens, stream)
+        else:
+            c.prefill(K, V, stream)
+        b.record(stream)
+        b.synchronize()
+        c.check_device()
+        if r > 0:
+            times.append(a.elapsed_time(b))
+        c.close()
+    del K, V
+    torch.cuda.empty_cache()
+    ms = statistics.median(times)
+    nbytes = sum(metrics.prefill_bytes_per_unit(L, w.d, w.G, w.R, w.P) for L in lens) * w.Hkv
+    return {"ms": ms, "tokens": sum(lens), "tokens_per_s": sum(lens) / (ms * 1e-3),
+            "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "launches": prefill_launches(w, lens), "reps": reps,
+            "timing": "CUDA events around the prefill call into a fresh cache, median of "
+                      f"{reps} after one warm-up; bytes: every prompt token read once (K and V), "
+                      "blocks with token indices, final pool and fp16 residual written"}
+
+
 def run_ours(args, w):
     import bit_kv_cache_ott_gb300 as ott
 

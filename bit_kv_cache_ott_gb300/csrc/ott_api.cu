@@ -67,6 +67,25 @@ void to_per_sequence(ott_cache *c) {
     c->nf = 0;
 }
 
+// Every flush of units [u0, u0 + nu), nf each, in one parallel pass (the
+// source holds unit u at (u - src_u0) * unit_stride). False when the policy
+// needs the flushes one after another or no scratch could be had: the caller
+// then flushes group by group.
+bool try_prefill_parallel(const ott_cache *c, const __half *K, const __half *V, long long unit_stride, int src_u0,
+                          int u0, int nu, int nf, cudaStream_t s, cudaError_t &err) {
+    err = cudaSuccess;
+    if (!prefill_parallel_ok(c, nf)) return false;
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, prefill_scratch_bytes(c, nu, nf), s) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    err = launch_prefill_parallel(c, K, V, unit_stride, src_u0, u0, nu, nf, static_cast<uint64_t *>(scratch), s);
+    const cudaError_t e2 = cudaFreeAsync(scratch, s);
+    if (err == cudaSuccess) err = e2;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,11 +322,13 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     const int nf = L >= c->G + c->R ? (L - c->R) / c->G : 0;
     if (blocks_needed(c, (long long)nf * c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, (long long)nf * c->U);
-    for (int j = 0; j < nf; ++j) {
-        cudaError_t e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
-        if (e != cudaSuccess) return fail_cuda(c, e);
+    cudaError_t e = cudaSuccess;
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, s, e)) {
+        for (int j = 0; j < nf && e == cudaSuccess; ++j)
+            e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
     }
-    cudaError_t e = launch_copy_tail(c, Kh, Vh, L, (long long)nf * c->G, s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    e = launch_copy_tail(c, Kh, Vh, L, (long long)nf * c->G, s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T = L;
     c->nf = nf;
@@ -337,16 +358,25 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
     c->free_blocks -= blocks_needed(c, unit_flushes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
-    // group j of every sequence that has one, in token order
+    // each sequence in one parallel pass where it can; the rest group by
+    // group, every such sequence's group j in one launch
+    std::vector<char> done(c->B, 0);
+    for (int b = 0; b < c->B; ++b) {
+        cudaError_t e = cudaSuccess;
+        done[b] = try_prefill_parallel(c, Kh, Vh, (long long)Lmax * c->d, 0, b * c->Hkv, c->Hkv,
+                                       flushes_after(c, lens[b]), s, e);
+        if (e != cudaSuccess) return fail_cuda(c, e);
+    }
     for (int j = 0; j < nf_max; ++j) {
         FlushList fl;
         fl.n = 0;
         for (int b = 0; b < c->B; ++b)
-            if (flushes_after(c, lens[b]) > j) {
+            if (!done[b] && flushes_after(c, lens[b]) > j) {
                 fl.lb[fl.n] = b;
                 fl.lj[fl.n] = j;
                 ++fl.n;
             }
+        if (fl.n == 0) break;
         cudaError_t e = launch_flush_list(c, Kh, Vh, (long long)Lmax * c->d, LLONG_MAX, fl, s);
         if (e != cudaSuccess) return fail_cuda(c, e);
     }
@@ -478,15 +508,18 @@ int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, vo
     c->free_blocks -= blocks_needed(c, (long long)nf * c->Hkv);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
-    for (int j = 0; j < nf; ++j) {
-        FlushList fl;
-        fl.n = 1;
-        fl.lb[0] = b;
-        fl.lj[0] = j;
-        cudaError_t e = launch_flush_list_src(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, b * c->Hkv, fl, s);
-        if (e != cudaSuccess) return fail_cuda(c, e);
+    cudaError_t e = cudaSuccess;
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, b * c->Hkv, b * c->Hkv, c->Hkv, nf, s, e)) {
+        for (int j = 0; j < nf && e == cudaSuccess; ++j) {
+            FlushList fl;
+            fl.n = 1;
+            fl.lb[0] = b;
+            fl.lj[0] = j;
+            e = launch_flush_list_src(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, b * c->Hkv, fl, s);
+        }
     }
-    cudaError_t e = launch_copy_tail_units(c, Kh, Vh, b * c->Hkv, c->Hkv, L, (long long)nf * c->G, L, s,
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    e = launch_copy_tail_units(c, Kh, Vh, b * c->Hkv, c->Hkv, L, (long long)nf * c->G, L, s,
                                            b * c->Hkv);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->Tb[b] = L;

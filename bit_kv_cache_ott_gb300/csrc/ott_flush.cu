@@ -23,22 +23,53 @@
 // discarded when it overflows. The block is then the group's tokens that did
 // not enter the pool, and its size, which depends on the data, is written to
 // the per-block count array.
+#include <math_constants.h>
+
+#include <climits>
+
 #include "ott_internal.cuh"
 
 namespace ott {
 namespace {
 
-constexpr int FLUSH_THREADS = 256;
+constexpr int FLUSH_THREADS = 512;
 
-// a < b with -0 ordered below +0 (makes min/max independent of order)
-__device__ __forceinline__ bool below(float a, float b) {
-    return a < b || (a == b && signbit(a) && !signbit(b));
+// The 2-bit code of x under scale s and zero z is clamp(rint(fl((x - z) / s)),
+// 0, 3) with fp32 round-to-nearest-even division and rint. Writing
+// f = fl(y), y = (x - z) / s and a = fl(x - z), the code is
+// [f > 1/2] + [f >= 3/2] + [f > 5/2]; fp32 rounding is monotone and 1/2, 3/2,
+// 5/2 have even significands (a tie at a midpoint rounds onto them), so
+//   f > 1/2  <=>  y > 1/2 + 2^-25  <=>  a > RD(s (1/2 + 2^-25))
+//   f >= 3/2 <=>  y >= 3/2 - 2^-24 <=>  a >= RU(s (3/2 - 2^-24))
+//   f > 5/2  <=>  y > 5/2 + 2^-23  <=>  a > RD(s (5/2 + 2^-23))
+// (a is an fp32 value, so comparing it with a real c is comparing it with c
+// rounded down, or up for >=). The scales are fp16 values (11 significant
+// bits, >= 2^-24), so s/2, 3s/2, 5s/2 and s 2^-k are exact in fp32 and each
+// threshold is one directed-rounding add of two exact terms. Code = three
+// compares instead of a division; the same codes bit for bit.
+__device__ __forceinline__ float4 code_rule(float s, float z) {
+    if (s == 0.0f) return make_float4(z, CUDART_INF_F, CUDART_INF_F, CUDART_INF_F);   // every code 0
+    const float t1 = __fadd_rd(__fmul_rn(0.5f, s), __fmul_rn(s, 0x1p-25f));
+    const float t2 = __fsub_ru(__fmul_rn(1.5f, s), __fmul_rn(s, 0x1p-24f));
+    const float t3 = __fadd_rd(__fmul_rn(2.5f, s), __fmul_rn(s, 0x1p-23f));
+    return make_float4(z, t1, t2, t3);
 }
 
-__device__ __forceinline__ uint32_t qcode(float x, float s, float z) {
-    if (s == 0.0f) return 0u;
-    int q = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
-    return (uint32_t)min(max(q, 0), 3);
+__device__ __forceinline__ uint32_t qcode(float x, const float4 &r) {
+    const float a = __fsub_rn(x, r.x);
+    return (uint32_t)(a > r.y) + (uint32_t)(a >= r.z) + (uint32_t)(a > r.w);
+}
+
+// Two fp16 values (bit patterns, one per 16-bit lane) -> 16-bit signed keys
+// in the values' order, with -0 below +0 (so that min and max do not depend
+// on the order the values come in): a negative value keeps its sign bit and
+// has its magnitude bits flipped. The map is its own inverse.
+__device__ __forceinline__ uint32_t okey2(uint32_t h2) {
+    return h2 ^ (((h2 >> 15) & 0x00010001u) * 0x7fffu);
+}
+// the fp16 value of the key in the low 16-bit lane
+__device__ __forceinline__ float okey_lo(uint32_t k2) {
+    return __half2float(__ushort_as_half((unsigned short)(okey2(k2) & 0xffffu)));
 }
 
 __device__ __forceinline__ uint32_t half2_bits(__half a, __half b) {
@@ -62,6 +93,12 @@ struct FlushArgs {
     int32_t *fstack;             // paged pool: free slots
     int *ftop;                   // paged pool: number of free slots
     int *ctl;                    // status word: [1] set when the pool had no free slot
+    // parallel prefill: every flush of units [pf_u0, pf_u0 + nu) in one
+    // launch (CTA i: unit pf_u0 + i / pf_nf, group i % pf_nf); the pool
+    // before group j is read from the pool history (keys of the pool after
+    // flush j - 1, ascending) and its rows from the prefill source
+    const uint64_t *phist;       // [nu][pf_nf][P], or null
+    int pf_nf, pf_u0;
     int src_u0;                  // the source holds units src_u0, src_u0 + 1, ...
     long long src_unit_stride;   // elements between units in the source
     long long src_mod;           // slot = token mod src_mod
@@ -75,7 +112,7 @@ struct FlushArgs {
 // one (ragged batches), CTA i flushes group fl.lj[i / Hkv] of kv head i % Hkv
 // of sequence fl.lb[i / Hkv].
 template <int D>
-__global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __grid_constant__ FlushList fl) {
+__global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const __grid_constant__ FlushList fl) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int RS = D + 8;          // padded row stride (halves): 16B-aligned rows
     constexpr int VPR = D / 8;         // 16-byte vectors per row
@@ -85,13 +122,20 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     const int tid = threadIdx.x, nth = blockDim.x;
     int u = blockIdx.x, jj = a.j;
     long long t0 = a.t0;
-    if (fl.n > 0) {
+    const uint64_t *ph = nullptr;      // parallel prefill: the pool before this group
+    if (a.phist) {
+        u = a.pf_u0 + blockIdx.x / a.pf_nf;
+        jj = blockIdx.x % a.pf_nf;
+        t0 = (long long)jj * a.G;
+        if (jj > 0) ph = a.phist + ((size_t)(u - a.pf_u0) * a.pf_nf + (jj - 1)) * a.P;
+    } else if (fl.n > 0) {
         const int e = blockIdx.x / a.Hkv;
         u = fl.lb[e] * a.Hkv + blockIdx.x % a.Hkv;
         jj = fl.lj[e];
         t0 = (long long)jj * a.G;
     }
-    const int G = a.G, P = a.P, np0 = fl.n > 0 ? pool_after(P, G, jj, a.pct) : a.np0, nc = np0 + G;
+    const int G = a.G, P = a.P;
+    const int np0 = (a.phist || fl.n > 0) ? pool_after(P, G, jj, a.pct) : a.np0, nc = np0 + G;
 
     __half *ck = reinterpret_cast<__half *>(smem);
     __half *cv = ck + (size_t)nc * RS;
@@ -99,16 +143,25 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     int *rank = reinterpret_cast<int *>(key + nc);
     int *bmap = rank + nc;
     int *emap = bmap + G;              // displaced pool rows by token order (cold-pool policy)
-    float *ks = reinterpret_cast<float *>(emap + (P > 0 ? P : 1));
+    // code rules: per channel for keys, per (token, 32 channels) for values;
+    // the value area first holds the key min/max partials
+    const size_t rule_off = ((size_t)(reinterpret_cast<uint8_t *>(emap + (P > 0 ? P : 1)) - smem) + 15) & ~(size_t)15;
+    float4 *krule = reinterpret_cast<float4 *>(smem + rule_off);
+    float4 *vrule = krule + D;
+    float *ks = reinterpret_cast<float *>(krule);   // channel criterion scratch (before the rules)
     float *kz = ks + D;
-    float *vs = kz + D;
-    float *vz = vs + G * NG;
+    const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
 
     // 1. stage the candidates: old pool rows, then the group's rows
     for (int e = tid; e < nc * VPR; e += nth) {
         const int row = e / VPR, v8 = e % VPR;
         const __half *sk, *sv;
-        if (row < np0) {
+        if (row < np0 && ph) {
+            const long long t = (long long)(uint32_t)ph[row];
+            const size_t off = (size_t)(u - a.src_u0) * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
+            sk = a.srcK + off;
+            sv = a.srcV + off;
+        } else if (row < np0) {
             const size_t off = ((size_t)u * P + row) * D;
             sk = a.pk + off;
             sv = a.pv + off;
@@ -129,6 +182,10 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         for (int row = tid; row < nc; row += nth) {
             float nrm;
             int idx;
+            if (row < np0 && ph) {
+                key[row] = ph[row];
+                continue;
+            }
             if (row < np0) {
                 nrm = a.pnorm[(size_t)u * P + row];
                 idx = a.pidx[(size_t)u * P + row];
@@ -179,12 +236,21 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     }
     __syncthreads();
 
-    // 3. rank of every candidate under (norm, index); keys are distinct
-    for (int r = tid; r < nc; r += nth) {
-        const uint64_t kr = key[r];
-        int rk = 0;
-        for (int q = 0; q < nc; ++q) rk += key[q] < kr;
-        rank[r] = rk;
+    // 3. rank of every candidate under (norm, index); keys are distinct.
+    // Each candidate's count is split into `parts` ranges of the others,
+    // summed by shared-memory atomics.
+    for (int r = tid; r < nc; r += nth) rank[r] = 0;
+    __syncthreads();
+    {
+        const int parts = nc < nth ? nth / nc : 1;
+        for (int e = tid; e < nc * parts; e += nth) {
+            const int r = e % nc, part = e / nc;
+            const int q0 = (nc * part) / parts, q1 = (nc * (part + 1)) / parts;
+            const uint64_t kr = key[r];
+            int c = 0;
+            for (int q = q0; q < q1; ++q) c += key[q] < kr;
+            if (c) atomicAdd(rank + r, c);
+        }
     }
     __syncthreads();
     // the pool keeps the P best, or under the channel criterion at most the
@@ -192,27 +258,44 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     int keep = min(P, nc);
     if (chan) keep = min(keep, (int)(((long long)a.pct * nc + 9999) / 10000));
     const bool cold = a.C >= 0;
-    // displaced pool tokens; under the cold-pool policy they leave the block
-    int ev = 0;
-    if (cold)
-        for (int q = 0; q < np0; ++q) ev += rank[q] >= keep;
+    // pool tokens that leave the pool (every warp counts them by ballots);
+    // under the cold-pool policy they also leave the block
+    int nlp = 0;
+    for (int q0 = 0; q0 < np0; q0 += 32) {
+        const int q = q0 + lane;
+        nlp += __popc(__ballot_sync(0xffffffffu, q < np0 && rank[q] >= keep));
+    }
+    const int ev = cold ? nlp : 0;
     const int cnt = nc - keep - ev;
 
     // 4. block slot of every leaving candidate (cold-pool policy: of every
     // leaving group token, and cold order of every displaced pool token):
     // rank by token index among its own kind
-    for (int r = tid; r < nc; r += nth) {
-        if (rank[r] >= keep) {
-            const uint32_t ir = (uint32_t)key[r];
-            const bool own = cold && r < np0;        // a displaced pool token
-            const int q0 = cold ? (own ? 0 : np0) : 0, q1 = cold ? (own ? np0 : nc) : nc;
-            int pos = 0;
-            for (int q = q0; q < q1; ++q) pos += (rank[q] >= keep) && ((uint32_t)key[q] < ir);
-            if (own)
-                emap[pos] = r;
-            else
-                bmap[pos] = r;
+    // Every pool token precedes every group token, and the group rows are
+    // staged in token order: a leaving group row's place is the leaving pool
+    // tokens (written back ones only) plus the leaving group rows before it,
+    // a prefix count taken by warp ballots over chunks of 32 rows.
+    for (int c = warp; c < (G + 31) / 32; c += nwarp) {
+        int base = cold ? 0 : nlp;
+        for (int k = 0; k < c; ++k) {
+            const int g = 32 * k + lane;
+            base += __popc(__ballot_sync(0xffffffffu, g < G && rank[np0 + g] >= keep));
         }
+        const int g = 32 * c + lane;
+        const bool f = g < G && rank[np0 + g] >= keep;
+        const uint32_t bal = __ballot_sync(0xffffffffu, f);
+        if (f) bmap[base + __popc(bal & ((1u << lane) - 1u))] = np0 + g;
+    }
+    // a leaving pool row: its place among the leaving pool rows by token index
+    for (int r = tid; r < np0; r += nth) {
+        if (rank[r] < keep) continue;
+        const uint32_t ir = (uint32_t)key[r];
+        int pos = 0;
+        for (int q = 0; q < np0; ++q) pos += (rank[q] >= keep) && ((uint32_t)key[q] < ir);
+        if (cold)
+            emap[pos] = r;
+        else
+            bmap[pos] = r;
     }
     // cold pool before this flush (read by every thread before thread 0
     // updates it below)
@@ -221,8 +304,10 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
         cn0 = a.cmeta[2 * u];
         ch0 = a.cmeta[2 * u + 1];
     }
-    // 5. the new pool (old pool rows are already staged in shared memory)
-    for (int e = tid; e < nc * VPR; e += nth) {
+    // 5. the new pool (old pool rows are already staged in shared memory);
+    // a parallel prefill keeps only the last group's
+    const bool write_pool = !a.phist || jj == a.pf_nf - 1;
+    for (int e = tid; write_pool && e < nc * VPR; e += nth) {
         const int row = e / VPR, v8 = e % VPR, rk = rank[row];
         if (rk < keep) {
             const size_t off = ((size_t)u * P + rk) * D;
@@ -230,7 +315,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
             reinterpret_cast<uint4 *>(a.pv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[v8];
         }
     }
-    for (int row = tid; row < nc; row += nth) {
+    for (int row = tid; write_pool && row < nc; row += nth) {
         const int rk = rank[row];
         if (rk < keep) {
             a.pnorm[(size_t)u * P + rk] = __uint_as_float((uint32_t)(key[row] >> 32));
@@ -281,39 +366,68 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     for (int t = tid; t < G; t += nth)
         a.bidx[((size_t)u * a.NB + jj) * G + t] = t < cnt ? (int32_t)(uint32_t)key[bmap[t]] : -1;
 
-    // 6. keys: one (scale, zero) per channel over the block's tokens
-    for (int ch = tid; ch < D; ch += nth) {
-        __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
-        if (cnt > 0) {
-            float mn = __half2float(ck[(size_t)bmap[0] * RS + ch]), mx = mn;
-            for (int t = 1; t < cnt; ++t) {
-                const float v = __half2float(ck[(size_t)bmap[t] * RS + ch]);
-                if (below(v, mn)) mn = v;
-                if (below(mx, v)) mx = v;
-            }
-            s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-            z16 = __float2half_rn(mn);
+    // 6. keys: one (scale, zero) per channel over the block's tokens. Each
+    // thread takes a channel pair over one slice of the tokens (min/max of
+    // ordered keys, two channels per SIMD instruction); the slices combine.
+    {
+        constexpr int NCP = D / 2;
+        const int nsl = nth / NCP;
+        uint32_t *kpart = reinterpret_cast<uint32_t *>(vrule);   // [nsl][2][D/2] key pairs
+        const int cp = tid % NCP, sl = tid / NCP;
+        const int tb = (cnt * sl) / nsl, te = (cnt * (sl + 1)) / nsl;
+        uint32_t mn = 0x7fff7fffu, mx = 0x80008000u;
+        for (int t = tb; t < te; ++t) {
+            const uint32_t k2 = okey2(*reinterpret_cast<const uint32_t *>(ck + (size_t)bmap[t] * RS + 2 * cp));
+            mn = __vmins2(mn, k2);
+            mx = __vmaxs2(mx, k2);
         }
-        ks[ch] = __half2float(s16);
-        kz[ch] = __half2float(z16);
-        reinterpret_cast<uint32_t *>(bb)[ch] = half2_bits(s16, z16);
+        kpart[(size_t)sl * D + cp] = mn;
+        kpart[(size_t)sl * D + NCP + cp] = mx;
+        __syncthreads();
+        for (int c2 = tid; c2 < NCP; c2 += nth) {
+            uint32_t m0 = kpart[c2], m1 = kpart[NCP + c2];
+            for (int q = 1; q < nsl; ++q) {
+                m0 = __vmins2(m0, kpart[(size_t)q * D + c2]);
+                m1 = __vmaxs2(m1, kpart[(size_t)q * D + NCP + c2]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ch = 2 * c2 + h;
+                __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
+                if (cnt > 0) {
+                    const float lo = okey_lo(m0 >> (16 * h)), hi = okey_lo(m1 >> (16 * h));
+                    s16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+                    z16 = __float2half_rn(lo);
+                }
+                reinterpret_cast<uint32_t *>(bb)[ch] = half2_bits(s16, z16);
+                krule[ch] = code_rule(__half2float(s16), __half2float(z16));
+            }
+        }
+        __syncthreads();   // the partials are read before the value rules overwrite them
     }
     // 7. values: one (scale, zero) per token per 32 channels
     for (int e = tid; e < a.ntile * TILE * NG; e += nth) {
         const int t = e / NG, gm = e % NG;
         __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
         if (t < cnt) {
-            const __half *row = cv + (size_t)bmap[t] * RS + 32 * gm;
-            float mn = __half2float(row[0]), mx = mn;
-            for (int k = 1; k < 32; ++k) {
-                const float v = __half2float(row[k]);
-                if (below(v, mn)) mn = v;
-                if (below(mx, v)) mx = v;
+            const uint4 *row = reinterpret_cast<const uint4 *>(cv + (size_t)bmap[t] * RS + 32 * gm);
+            uint32_t m0 = 0x7fff7fffu, m1 = 0x80008000u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 x = row[k];
+                const uint32_t w4[4] = {okey2(x.x), okey2(x.y), okey2(x.z), okey2(x.w)};
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    m0 = __vmins2(m0, w4[e2]);
+                    m1 = __vmaxs2(m1, w4[e2]);
+                }
             }
+            m0 = __vmins2(m0, m0 >> 16);   // the low lane takes the smaller of the two
+            m1 = __vmaxs2(m1, __byte_perm(m1, 0, 0x3232));
+            const float mn = okey_lo(m0), mx = okey_lo(m1);
             s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
             z16 = __float2half_rn(mn);
-            vs[t * NG + gm] = __half2float(s16);
-            vz[t * NG + gm] = __half2float(z16);
+            vrule[t * NG + gm] = code_rule(__half2float(s16), __half2float(z16));
         }
         uint8_t *tb = tiles + (size_t)(t / TILE) * tile_bytes(D) + tile_sz_off(D);
         reinterpret_cast<uint32_t *>(tb)[vsz_index(t, gm)] = half2_bits(s16, z16);
@@ -323,34 +437,138 @@ __global__ void __launch_bounds__(FLUSH_THREADS) k_flush(FlushArgs a, const __gr
     // 8. pack the codes into the mma.sync word format (see ott_internal.cuh)
     const int nwords = a.ntile * 32 * NW;
     for (int e = tid; e < nwords; e += nth) {
-        const int tau = e / (32 * NW), rem = e % (32 * NW), lane = rem / NW, w = rem % NW;
-        const int r = lane >> 2, i = lane & 3, wp = w >> 1, hi = w & 1;
+        const int tau = e / (32 * NW), rem = e % (32 * NW), ln = rem / NW, w = rem % NW;
+        const int r = ln >> 2, i = ln & 3, wp = w >> 1, hi = w & 1;
         uint32_t kw = 0, vw = 0;
         const int tk = TILE * tau + r + 8 * hi;   // K: token slot of this word
-        const __half *krow = tk < cnt ? ck + (size_t)bmap[tk] * RS : nullptr;
+        if (tk < cnt) {
+            const __half *krow = ck + (size_t)bmap[tk] * RS;
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int q = 8 * wp + p;
-            // K word: channels 16kt + 2i + 8o (+1) of token tk
-            const int o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
-            if (krow) {
-                kw |= qcode(__half2float(krow[ch]), ks[ch], kz[ch]) << (2 * p);
-                kw |= qcode(__half2float(krow[ch + 1]), ks[ch + 1], kz[ch + 1]) << (16 + 2 * p);
+            for (int p = 0; p < 8; ++p) {
+                // K word: channels 16kt + 2i + 8o (+1) of token tk
+                const int q = 8 * wp + p, o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(krow + ch));
+                kw |= qcode(f.x, krule[ch]) << (2 * p);
+                kw |= qcode(f.y, krule[ch + 1]) << (16 + 2 * p);
             }
-            // V word: channel 16mt + r + 8rowhalf of token slots 16tau + 2i + 8hi (+1)
-            const int rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
+        }
+        // V word: channel 16mt + r + 8rowhalf of token slots 16tau + 2i + 8hi (+1)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int tv = TILE * tau + 2 * i + 8 * hi + h;
-                if (tv < cnt) {
-                    const int gi = tv * NG + vch / 32;
-                    vw |= qcode(__half2float(cv[(size_t)bmap[tv] * RS + vch]), vs[gi], vz[gi]) << (16 * h + 2 * p);
+        for (int h = 0; h < 2; ++h) {
+            const int tv = TILE * tau + 2 * i + 8 * hi + h;
+            if (tv < cnt) {
+                const __half *vrow = cv + (size_t)bmap[tv] * RS;
+                const float4 *vr = vrule + tv * NG;
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const int q = 8 * wp + p, rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
+                    vw |= qcode(__half2float(vrow[vch]), vr[vch / 32]) << (16 * h + 2 * p);
                 }
             }
         }
         uint8_t *tb = tiles + (size_t)tau * tile_bytes(D);
-        reinterpret_cast<uint32_t *>(tb + tile_k_off(D))[lane * NW + w] = kw;
-        reinterpret_cast<uint32_t *>(tb + tile_v_off(D))[lane * NW + w] = vw;
+        reinterpret_cast<uint32_t *>(tb + tile_k_off(D))[ln * NW + w] = kw;
+        reinterpret_cast<uint32_t *>(tb + tile_v_off(D))[ln * NW + w] = vw;
+    }
+}
+
+// Parallel prefill. The pool after flush j is the min(P, (j + 1) G) smallest
+// (norm, index) keys among every token flushed so far (keeping the smallest
+// of a union is associative), so it can be found for all j before any block
+// is built, and then every flush of the prefill runs at once: pass 1 finds
+// each group's own smallest keys, pass 2 merges them unit by unit into the
+// pool history, pass 3 (k_flush with the history) builds every block.
+constexpr int PF_THREADS = 128;
+
+// Pass 1, one CTA per group j of unit u0 + i: the G keys' squared norms,
+// summed in fp32 in channel order exactly as k_flush sums them, and the
+// group's min(P, G) smallest keys, ascending (no other group token can be in
+// the pool after this group's flush).
+template <int D>
+__global__ void __launch_bounds__(PF_THREADS) k_pf_group(const __half *__restrict__ srcK, long long src_unit_stride,
+                                                         int src_u0, int u0, int nf, int G, int P,
+                                                         uint64_t *__restrict__ gtop) {
+    extern __shared__ uint64_t gkey[];   // [G]
+    const int uu = blockIdx.x / nf, j = blockIdx.x % nf, u = u0 + uu;
+    const long long t0 = (long long)j * G;
+    const __half *base = srcK + (size_t)(u - src_u0) * src_unit_stride;
+    for (int t = threadIdx.x; t < G; t += blockDim.x) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(base + (size_t)(t0 + t) * D);
+        float s = 0.0f;
+#pragma unroll 4
+        for (int v8 = 0; v8 < D / 8; ++v8) {
+            const uint4 x = __ldg(row + v8);
+            const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {   // channels 8 v8 + 2e, 8 v8 + 2e + 1
+                const float2 f = __half22float2(h[e]);
+                s = __fadd_rn(s, __fmul_rn(f.x, f.x));
+                s = __fadd_rn(s, __fmul_rn(f.y, f.y));
+            }
+        }
+        gkey[t] = ((uint64_t)__float_as_uint(s) << 32) | (uint32_t)(t0 + t);
+    }
+    __syncthreads();
+    const int nb = min(P, G);
+    uint64_t *dst = gtop + ((size_t)uu * nf + j) * P;
+    for (int t = threadIdx.x; t < G; t += blockDim.x) {
+        const uint64_t k = gkey[t];
+        int r = 0;
+        for (int q = 0; q < G; ++q) r += gkey[q] < k;
+        if (r < nb) dst[r] = k;
+    }
+}
+
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Pass 2, one warp per unit: the pool after flush j (ascending keys) is the
+// first min(P, pool + G) of the merge of the pool after flush j - 1 with
+// group j's smallest keys. Lane k finds output k by a binary search on the
+// merge path; the next group's keys arrive by cp.async during the merge.
+__global__ void k_pf_scan(const uint64_t *__restrict__ gtop, uint64_t *__restrict__ phist, int nu, int nf, int G,
+                          int P) {
+    extern __shared__ uint64_t scan_sm[];   // per warp: two pool lists, two group lists
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int uu = blockIdx.x * (blockDim.x >> 5) + wib;
+    if (uu >= nu) return;
+    uint64_t *A = scan_sm + (size_t)wib * 4 * P, *Cn = A + P, *Bc = Cn + P, *Bn = Bc + P;
+    const int nb = min(P, G);
+    const uint64_t *gt = gtop + (size_t)uu * nf * P;
+    uint64_t *ph = phist + (size_t)uu * nf * P;
+    for (int k = lane; k < nb; k += 32) Bc[k] = gt[k];
+    __syncwarp();
+    int na = 0;
+    for (int j = 0; j < nf; ++j) {
+        if (j + 1 < nf)
+            for (int k = lane; k < nb; k += 32) cp_async8(Bn + k, gt + (size_t)(j + 1) * P + k);
+        const int m = (int)min((long long)P, (long long)na + G);
+        for (int k = lane; k < m; k += 32) {
+            // i = keys taken from A among the first k + 1 of the merge
+            int lo = max(0, k + 1 - nb), hi = min(k + 1, na);
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (A[mid] < Bc[k - mid]) lo = mid + 1;
+                else hi = mid;
+            }
+            uint64_t x = lo > 0 ? A[lo - 1] : 0ull;
+            if (k - lo >= 0) {
+                const uint64_t y = Bc[k - lo];
+                x = y > x ? y : x;
+            }
+            Cn[k] = x;
+            ph[(size_t)j * P + k] = x;
+        }
+        cp_async_wait_all();
+        __syncwarp();
+        uint64_t *t = A; A = Cn; Cn = t;
+        t = Bc; Bc = Bn; Bn = t;
+        na = m;
     }
 }
 
@@ -474,9 +692,13 @@ int flush_smem_bytes(int d, int G, int P) {
                         + nc * 8               // keys
                         + nc * 4 + (long long)G * 4           // ranks, block map
                         + (long long)(P > 0 ? P : 1) * 4      // cold order
-                        + 2LL * d * 4                         // key scale/zero
-                        + 2LL * ntiles_of(G) * TILE * (d / 32) * 4;  // value scale/zero
-    return b > (1LL << 30) ? (1 << 30) : (int)b;
+                        + 16                                  // alignment of the code rules
+                        + (long long)d * 16;                  // key code rules
+    // value code rules, an area that first holds the key min/max partials
+    const long long vr = (long long)ntiles_of(G) * TILE * (d / 32) * 16;
+    const long long kp = (long long)(FLUSH_THREADS / (d / 2)) * 2 * d * 4;
+    const long long t = b + (vr > kp ? vr : kp);
+    return t > (1LL << 30) ? (1 << 30) : (int)t;
 }
 
 cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
@@ -512,6 +734,9 @@ FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV,
     a.ftop = c->ftop;
     a.ctl = c->ctl;
     a.src_u0 = 0;
+    a.phist = nullptr;
+    a.pf_nf = 0;
+    a.pf_u0 = 0;
     a.src_unit_stride = src_unit_stride;
     a.src_mod = src_mod;
     a.t0 = t0;
@@ -546,6 +771,48 @@ cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *s
     none.n = 0;
     return run_flush(c, flush_args(c, srcK, srcV, src_unit_stride, src_mod, t0, j), none, c->U, s);
 }
+
+bool prefill_parallel_ok(const ott_cache *c, int nf) {
+    // the cold pool and the channel criterion carry state that a flush needs
+    // from the one before it; the others take the parallel path from two groups on
+    return c->cold < 0 && c->pct < 0 && nf >= 2;
+}
+
+cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, const __half *srcV,
+                                    long long src_unit_stride, int src_u0, int u0, int nu, int nf,
+                                    uint64_t *scratch, cudaStream_t s) {
+    if (nu <= 0 || nf <= 0) return cudaSuccess;
+    const int G = c->G, P = c->P;
+    uint64_t *gtop = scratch, *phist = scratch + (size_t)nu * nf * P;
+    const long long groups = (long long)nu * nf;
+    if (groups > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t e = cudaSuccess;
+    if (P > 0) {   // with no pool every block is its own group: pass 3 alone
+    if (c->d == 128)
+        k_pf_group<128><<<(int)groups, PF_THREADS, (size_t)G * 8, s>>>(srcK, src_unit_stride, src_u0, u0, nf, G, P,
+                                                                      gtop);
+    else
+        k_pf_group<64><<<(int)groups, PF_THREADS, (size_t)G * 8, s>>>(srcK, src_unit_stride, src_u0, u0, nf, G, P,
+                                                                     gtop);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    constexpr int SCAN_WARPS = 4;
+    k_pf_scan<<<(nu + SCAN_WARPS - 1) / SCAN_WARPS, 32 * SCAN_WARPS, (size_t)SCAN_WARPS * 4 * P * 8, s>>>(
+        gtop, phist, nu, nf, G, P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    }
+    FlushArgs a = flush_args(c, srcK, srcV, src_unit_stride, LLONG_MAX, 0, 0);
+    a.src_u0 = src_u0;
+    a.phist = phist;
+    a.pf_nf = nf;
+    a.pf_u0 = u0;
+    FlushList none;
+    none.n = 0;
+    return run_flush(c, a, none, (int)groups, s);
+}
+
+size_t prefill_scratch_bytes(const ott_cache *c, int nu, int nf) { return (size_t)2 * nu * nf * c->P * 8 + 16; }
 
 cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __half *srcV,
                               long long src_unit_stride, long long src_mod, const FlushList &fl,

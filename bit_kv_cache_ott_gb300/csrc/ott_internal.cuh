@@ -212,6 +212,14 @@ cudaError_t launch_flush_list_src(const ott_cache *c, const __half *srcK, const 
                                   long long src_unit_stride, long long src_mod, int src_u0, const FlushList &fl,
                                   cudaStream_t s);
 cudaError_t launch_release(const ott_cache *c, int b, cudaStream_t s);
+// Parallel prefill of units [u0, u0 + nu), nf flushes each, from a source
+// holding unit u at (u - src_u0) * src_unit_stride; scratch of
+// prefill_scratch_bytes(c, nu, nf) bytes on the device.
+bool prefill_parallel_ok(const ott_cache *c, int nf);
+size_t prefill_scratch_bytes(const ott_cache *c, int nu, int nf);
+cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, const __half *srcV,
+                                    long long src_unit_stride, int src_u0, int u0, int nu, int nf,
+                                    uint64_t *scratch, cudaStream_t s);
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
 cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s);
 cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s);

@@ -82,3 +82,27 @@ def topk_bytes(T: int, B: int, Hq: int, Hkv: int, d: int, G: int, R: int, P: int
 def fp16_cache_bytes(T: int, B: int, Hkv: int, d: int) -> int:
     """The same cache held entirely in fp16 (K and V)."""
     return B * Hkv * T * d * 4
+
+
+def block_bytes(d: int, G: int) -> int:
+    """One packed block as stored: K scale/zero per channel (4d), then per 16
+    token slots the K and V codes and the V scale/zero (10d)."""
+    return 4 * d + -(-G // 16) * 10 * d
+
+
+def flush_bytes_per_unit(j: int, d: int, G: int, P: int) -> int:
+    """Algorithmic bytes of flush j of one (sequence, kv head) unit: read the
+    group's G fp16 tokens and the pool's tokens (K and V, 4d each) with the
+    pool's norms and indices (8 each); write the packed block, its G token
+    indices, and the new pool (tokens, norms, indices)."""
+    np0, np1 = min(P, j * G), min(P, (j + 1) * G)
+    return G * 4 * d + np0 * (4 * d + 8) + block_bytes(d, G) + 4 * G + np1 * (4 * d + 8)
+
+
+def prefill_bytes_per_unit(L: int, d: int, G: int, R: int, P: int) -> int:
+    """Algorithmic bytes of a prefill of L tokens into one empty unit: read
+    every token once (K and V); write the nf packed blocks with their token
+    indices, the final pool (tokens, norms, indices) and the fp16 residual."""
+    nf = flush_count(L, G, R)
+    return (L * 4 * d + nf * (block_bytes(d, G) + 4 * G) + pool_size(L, G, R, P) * (4 * d + 8)
+            + (L - nf * G) * 4 * d)
