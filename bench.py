@@ -637,6 +637,26 @@ def run_ours(args, w):
                "d2h_bytes_per_step": int(out_h[0].numel() * out_h[0].element_size()), "steps": E_steps,
                "copies": "k, v, q in one pinned host buffer per step, double-buffered on a second stream"}
 
+    # the prefill of one layer's cache (the parallel pass), timed on its own
+    pf = None
+    if not args.no_prefill:
+        pf = measure_prefill(ott, w, wr, dev, stream)
+        pf_ms = max_over_ranks(pf["ms"], dev)
+        pf.update(ms=pf_ms, tokens_per_s=ws * pf["tokens"] / (pf_ms * 1e-3),
+                  gbs=ws * pf["algorithmic_bytes"] / (pf_ms * 1e-3) / 1e9, n_gpus=ws)
+        pf["frac_of_hbm_peak"] = pf["gbs"] / ws / hbm_peak()[0]
+
+    # one decode-time flush (every unit packs one group): its bytes against its time
+    flush_roof = None
+    if flush_us:
+        nf_now = metrics.flush_count(T0, w.G, w.R)
+        fb = w.B * w.Hkv * metrics.flush_bytes_per_unit(nf_now, w.d, w.G, w.P)
+        flush_roof = {"kernel": "k_flush (one group of every unit)", "algorithmic_bytes": fb,
+                      "achieved_gbs": fb / (flush_us * 1e-6) / 1e9,
+                      "frac_of_hbm_peak": fb / (flush_us * 1e-6) / 1e9 / hbm_peak()[0],
+                      "timing": "CUDA events around each append of one flush cycle: the appends that flush "
+                                "minus the median of those that do not"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate1, dt1, sample1 = oracle_rate(w, args.oracle_steps, 1, args.oracle_units)
@@ -668,7 +688,8 @@ def run_ours(args, w):
                               f"cache {cache_bytes / 1e6:.0f} MB > 2 x L2 {L2_BYTES / 1e6:.0f} MB, no flush needed"),
                        "parallelism": f"weak-scaled shards x{ws}" if ws > 1 else "1 GPU"},
             "ms_per_step_measured": ms / K_steps,
-            "flush": {"us_per_flush": flush_us, "flush_steps_in_timed_region": flush_steps,
+            "prefill": pf,
+            "flush": {"us_per_flush": flush_us, "flush_steps_in_timed_region": flush_steps, "roofline": flush_roof,
                       "charged": (f"one flush per {w.G} steps: {K_steps / w.G:.3f} flushes for {K_steps} steps, "
                                   f"{flush_steps} timed" if flush_us is not None else
                                   "ragged batch: its timed steps hold their own flushes")},
@@ -717,6 +738,7 @@ def main(argv=None):
     ap.add_argument("--oracle-units-per-core", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-peak", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
