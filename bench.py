@@ -650,8 +650,9 @@ def run_ours(args, w):
     flush_roof = None
     if flush_us:
         nf_now = metrics.flush_count(T0, w.G, w.R)
-        fb = w.B * w.Hkv * metrics.flush_bytes_per_unit(nf_now, w.d, w.G, w.P)
-        flush_roof = {"kernel": "k_flush (one group of every unit)", "algorithmic_bytes": fb,
+        # one flush of every unit of every layer (each layer has its own cache)
+        fb = w.layers * w.B * w.Hkv * metrics.flush_bytes_per_unit(nf_now, w.d, w.G, w.P)
+        flush_roof = {"kernel": "k_flush (one group of every unit, every layer)", "algorithmic_bytes": fb,
                       "achieved_gbs": fb / (flush_us * 1e-6) / 1e9,
                       "frac_of_hbm_peak": fb / (flush_us * 1e-6) / 1e9 / hbm_peak()[0],
                       "timing": "CUDA events around each append of one flush cycle: the appends that flush "

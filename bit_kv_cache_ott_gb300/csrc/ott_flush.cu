@@ -146,8 +146,13 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
     // code rules: per channel for keys, per (token, 32 channels) for values;
     // the value area first holds the key min/max partials
     const size_t rule_off = ((size_t)(reinterpret_cast<uint8_t *>(emap + (P > 0 ? P : 1)) - smem) + 15) & ~(size_t)15;
+    // Rule arrays are skewed by one entry per 8 so that the pack phase's
+    // loads (8 channels or 8 tokens, 2 apart, per warp) hit distinct banks:
+    // channel ch at krule[ch + ch/8]; token t of value group g at
+    // vrule[g*VS + t + t/8].
     float4 *krule = reinterpret_cast<float4 *>(smem + rule_off);
-    float4 *vrule = krule + D;
+    float4 *vrule = krule + D + D / 8;
+    const int TS = a.ntile * TILE, VS = TS + TS / 8;
     float *ks = reinterpret_cast<float *>(krule);   // channel criterion scratch (before the rules)
     float *kz = ks + D;
     const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
@@ -400,14 +405,15 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
                     z16 = __float2half_rn(lo);
                 }
                 reinterpret_cast<uint32_t *>(bb)[ch] = half2_bits(s16, z16);
-                krule[ch] = code_rule(__half2float(s16), __half2float(z16));
+                krule[ch + (ch >> 3)] = code_rule(__half2float(s16), __half2float(z16));
             }
         }
         __syncthreads();   // the partials are read before the value rules overwrite them
     }
-    // 7. values: one (scale, zero) per token per 32 channels
-    for (int e = tid; e < a.ntile * TILE * NG; e += nth) {
-        const int t = e / NG, gm = e % NG;
+    // 7. values: one (scale, zero) per token per 32 channels (consecutive
+    // threads take consecutive tokens of one group)
+    for (int e = tid; e < TS * NG; e += nth) {
+        const int t = e % TS, gm = e / TS;
         __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
         if (t < cnt) {
             const uint4 *row = reinterpret_cast<const uint4 *>(cv + (size_t)bmap[t] * RS + 32 * gm);
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             const float mn = okey_lo(m0), mx = okey_lo(m1);
             s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
             z16 = __float2half_rn(mn);
-            vrule[t * NG + gm] = code_rule(__half2float(s16), __half2float(z16));
+            vrule[gm * VS + t + (t >> 3)] = code_rule(__half2float(s16), __half2float(z16));
         }
         uint8_t *tb = tiles + (size_t)(t / TILE) * tile_bytes(D) + tile_sz_off(D);
         reinterpret_cast<uint32_t *>(tb)[vsz_index(t, gm)] = half2_bits(s16, z16);
@@ -448,8 +454,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
                 // K word: channels 16kt + 2i + 8o (+1) of token tk
                 const int q = 8 * wp + p, o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
                 const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(krow + ch));
-                kw |= qcode(f.x, krule[ch]) << (2 * p);
-                kw |= qcode(f.y, krule[ch + 1]) << (16 + 2 * p);
+                kw |= qcode(f.x, krule[ch + (ch >> 3)]) << (2 * p);
+                kw |= qcode(f.y, krule[ch + 1 + ((ch + 1) >> 3)]) << (16 + 2 * p);
             }
         }
         // V word: channel 16mt + r + 8rowhalf of token slots 16tau + 2i + 8hi (+1)
@@ -458,11 +464,11 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             const int tv = TILE * tau + 2 * i + 8 * hi + h;
             if (tv < cnt) {
                 const __half *vrow = cv + (size_t)bmap[tv] * RS;
-                const float4 *vr = vrule + tv * NG;
+                const float4 *vr = vrule + tv + (tv >> 3);
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const int q = 8 * wp + p, rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
-                    vw |= qcode(__half2float(vrow[vch]), vr[vch / 32]) << (16 * h + 2 * p);
+                    vw |= qcode(__half2float(vrow[vch]), vr[(vch / 32) * VS]) << (16 * h + 2 * p);
                 }
             }
         }
@@ -693,9 +699,10 @@ int flush_smem_bytes(int d, int G, int P) {
                         + nc * 4 + (long long)G * 4           // ranks, block map
                         + (long long)(P > 0 ? P : 1) * 4      // cold order
                         + 16                                  // alignment of the code rules
-                        + (long long)d * 16;                  // key code rules
-    // value code rules, an area that first holds the key min/max partials
-    const long long vr = (long long)ntiles_of(G) * TILE * (d / 32) * 16;
+                        + (long long)(d + d / 8) * 16;        // key code rules (skewed)
+    // value code rules (skewed), an area that first holds the key min/max partials
+    const long long ts = (long long)ntiles_of(G) * TILE;
+    const long long vr = (ts + ts / 8) * (d / 32) * 16;
     const long long kp = (long long)(FLUSH_THREADS / (d / 2)) * 2 * d * 4;
     const long long t = b + (vr > kp ? vr : kp);
     return t > (1LL << 30) ? (1 << 30) : (int)t;
