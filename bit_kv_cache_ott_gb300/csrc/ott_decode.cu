@@ -168,9 +168,9 @@ struct Cfg {
     static constexpr int GPV = 4 / GQ;             // value groups per PV B variant
     static constexpr int NV = (NG + GPV - 1) / GPV;  // PV B variants
     static constexpr int STAGE = stage_bytes(D);
-    static constexpr bool COOP = GQ <= 2;          // per-block constants computed cooperatively
-    static constexpr int QHL = COOP ? GQ * 2 * (D + 8) * 2 : 0;   // hi/lo staging bytes
-    static constexpr int WARP_SMEM = 2 * STAGE + 16 + GQ * D * 4 + QHL;
+    static constexpr int QHL = GQ * 2 * (D + 8) * 2;   // per-block hi/lo staging bytes
+    // stages, barriers, the queries (fp16, as given) and the hi/lo staging
+    static constexpr int WARP_SMEM = 2 * STAGE + 16 + GQ * D * 2 + QHL;
     // the fp16 path stages 8 key and 8 value rows of d+8 halves in each of
     // the same two stage buffers
     static_assert(2 * 8 * (D + 8) * 2 <= STAGE, "fp16 sub-tile staging must fit a stage buffer");
@@ -268,11 +268,7 @@ template <int D, int GQ>
 __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
     const int b = u / a.Hkv, hkv = u % a.Hkv;
     const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + hkv * GQ) * D);
-    for (int e = lane; e < GQ * D / 2; e += 32) {
-        const float2 f = __half22float2(qp[e]);
-        qsm[2 * e] = f.x;
-        qsm[2 * e + 1] = f.y;
-    }
+    for (int e = lane; e < GQ * D / 2; e += 32) reinterpret_cast<__half2 *>(qsm)[e] = qp[e];
     __syncwarp();
 }
 
@@ -374,7 +370,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
     // for the whole segment.
     constexpr int NPAIR = D / 64;
     float clsf[NPAIR];
-    if constexpr (C::COOP) {
+    {
 #pragma unroll
         for (int m = 0; m < NPAIR; ++m) {
             const int ch = 2 * lane + 64 * m;
@@ -413,7 +409,6 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
     // i mod GQ.
     const int hB = (r >> 1) % GQ;
     const bool piece = (r & 1) != 0;
-    const float pm = piece ? 1.0f : 0.0f;
     const int hS = i % GQ;
     // PV B column of this lane: head hV, value-group offset glow, piece
     const int hV = (r >> 1) / GPV, glow = (r >> 1) % GPV;
@@ -445,7 +440,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
             const uint32_t *ksz = reinterpret_cast<const uint32_t *>(stage);
             int Eh[GQ];
             float qzh[GQ];
-            if constexpr (C::COOP) {
+            {
                 float2 xs[GQ][NPAIR];
 #pragma unroll
                 for (int h = 0; h < GQ; ++h) {
@@ -456,7 +451,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                         const uint2 sz2 = *reinterpret_cast<const uint2 *>(ksz + 2 * lane + 64 * m);
                         const float2 e0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.x));
                         const float2 e1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz2.y));
-                        const float2 qv = *reinterpret_cast<const float2 *>(qsm + h * D + 2 * lane + 64 * m);
+                        const float2 qv = __half22float2(reinterpret_cast<const __half2 *>(qsm)[(h * D + 2 * lane + 64 * m) / 2]);
                         xs[h][m] = __fmul2_rn(qv, make_float2(e0.x, e1.x));
                         qz2 = __ffma2_rn(qv, make_float2(e0.y, e1.y), qz2);
                         amax = fmaxf(amax, fmaxf(fabsf(xs[h][m].x), fabsf(xs[h][m].y)));
@@ -492,46 +487,6 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
                     for (int o = 0; o < 2; ++o)
                         Bk[kt][o] = *reinterpret_cast<const uint32_t *>(row + 16 * kt + 2 * i + 8 * o);
                 __syncwarp();
-            } else {
-                // every lane computes its own 32 values (all columns are live)
-                const float *qrow = qsm + hB * D;
-                float qs[NKT][2][2];
-                float amax = 0.0f, qz = 0.0f;
-#pragma unroll
-                for (int kt = 0; kt < NKT; ++kt)
-#pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const uint2 sz = *reinterpret_cast<const uint2 *>(ksz + 16 * kt + 2 * i + 8 * o);
-                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.x));
-                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&sz.y));
-                        const float2 qq = *reinterpret_cast<const float2 *>(qrow + 16 * kt + 2 * i + 8 * o);
-                        qs[kt][o][0] = qq.x * f0.x;
-                        qs[kt][o][1] = qq.y * f1.x;
-                        qz = fmaf(qq.x, f0.y, qz);
-                        qz = fmaf(qq.y, f1.y, qz);
-                        amax = fmaxf(amax, fmaxf(fabsf(qs[kt][o][0]), fabsf(qs[kt][o][1])));
-                    }
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                qz += __shfl_xor_sync(0xffffffffu, qz, 1);
-                qz += __shfl_xor_sync(0xffffffffu, qz, 2);
-                const int E = amax > 0.0f ? min(max(14 - (((__float_as_int(amax) >> 23) & 0xff) - 127), -100), 100) : 0;
-#pragma unroll
-                for (int kt = 0; kt < NKT; ++kt)
-#pragma unroll
-                    for (int o = 0; o < 2; ++o) {
-                        const float sc = pow2i(E - 2 * cls_of_pos((o * NKT + kt) & 7));
-                        const float x0 = qs[kt][o][0] * sc, x1 = qs[kt][o][1] * sc;
-                        const __half2 hh = __floats2half2_rn(x0, x1);
-                        const float2 hf = __half22float2(hh);
-                        Bk[kt][o] = h2bits(__floats2half2_rn(x0 - pm * hf.x, x1 - pm * hf.y));
-                    }
-                // lane 8h holds head h (piece 0)
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) {
-                    Eh[h] = __shfl_sync(0xffffffffu, E, 8 * h);
-                    qzh[h] = __shfl_sync(0xffffffffu, qz, 8 * h);
-                }
             }
             // score constants of head hS: logit = raw * c1 + c0 (c1 > 0)
             int Ei = Eh[0];
@@ -843,8 +798,8 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
     for (int kt = 0; kt < NKT; ++kt)
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
-            const float2 qq = *reinterpret_cast<const float2 *>(qsm + (hB < GQ ? hB : 0) * D + 16 * kt + 2 * i + 8 * o);
-            Bq[kt][o] = (hB < GQ && (r & 1) == 0) ? h2bits(__floats2half2_rn(qq.x, qq.y)) : 0u;
+            const __half2 qq = reinterpret_cast<const __half2 *>(qsm)[((hB < GQ ? hB : 0) * D + 16 * kt + 2 * i + 8 * o) / 2];
+            Bq[kt][o] = (hB < GQ && (r & 1) == 0) ? h2bits(qq) : 0u;
         }
     float acc[NKT][4];
 #pragma unroll
@@ -938,7 +893,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
     uint8_t *stg1 = wbase + C::STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(wbase + 2 * C::STAGE);
     float *qsm = reinterpret_cast<float *>(wbase + 2 * C::STAGE + 16);
-    __half *qhl = reinterpret_cast<__half *>(wbase + 2 * C::STAGE + 16 + GQ * D * 4);
+    __half *qhl = reinterpret_cast<__half *>(wbase + 2 * C::STAGE + 16 + GQ * D * 2);
     if (lane == 0) {
         mbar_init(&bars[0]);
         mbar_init(&bars[1]);
