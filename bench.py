@@ -342,18 +342,21 @@ def copy_peak(ott, dev, stream, gib: int = 2, reps: int = 10):
             "method": f"{gib} GiB read + {gib} GiB written per call, best of {reps} CUDA-event-timed calls"}
 
 
-def prefill_launches(w, lens) -> int:
+def prefill_launches(w, lens, sm_count: int) -> int:
     """Kernel launches of one layer's prefill, as the library issues them:
-    a prompt of two or more groups takes the parallel pass (group keys, pool
-    scan, every block at once; with P = 0 the blocks alone), except under the
-    cold-pool policy, whose flushes run group by group; then the residual
-    tokens are copied (one launch, or one per sequence of a ragged batch)."""
+    when fewer (sequence, kv head) units flush than the GPU has SMs, a prompt
+    of two or more groups takes the parallel pass (group keys, pool scan,
+    every block at once; with P = 0 the blocks alone); otherwise, and under
+    the cold-pool policy, the flushes run group by group (one launch per
+    group for all units that have it). Then the residual tokens are copied
+    (one launch, or one per sequence of a ragged batch)."""
     nfs = [metrics.flush_count(L, w.G, w.R) for L in lens]
     par_cost = 3 if w.P > 0 else 1
+    few = w.B * w.Hkv < sm_count
     if not w.ragged:
         nf = nfs[0]
-        return (par_cost if (nf >= 2 and w.cold < 0) else nf) + 1
-    par = [nf >= 2 and w.cold < 0 for nf in nfs]
+        return (par_cost if (nf >= 2 and w.cold < 0 and few) else nf) + 1
+    par = [nf >= 2 and w.cold < 0 and few for nf in nfs]
     serial = max([nf for nf, p in zip(nfs, par) if not p], default=0)
     return par_cost * sum(par) + serial + len(lens)
 
@@ -391,7 +394,8 @@ def measure_prefill(ott, w, wr, dev, stream, reps: int = 3):
     nbytes = sum(metrics.prefill_bytes_per_unit(L, w.d, w.G, w.R, w.P) for L in lens) * w.Hkv
     return {"ms": ms, "tokens": sum(lens), "tokens_per_s": sum(lens) / (ms * 1e-3),
             "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
-            "launches": prefill_launches(w, lens), "reps": reps,
+            "launches": prefill_launches(w, lens, torch.cuda.get_device_properties(dev).multi_processor_count),
+            "reps": reps,
             "timing": "CUDA events around the prefill call into a fresh cache, median of "
                       f"{reps} after one warm-up; bytes: every prompt token read once (K and V), "
                       "blocks with token indices, final pool and fp16 residual written"}

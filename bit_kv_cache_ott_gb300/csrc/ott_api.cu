@@ -69,12 +69,13 @@ void to_per_sequence(ott_cache *c) {
 
 // Every flush of units [u0, u0 + nu), nf each, in one parallel pass (the
 // source holds unit u at (u - src_u0) * unit_stride). False when the policy
-// needs the flushes one after another or no scratch could be had: the caller
-// then flushes group by group.
+// needs the flushes one after another, when the call flushes enough units
+// (units_flushing) for group-by-group launches to fill the GPU, or when no
+// scratch could be had: the caller then flushes group by group.
 bool try_prefill_parallel(const ott_cache *c, const __half *K, const __half *V, long long unit_stride, int src_u0,
-                          int u0, int nu, int nf, cudaStream_t s, cudaError_t &err) {
+                          int u0, int nu, int nf, int units_flushing, cudaStream_t s, cudaError_t &err) {
     err = cudaSuccess;
-    if (!prefill_parallel_ok(c, nf)) return false;
+    if (!prefill_parallel_ok(c, nf, units_flushing)) return false;
     void *scratch = nullptr;
     if (cudaMallocAsync(&scratch, prefill_scratch_bytes(c, nu, nf), s) != cudaSuccess) {
         cudaGetLastError();
@@ -323,7 +324,7 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     if (blocks_needed(c, (long long)nf * c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, (long long)nf * c->U);
     cudaError_t e = cudaSuccess;
-    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, s, e)) {
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, c->U, s, e)) {
         for (int j = 0; j < nf && e == cudaSuccess; ++j)
             e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
     }
@@ -364,7 +365,7 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
     for (int b = 0; b < c->B; ++b) {
         cudaError_t e = cudaSuccess;
         done[b] = try_prefill_parallel(c, Kh, Vh, (long long)Lmax * c->d, 0, b * c->Hkv, c->Hkv,
-                                       flushes_after(c, lens[b]), s, e);
+                                       flushes_after(c, lens[b]), c->U, s, e);
         if (e != cudaSuccess) return fail_cuda(c, e);
     }
     for (int j = 0; j < nf_max; ++j) {
@@ -509,7 +510,7 @@ int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     cudaError_t e = cudaSuccess;
-    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, b * c->Hkv, b * c->Hkv, c->Hkv, nf, s, e)) {
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, b * c->Hkv, b * c->Hkv, c->Hkv, nf, c->Hkv, s, e)) {
         for (int j = 0; j < nf && e == cudaSuccess; ++j) {
             FlushList fl;
             fl.n = 1;
