@@ -533,48 +533,97 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Pass 2, one warp per unit: the pool after flush j (ascending keys) is the
-// first min(P, pool + G) of the merge of the pool after flush j - 1 with
-// group j's smallest keys. Lane k finds output k by a binary search on the
-// merge path; the next group's keys arrive by cp.async during the merge.
-__global__ void k_pf_scan(const uint64_t *__restrict__ gtop, uint64_t *__restrict__ phist, int nu, int nf, int G,
-                          int P) {
-    extern __shared__ uint64_t scan_sm[];   // per warp: two pool lists, two group lists
-    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int uu = blockIdx.x * (blockDim.x >> 5) + wib;
-    if (uu >= nu) return;
-    uint64_t *A = scan_sm + (size_t)wib * 4 * P, *Cn = A + P, *Bc = Cn + P, *Bn = Bc + P;
+// Output k (0-based) of the merge of the ascending lists A (na keys) and B
+// (nb keys), all keys distinct, k < na + nb: a binary search on the merge
+// path for the number of A's keys among the first k + 1.
+__device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int na, const uint64_t *B, int nb, int k) {
+    int lo = max(0, k + 1 - nb), hi = min(k + 1, na);
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] < B[k - mid]) lo = mid + 1;
+        else hi = mid;
+    }
+    uint64_t x = lo > 0 ? A[lo - 1] : 0ull;
+    if (k - lo >= 0) {
+        const uint64_t y = B[k - lo];
+        x = y > x ? y : x;
+    }
+    return x;
+}
+
+// Pass 2, one CTA per unit: the pool after flush j (ascending keys) is the
+// smallest min(P, (j + 1) G) of groups 0..j's smallest keys. Keeping the
+// smallest of a union is associative, so it runs as a two-level scan:
+//   1. warp c scans its chunk of groups [j0, j1) alone: the local prefix
+//      after group j (the smallest of groups j0..j), written to the history;
+//   2. warp 0 carries across the chunks: the smallest of groups 0..j0 - 1
+//      for every chunk;
+//   3. warp c merges its chunk's carry into each local prefix.
+// The dependent merges per unit drop from nf to about 3 nf / warps + warps.
+// Lanes find their outputs by merge_at; the next group's keys arrive by
+// cp.async during a merge.
+constexpr int SCAN_WARPS = 16;
+
+__global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__restrict__ gtop,
+                                                             uint64_t *__restrict__ phist, int nf, int G, int P) {
+    extern __shared__ uint64_t scan_sm[];   // per warp 4 lists; then chunk totals and carries
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int uu = blockIdx.x;
+    uint64_t *A = scan_sm + (size_t)w * 4 * P, *Cn = A + P, *Bc = Cn + P, *Bn = Bc + P;
+    uint64_t *tot = scan_sm + (size_t)nw * 4 * P, *car = tot + (size_t)nw * P;
     const int nb = min(P, G);
     const uint64_t *gt = gtop + (size_t)uu * nf * P;
     uint64_t *ph = phist + (size_t)uu * nf * P;
-    for (int k = lane; k < nb; k += 32) Bc[k] = gt[k];
-    __syncwarp();
-    int na = 0;
-    for (int j = 0; j < nf; ++j) {
-        if (j + 1 < nf)
-            for (int k = lane; k < nb; k += 32) cp_async8(Bn + k, gt + (size_t)(j + 1) * P + k);
-        const int m = (int)min((long long)P, (long long)na + G);
-        for (int k = lane; k < m; k += 32) {
-            // i = keys taken from A among the first k + 1 of the merge
-            int lo = max(0, k + 1 - nb), hi = min(k + 1, na);
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (A[mid] < Bc[k - mid]) lo = mid + 1;
-                else hi = mid;
-            }
-            uint64_t x = lo > 0 ? A[lo - 1] : 0ull;
-            if (k - lo >= 0) {
-                const uint64_t y = Bc[k - lo];
-                x = y > x ? y : x;
-            }
-            Cn[k] = x;
-            ph[(size_t)j * P + k] = x;
-        }
-        cp_async_wait_all();
+    const int j0 = (int)((long long)nf * w / nw), j1 = (int)((long long)nf * (w + 1) / nw);
+    // 1. local prefixes of this warp's chunk
+    if (j0 < j1) {
+        for (int k = lane; k < nb; k += 32) Bc[k] = gt[(size_t)j0 * P + k];
         __syncwarp();
-        uint64_t *t = A; A = Cn; Cn = t;
-        t = Bc; Bc = Bn; Bn = t;
-        na = m;
+        int na = 0;
+        for (int j = j0; j < j1; ++j) {
+            if (j + 1 < j1)
+                for (int k = lane; k < nb; k += 32) cp_async8(Bn + k, gt + (size_t)(j + 1) * P + k);
+            const int m = (int)min((long long)P, (long long)na + G);
+            for (int k = lane; k < m; k += 32) {
+                const uint64_t x = merge_at(A, na, Bc, nb, k);
+                Cn[k] = x;
+                ph[(size_t)j * P + k] = x;
+            }
+            cp_async_wait_all();
+            __syncwarp();
+            uint64_t *t = A; A = Cn; Cn = t;
+            t = Bc; Bc = Bn; Bn = t;
+            na = m;
+        }
+        for (int k = lane; k < na; k += 32) tot[(size_t)w * P + k] = A[k];
+    }
+    __syncthreads();
+    // 2. carries: car[c] = the smallest min(P, j0(c) G) keys of groups before chunk c
+    if (w == 0) {
+        int nc = 0;
+        for (int c = 1; c < nw; ++c) {
+            const int pj0 = (int)((long long)nf * (c - 1) / nw), pj1 = (int)((long long)nf * c / nw);
+            const int nt = (int)min((long long)P, (long long)(pj1 - pj0) * G);
+            const int m = (int)min((long long)P, (long long)pj1 * G);
+            for (int k = lane; k < m; k += 32)
+                car[(size_t)c * P + k] = merge_at(car + (size_t)(c - 1) * P, nc, tot + (size_t)(c - 1) * P, nt, k);
+            __syncwarp();
+            nc = m;
+        }
+    }
+    __syncthreads();
+    // 3. the pool after group j: the carry merged with the local prefix
+    if (w > 0 && j0 < j1) {
+        const int ncar = (int)min((long long)P, (long long)j0 * G);
+        const uint64_t *cw = car + (size_t)w * P;
+        for (int j = j0; j < j1; ++j) {
+            const int nl = (int)min((long long)P, (long long)(j - j0 + 1) * G);
+            const int m = (int)min((long long)P, (long long)(j + 1) * G);
+            for (int k = lane; k < nl; k += 32) Bc[k] = ph[(size_t)j * P + k];
+            __syncwarp();
+            for (int k = lane; k < m; k += 32) ph[(size_t)j * P + k] = merge_at(cw, ncar, Bc, nl, k);
+            __syncwarp();
+        }
     }
 }
 
@@ -807,9 +856,8 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
                                                                      gtop);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    constexpr int SCAN_WARPS = 4;
-    k_pf_scan<<<(nu + SCAN_WARPS - 1) / SCAN_WARPS, 32 * SCAN_WARPS, (size_t)SCAN_WARPS * 4 * P * 8, s>>>(
-        gtop, phist, nu, nf, G, P);
+    const int sw = nf < SCAN_WARPS ? nf : SCAN_WARPS;
+    k_pf_scan<<<nu, 32 * sw, (size_t)sw * P * 6 * 8, s>>>(gtop, phist, nf, G, P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     }
@@ -917,6 +965,8 @@ cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *s
 }
 
 cudaError_t set_flush_attributes(int d, int smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_pf_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     if (d == 128) return cudaFuncSetAttribute(k_flush<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     return cudaFuncSetAttribute(k_flush<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
