@@ -60,6 +60,21 @@ __device__ __forceinline__ uint32_t qcode(float x, const float4 &r) {
     return (uint32_t)(a > r.y) + (uint32_t)(a >= r.z) + (uint32_t)(a > r.w);
 }
 
+// Position of channel ch within staged row r: the row's 16-byte chunks are
+// permuted by XOR with r mod 8.
+__device__ __forceinline__ int SWZ(int r, int ch) { return (((ch >> 3) ^ (r & 7)) << 3) | (ch & 7); }
+
+// Staged-row layout: padded rows (stride D + 8 halves, no address
+// arithmetic) or unpadded swizzled rows (stride D, chunk index XOR r mod 8),
+// which save 16 bytes per row where the padding would cost a second CTA per
+// SM.
+template <int D, bool SW>
+struct Rows {
+    static constexpr int RS = SW ? D : D + 8;
+    __device__ static __forceinline__ int pos(int r, int ch) { return SW ? SWZ(r, ch) : ch; }
+    __device__ static __forceinline__ int chunk(int r, int v8) { return SW ? (v8 ^ (r & 7)) : v8; }
+};
+
 // Two fp16 values (bit patterns, one per 16-bit lane) -> 16-bit signed keys
 // in the values' order, with -0 below +0 (so that min and max do not depend
 // on the order the values come in): a negative value keeps its sign bit and
@@ -111,10 +126,12 @@ struct FlushArgs {
 // One CTA per unit. Without a list, CTA u flushes group a.j of unit u; with
 // one (ragged batches), CTA i flushes group fl.lj[i / Hkv] of kv head i % Hkv
 // of sequence fl.lb[i / Hkv].
-template <int D>
+template <int D, bool SW>
 __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const __grid_constant__ FlushList fl) {
     extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int RS = D + 8;          // padded row stride (halves): 16B-aligned rows
+    // Staged rows are D halves, unpadded; the 16-byte chunks of row r are
+    // permuted by XOR with r mod 8 (SWZ), so that the same chunk of 8
+    // consecutive rows falls on 8 different bank groups.
     constexpr int VPR = D / 8;         // 16-byte vectors per row
     constexpr int NG = D / 32;         // value groups
     constexpr int NKT = D / 16;
@@ -138,6 +155,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
     const int np0 = (a.phist || fl.n > 0) ? pool_after(P, G, jj, a.pct) : a.np0, nc = np0 + G;
 
     __half *ck = reinterpret_cast<__half *>(smem);
+    using RL = Rows<D, SW>;
+    constexpr int RS = RL::RS;
     __half *cv = ck + (size_t)nc * RS;
     uint64_t *key = reinterpret_cast<uint64_t *>(cv + (size_t)nc * RS);
     int *rank = reinterpret_cast<int *>(key + nc);
@@ -176,8 +195,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             sk = a.srcK + off;
             sv = a.srcV + off;
         }
-        reinterpret_cast<uint4 *>(ck + (size_t)row * RS)[v8] = reinterpret_cast<const uint4 *>(sk)[v8];
-        reinterpret_cast<uint4 *>(cv + (size_t)row * RS)[v8] = reinterpret_cast<const uint4 *>(sv)[v8];
+        reinterpret_cast<uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)] = reinterpret_cast<const uint4 *>(sk)[v8];
+        reinterpret_cast<uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)] = reinterpret_cast<const uint4 *>(sv)[v8];
     }
     __syncthreads();
 
@@ -195,11 +214,17 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
                 nrm = a.pnorm[(size_t)u * P + row];
                 idx = a.pidx[(size_t)u * P + row];
             } else {
-                const __half *kr = ck + (size_t)row * RS;
+                const uint4 *kr = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS);
                 float s = 0.0f;
-                for (int ch = 0; ch < D; ++ch) {
-                    const float x = __half2float(kr[ch]);
-                    s = __fadd_rn(s, __fmul_rn(x, x));
+                for (int v8 = 0; v8 < VPR; ++v8) {   // channels 8 v8 .. 8 v8 + 7, in order
+                    const uint4 x = kr[RL::chunk(row, v8)];
+                    const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h[e]);
+                        s = __fadd_rn(s, __fmul_rn(f.x, f.x));
+                        s = __fadd_rn(s, __fmul_rn(f.y, f.y));
+                    }
                 }
                 nrm = s;
                 idx = (int)(t0 + (row - np0));
@@ -216,7 +241,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         int *csel = reinterpret_cast<int *>(kz);
         for (int ch = tid; ch < D; ch += nth) {
             float m = 0.0f;
-            for (int row = 0; row < nc; ++row) m = fmaxf(m, fabsf(__half2float(ck[(size_t)row * RS + ch])));
+            for (int row = 0; row < nc; ++row) m = fmaxf(m, fabsf(__half2float(ck[(size_t)row * RS + RL::pos(row, ch)])));
             camax[ch] = m;
         }
         __syncthreads();
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             float s = 0.0f;
             for (int ch = 0; ch < D; ++ch) {
                 if (!csel[ch]) continue;
-                const float x = __half2float(kr[ch]);
+                const float x = __half2float(kr[RL::pos(row, ch)]);
                 s = __fadd_rn(s, __fmul_rn(x, x));
             }
             const int idx = row < np0 ? a.pidx[(size_t)u * P + row] : (int)(t0 + (row - np0));
@@ -316,8 +341,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         const int row = e / VPR, v8 = e % VPR, rk = rank[row];
         if (rk < keep) {
             const size_t off = ((size_t)u * P + rk) * D;
-            reinterpret_cast<uint4 *>(a.pk + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[v8];
-            reinterpret_cast<uint4 *>(a.pv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[v8];
+            reinterpret_cast<uint4 *>(a.pk + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)];
+            reinterpret_cast<uint4 *>(a.pv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)];
         }
     }
     for (int row = tid; write_pool && row < nc; row += nth) {
@@ -339,8 +364,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
                 const int x = skip + e / VPR, v8 = e % VPR, row = emap[x];
                 const int slotc = (ch0 + cn0 + x) % a.C;
                 const size_t off = ((size_t)u * a.C + slotc) * D;
-                reinterpret_cast<uint4 *>(a.ck + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[v8];
-                reinterpret_cast<uint4 *>(a.cv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[v8];
+                reinterpret_cast<uint4 *>(a.ck + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)];
+                reinterpret_cast<uint4 *>(a.cv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)];
                 if (v8 == 0) a.cidx[(size_t)u * a.C + slotc] = (int32_t)(uint32_t)key[row];
             }
             if (tid == 0) {
@@ -382,7 +407,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         const int tb = (cnt * sl) / nsl, te = (cnt * (sl + 1)) / nsl;
         uint32_t mn = 0x7fff7fffu, mx = 0x80008000u;
         for (int t = tb; t < te; ++t) {
-            const uint32_t k2 = okey2(*reinterpret_cast<const uint32_t *>(ck + (size_t)bmap[t] * RS + 2 * cp));
+            const int rw = bmap[t];
+            const uint32_t k2 = okey2(*reinterpret_cast<const uint32_t *>(ck + (size_t)rw * RS + RL::pos(rw, 2 * cp)));
             mn = __vmins2(mn, k2);
             mx = __vmaxs2(mx, k2);
         }
@@ -416,11 +442,12 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         const int t = e % TS, gm = e / TS;
         __half s16 = __ushort_as_half(0), z16 = __ushort_as_half(0);
         if (t < cnt) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(cv + (size_t)bmap[t] * RS + 32 * gm);
+            const int rw = bmap[t];
+            const uint4 *row = reinterpret_cast<const uint4 *>(cv + (size_t)rw * RS);
             uint32_t m0 = 0x7fff7fffu, m1 = 0x80008000u;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint4 x = row[k];
+                const uint4 x = row[RL::chunk(rw, 4 * gm + k)];
                 const uint32_t w4[4] = {okey2(x.x), okey2(x.y), okey2(x.z), okey2(x.w)};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
@@ -448,12 +475,13 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         uint32_t kw = 0, vw = 0;
         const int tk = TILE * tau + r + 8 * hi;   // K: token slot of this word
         if (tk < cnt) {
-            const __half *krow = ck + (size_t)bmap[tk] * RS;
+            const int rk_ = bmap[tk];
+            const __half *krow = ck + (size_t)rk_ * RS;
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
                 // K word: channels 16kt + 2i + 8o (+1) of token tk
                 const int q = 8 * wp + p, o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(krow + ch));
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(krow + RL::pos(rk_, ch)));
                 kw |= qcode(f.x, krule[ch + (ch >> 3)]) << (2 * p);
                 kw |= qcode(f.y, krule[ch + 1 + ((ch + 1) >> 3)]) << (16 + 2 * p);
             }
@@ -463,12 +491,13 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
         for (int h = 0; h < 2; ++h) {
             const int tv = TILE * tau + 2 * i + 8 * hi + h;
             if (tv < cnt) {
-                const __half *vrow = cv + (size_t)bmap[tv] * RS;
+                const int rv_ = bmap[tv];
+                const __half *vrow = cv + (size_t)rv_ * RS;
                 const float4 *vr = vrule + tv + (tv >> 3);
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const int q = 8 * wp + p, rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
-                    vw |= qcode(__half2float(vrow[vch]), vr[(vch / 32) * VS]) << (16 * h + 2 * p);
+                    vw |= qcode(__half2float(vrow[RL::pos(rv_, vch)]), vr[(vch / 32) * VS]) << (16 * h + 2 * p);
                 }
             }
         }
@@ -562,7 +591,7 @@ __device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int na, const ui
 // The dependent merges per unit drop from nf to about 3 nf / warps + warps.
 // Lanes find their outputs by merge_at; the next group's keys arrive by
 // cp.async during a merge.
-constexpr int SCAN_WARPS = 16;
+constexpr int SCAN_WARPS = 32;
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__restrict__ gtop,
                                                              uint64_t *__restrict__ phist, int nf, int G, int P) {
@@ -741,9 +770,11 @@ __global__ void k_export(ExportArgs a) {
 
 }  // namespace
 
-int flush_smem_bytes(int d, int G, int P) {
+namespace {
+
+long long flush_smem_layout(int d, int G, int P, bool sw) {
     const long long nc = (long long)P + G;
-    const long long b = nc * (d + 8) * 2 * 2   // staged K and V rows
+    const long long b = nc * (sw ? d : d + 8) * 2 * 2   // staged K and V rows
                         + nc * 8               // keys
                         + nc * 4 + (long long)G * 4           // ranks, block map
                         + (long long)(P > 0 ? P : 1) * 4      // cold order
@@ -753,7 +784,25 @@ int flush_smem_bytes(int d, int G, int P) {
     const long long ts = (long long)ntiles_of(G) * TILE;
     const long long vr = (ts + ts / 8) * (d / 32) * 16;
     const long long kp = (long long)(FLUSH_THREADS / (d / 2)) * 2 * d * 4;
-    const long long t = b + (vr > kp ? vr : kp);
+    return b + (vr > kp ? vr : kp);
+}
+
+// Swizzled rows only where they let a second CTA share the SM (its 228 KB of
+// shared memory, 1 KB reserved per CTA) and padded rows would not: the
+// swizzle costs address arithmetic in an issue-bound kernel.
+bool flush_swizzle(int d, int G, int P) {
+    constexpr long long SM_SMEM = 228 * 1024, RESERVED = 1024;
+    const bool two_padded = 2 * (flush_smem_layout(d, G, P, false) + RESERVED) <= SM_SMEM;
+    const bool two_swizzled = 2 * (flush_smem_layout(d, G, P, true) + RESERVED) <= SM_SMEM;
+    return !two_padded && two_swizzled;
+}
+
+bool flush_swizzled(const ott_cache *c) { return flush_swizzle(c->d, c->G, c->P); }
+
+}  // namespace
+
+int flush_smem_bytes(int d, int G, int P) {
+    const long long t = flush_smem_layout(d, G, P, flush_swizzle(d, G, P));
     return t > (1LL << 30) ? (1 << 30) : (int)t;
 }
 
@@ -812,9 +861,11 @@ FlushArgs flush_args(const ott_cache *c, const __half *srcK, const __half *srcV,
 cudaError_t run_flush(const ott_cache *c, const FlushArgs &a, const FlushList &fl, int ctas, cudaStream_t s) {
     const int smem = flush_smem_bytes(c->d, c->G, c->P);
     if (c->d == 128)
-        k_flush<128><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
+        flush_swizzled(c) ? k_flush<128, true><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl)
+                          : k_flush<128, false><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
     else
-        k_flush<64><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
+        flush_swizzled(c) ? k_flush<64, true><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl)
+                          : k_flush<64, false><<<ctas, FLUSH_THREADS, smem, s>>>(a, fl);
     return cudaGetLastError();
 }
 
@@ -856,7 +907,12 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
                                                                      gtop);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int sw = nf < SCAN_WARPS ? nf : SCAN_WARPS;
+    // as many warps as groups, at most SCAN_WARPS, within the shared memory
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    if (e != cudaSuccess) return e;
+    int sw = nf < SCAN_WARPS ? nf : SCAN_WARPS;
+    while (sw > 1 && (long long)sw * P * 6 * 8 > optin) --sw;
     k_pf_scan<<<nu, 32 * sw, (size_t)sw * P * 6 * 8, s>>>(gtop, phist, nf, G, P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -967,8 +1023,15 @@ cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *s
 cudaError_t set_flush_attributes(int d, int smem) {
     cudaError_t e = cudaFuncSetAttribute(k_pf_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (d == 128) return cudaFuncSetAttribute(k_flush<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    return cudaFuncSetAttribute(k_flush<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const void *fns[] = {reinterpret_cast<const void *>(k_flush<128, true>),
+                         reinterpret_cast<const void *>(k_flush<128, false>),
+                         reinterpret_cast<const void *>(k_flush<64, true>),
+                         reinterpret_cast<const void *>(k_flush<64, false>)};
+    for (const void *f : fns) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace ott
