@@ -323,6 +323,7 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     const int nf = L >= c->G + c->R ? (L - c->R) / c->G : 0;
     if (blocks_needed(c, (long long)nf * c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, (long long)nf * c->U);
+    c->blocks_settled = 0;
     cudaError_t e = cudaSuccess;
     if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, c->U, s, e)) {
         for (int j = 0; j < nf && e == cudaSuccess; ++j)
@@ -357,6 +358,7 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
     }
     if (blocks_needed(c, unit_flushes) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, unit_flushes);
+    c->blocks_settled = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     // each sequence in one parallel pass where it can; the rest group by
@@ -418,6 +420,7 @@ int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s
         }
     }
     c->T += 1;
+    if (fl.n > 0) c->blocks_settled = 0;
     e = launch_flush_list(c, c->rk, c->rv, (long long)c->ring * c->d, c->ring, fl, s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     for (int i = 0; i < fl.n; ++i) c->nfb[fl.lb[i]] += 1;
@@ -445,6 +448,7 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T += 1;
     if (flush_due(c)) {
+        c->blocks_settled = 0;
         e = launch_flush(c, c->rk, c->rv, (long long)c->ring * c->d, c->ring, (long long)c->nf * c->G, c->nf, s);
         if (e != cudaSuccess) return fail_cuda(c, e);
         c->nf += 1;
@@ -458,6 +462,7 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream) {
     if (!q || !out || !aligned16(q) || !aligned16(out) || q == out) return OTT_ERR_INVALID;
     cudaError_t e = launch_decode(c, static_cast<const __half *>(q), static_cast<__half *>(out),
                                   static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) c->blocks_settled = 1;
     return fail_cuda(c, e);
 }
 
@@ -474,6 +479,7 @@ int ott_decode_attn_topk(ott_cache *c, const void *q, void *out, int K, int32_t 
     cudaError_t e = cudaSuccess;
     if (Kc > 0) e = launch_topk_select(c, qh, K, Kc, s);
     if (e == cudaSuccess) e = launch_decode_topk(c, qh, static_cast<__half *>(out), Kc, s);
+    if (e == cudaSuccess) c->blocks_settled = 1;
     if (e == cudaSuccess && sel && Kc > 0)
         e = cudaMemcpyAsync(sel, c->sel, (size_t)c->U * Kc * 4, cudaMemcpyDeviceToDevice, s);
     return fail_cuda(c, e);
@@ -485,6 +491,7 @@ int ott_release_seq(ott_cache *c, int b, void *stream) {
     if (b < 0 || b >= c->B) return OTT_ERR_INVALID;
     if (!c->ragged) to_per_sequence(c);   // a uniform prefill so far
     if (c->Tb[b] == 0) return OTT_OK;      // already empty
+    c->blocks_settled = 0;
     cudaError_t e = launch_release(c, b, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->free_blocks += blocks_needed(c, (long long)c->nfb[b] * c->Hkv);
@@ -507,6 +514,7 @@ int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, vo
     const int nf = flushes_after(c, L);
     if (blocks_needed(c, (long long)nf * c->Hkv) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, (long long)nf * c->Hkv);
+    c->blocks_settled = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     cudaError_t e = cudaSuccess;

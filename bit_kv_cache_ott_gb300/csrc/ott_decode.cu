@@ -355,7 +355,9 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
             }
         }
     };
-    // start the copies first, then stage the queries while they fly
+    // start the copies first (blocks are final here: no flush precedes a
+    // programmatic launch), then wait for the kernel this grid depends on,
+    // and stage the queries while the copies fly
     Cursor cc = ic;
     int st_issue = 0;
     for (int n = 0; n < 2 && !past(ic); ++n) {
@@ -363,6 +365,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
         st_issue ^= 1;
         advance(ic);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     load_queries<D, GQ>(a, u, qsm, lane);
 
     // Cooperative per-block constants: lane L handles channel pairs
@@ -785,6 +788,9 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
             bulk_copy_only(dst + (size_t)lane * RS * 2, row_ptr(f, lane >= SUB), D * 2, &bars[st]);
         }
     };
+    // the ring and the pool may have been written by the kernel this grid
+    // depends on (an append): wait for it before the first copy
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int st_issue = 0;
     for (int k = 0; k < 2 && k < nsub; ++k) {
         issue(k, st_issue);
@@ -977,6 +983,9 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
     // everything above depends on the arguments only; the partials are the
     // decode grid's results
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next decode may be scheduled now (it waits for this grid before
+    // reading its inputs or writing partials)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float M = -CUDART_INF_F, L = 0.0f, acc[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
@@ -1174,8 +1183,23 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, k_decode<D, GQ, RG, CO, TK>, a, st);
     } else {
-        k_decode<D, GQ, RG, CO, TK><<<c->sm_count, wpc * 32, Cfg<D, GQ>::WARP_SMEM * wpc, s>>>(a, st);
-        e = cudaGetLastError();
+        // Launched as a programmatic dependent of the kernel before it when
+        // no flush was queued since the last decode: its warps then issue
+        // their first block copies early and wait for that kernel (an append
+        // or the previous call's combine) before reading the queries, the
+        // ring, the pool or writing partials. Blocks are written only by
+        // flushes, which the host tracks.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)c->sm_count);
+        cfg.blockDim = dim3((unsigned)(wpc * 32));
+        cfg.dynamicSmemBytes = (size_t)Cfg<D, GQ>::WARP_SMEM * wpc;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = c->blocks_settled ? 1 : 0;
+        e = cudaLaunchKernelEx(&cfg, k_decode<D, GQ, RG, CO, TK>, a, st);
     }
     if (e != cudaSuccess) return e;
     return launch_combine<D, GQ, RG>(a, st, c->B, s);
@@ -1388,5 +1412,6 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
         c->poisoned = 1;
         return OTT_ERR_CUDA;
     }
+    c->blocks_settled = 1;
     return OTT_OK;
 }

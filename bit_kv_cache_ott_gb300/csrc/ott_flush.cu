@@ -659,6 +659,8 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
 // k, v [U][d] -> ring slot `slot` of every unit
 __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
                          __half *rv, int U, int d, int ring, int slot) {
+    // a decode queued next may start now; it waits for this grid before reading the ring
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int vpr = d / 8;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
         const int u = e / vpr, x = e % vpr;
@@ -675,6 +677,7 @@ struct SlotTable {
 
 __global__ void k_append_ragged(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
                                 __half *rv, int U, int Hkv, int d, int ring, const __grid_constant__ SlotTable st) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int vpr = d / 8;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
         const int u = e / vpr, x = e % vpr;

@@ -131,6 +131,9 @@ struct ott_cache {
     long long T;
     int nf;
     int poisoned;
+    // no flush (or anything else that writes blocks) queued since the last
+    // decode: the next decode may be launched as a programmatic dependent
+    int blocks_settled;
     int device;
     int sm_count;
     int flush_smem;
