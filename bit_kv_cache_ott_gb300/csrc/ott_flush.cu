@@ -661,6 +661,9 @@ __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ 
                          __half *rv, int U, int d, int ring, int slot) {
     // a decode queued next may start now; it waits for this grid before reading the ring
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched as a programmatic dependent: the kernel before this one (the
+    // previous call's combine, or whatever wrote k and v) completes first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int vpr = d / 8;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
         const int u = e / vpr, x = e % vpr;
@@ -678,6 +681,7 @@ struct SlotTable {
 __global__ void k_append_ragged(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
                                 __half *rv, int U, int Hkv, int d, int ring, const __grid_constant__ SlotTable st) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int vpr = d / 8;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
         const int u = e / vpr, x = e % vpr;
@@ -809,13 +813,38 @@ int flush_smem_bytes(int d, int G, int P) {
     return t > (1LL << 30) ? (1 << 30) : (int)t;
 }
 
+namespace {
+
+// An append is launched as a programmatic dependent of the kernel before it:
+// it releases its own dependents at once and then waits for that kernel, so
+// only its launch overlaps the previous kernel's tail.
+cudaLaunchConfig_t pdl_config(int blocks, int threads, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    return cfg;
+}
+
+void pdl_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+}
+
+}  // namespace
+
 cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
     const int slot = (int)(c->T % c->ring);
     const int n = c->U * c->d / 8;
     const int th = 256, bl = (n + th - 1) / th;
-    k_append<<<bl, th, 0, s>>>(reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
-                               c->rk, c->rv, c->U, c->d, c->ring, slot);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = pdl_config(bl, th, s);
+    cudaLaunchAttribute attr[1];
+    pdl_attr(cfg, attr);
+    return cudaLaunchKernelEx(&cfg, k_append, reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
+                              c->rk, c->rv, c->U, c->d, c->ring, slot);
 }
 
 namespace {
@@ -973,9 +1002,11 @@ cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __ha
     for (int b = 0; b < c->B; ++b) st.slot[b] = (int)(c->Tb[b] % c->ring);
     const int n = c->U * c->d / 8;
     const int th = 256, bl = (n + th - 1) / th;
-    k_append_ragged<<<bl, th, 0, s>>>(reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
-                                      c->rk, c->rv, c->U, c->Hkv, c->d, c->ring, st);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = pdl_config(bl, th, s);
+    cudaLaunchAttribute attr[1];
+    pdl_attr(cfg, attr);
+    return cudaLaunchKernelEx(&cfg, k_append_ragged, reinterpret_cast<const uint4 *>(k),
+                              reinterpret_cast<const uint4 *>(v), c->rk, c->rv, c->U, c->Hkv, c->d, c->ring, st);
 }
 
 cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,
