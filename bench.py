@@ -580,12 +580,12 @@ def run_ours(args, w):
     achieved = dec_call_bytes * n_dec / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
 
-    # end to end through the public API with host buffers (pinned), per step:
-    # k, v, q host->device, append, decode, out device->host. Two buffer sets:
+    # end to end through the public API with host buffers (pinned), per step.
+    # Top-K decode: k, v, q host->device, append, decode, out device->host. Two buffer sets:
     # the copy stream brings in step s+1's inputs and reads back step s's
     # output while step s's kernels run, as a serving loop would drive the API.
     e2e = None
-    if E_steps > 0:
+    if E_steps > 0 and w.topk > 0:
         # each step's k, v and q travel in one pinned buffer (one copy per step)
         shapes = [tuple(t.shape) for t in host[0]]
         sizes = [t.numel() for t in host[0]]
@@ -640,6 +640,36 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(pin[0].numel() * pin[0].element_size()),
                "d2h_bytes_per_step": int(out_h[0].numel() * out_h[0].element_size()), "steps": E_steps,
                "copies": "k, v, q in one pinned host buffer per step, double-buffered on a second stream"}
+
+    # Full decode: ott_step_host appends k, v and decodes q straight from
+    # pinned host memory (the append kernel reads them; the combine writes out
+    # back to pinned host memory), so the step stays one chain of kernels.
+    if E_steps > 0 and w.topk == 0:
+        shapes = [tuple(t.shape) for t in host[0]]
+        sizes = [t.numel() for t in host[0]]
+        pin = [torch.cat([t.reshape(-1) for t in x]).pin_memory() for x in host]
+        offs = (0, sizes[0], sizes[0] + sizes[1])
+        views = [tuple(p_.narrow(0, o, n).view(sh) for o, n, sh in zip(offs, sizes, shapes)) for p_ in pin]
+        out_h = [torch.empty(w.B, w.Hq, w.d, dtype=torch.float16).pin_memory() for _ in range(2)]
+        torch.cuda.synchronize()
+        barrier()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for s in range(E_steps):
+            kh, vh, qh = views[(W_steps + K_steps + s) % n_distinct]
+            for c in caches:
+                c.step_host(kh, vh, qh, out_h[s % 2], stream)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = max_over_ranks(x0.elapsed_time(x1), dev)
+        in_bytes = int(pin[0].numel() * pin[0].element_size())
+        out_bytes = int(out_h[0].numel() * out_h[0].element_size())
+        e2e = {"value": job_tokens_per_s(w.B, E_steps, ws, ems), "unit": "tokens/s",
+               "h2d_bytes_per_step": in_bytes * w.layers, "d2h_bytes_per_step": out_bytes * w.layers,
+               "steps": E_steps,
+               "copies": "ott_step_host per layer: k, v and q read by the append kernel from one pinned host "
+                         "buffer per step, out written by the combine into pinned host memory (two, alternating)"}
 
     # the prefill of one layer's cache (the parallel pass), timed on its own
     pf = None

@@ -226,6 +226,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t o_pi = off; off = round_up(off + sz_pn, 256);
     const size_t o_part = off; off = round_up(off + sz_part, 256);
     const size_t o_ctl = off; off = round_up(off + 64, 256);
+    const size_t o_q = off; off = round_up(off + (size_t)B * Hq * d * 2, 256);
     const size_t o_ck = off; off = round_up(off + sz_cold, 256);
     const size_t o_cv = off; off = round_up(off + sz_cold, 256);
     const size_t o_ci = off; off = round_up(off + sz_cidx, 256);
@@ -264,6 +265,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->pidx = reinterpret_cast<int32_t *>(base + o_pi);
     c->part = reinterpret_cast<float *>(base + o_part);
     c->ctl = reinterpret_cast<int *>(base + o_ctl);
+    c->qdev = reinterpret_cast<__half *>(base + o_q);
     c->ck = sz_cold ? reinterpret_cast<__half *>(base + o_ck) : nullptr;
     c->cv = sz_cold ? reinterpret_cast<__half *>(base + o_cv) : nullptr;
     c->cidx = sz_cidx ? reinterpret_cast<int32_t *>(base + o_ci) : nullptr;
@@ -401,13 +403,13 @@ int ott_prefill_lens(ott_cache *c, const void *K, const void *V, const int *lens
 
 namespace {
 
-int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s, const __half *qsrc) {
     long long due = 0;   // sequences whose residual window fills with this token
     for (int b = 0; b < c->B; ++b)
         due += c->Tb[b] + 1 - (long long)c->nfb[b] * c->G >= (long long)c->G + c->R;
     if (blocks_needed(c, due * c->Hkv) > c->free_blocks) return OTT_ERR_CAPACITY;
     c->free_blocks -= blocks_needed(c, due * c->Hkv);
-    cudaError_t e = launch_append_ragged(c, k, v, s);
+    cudaError_t e = launch_append_ragged(c, k, v, s, qsrc);
     if (e != cudaSuccess) return fail_cuda(c, e);
     FlushList fl;
     fl.n = 0;
@@ -429,22 +431,22 @@ int append_ragged(ott_cache *c, const __half *k, const __half *v, cudaStream_t s
 
 }  // namespace
 
-int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
-    if (!c) return OTT_ERR_INVALID;
-    if (c->poisoned) return OTT_ERR_STATE;
-    if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
+namespace {
+
+// The append of ott_append and ott_step_host (qsrc: the step's queries to
+// copy to c->qdev in the same kernel, or null). Arguments are checked.
+int append_impl(ott_cache *c, const void *k, const void *v, cudaStream_t s, const __half *qsrc) {
     // with per-sequence counts T is the longest sequence, so this is each
     // sequence's own capacity check
     if (c->T + 1 > c->max_tokens) return OTT_ERR_CAPACITY;
     if (some_sequence_empty(c)) return OTT_ERR_STATE;
     if (c->paged && !c->ragged) to_per_sequence(c);   // blocks are read through the table
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (c->ragged)
-        return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
+        return append_ragged(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s, qsrc);
     const bool due = c->T + 1 - (long long)c->nf * c->G >= (long long)c->G + c->R;
     if (due && blocks_needed(c, c->U) > c->free_blocks) return OTT_ERR_CAPACITY;
     if (due) c->free_blocks -= blocks_needed(c, c->U);
-    cudaError_t e = launch_append(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s);
+    cudaError_t e = launch_append(c, static_cast<const __half *>(k), static_cast<const __half *>(v), s, qsrc);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->T += 1;
     if (flush_due(c)) {
@@ -453,6 +455,42 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
         if (e != cudaSuccess) return fail_cuda(c, e);
         c->nf += 1;
     }
+    return OTT_OK;
+}
+
+// The device address of pinned host memory (null if it is not mapped pinned memory).
+const void *mapped(const void *host) {
+    void *d = nullptr;
+    if (!host || cudaHostGetDevicePointer(&d, const_cast<void *>(host), 0) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return d;
+}
+
+}  // namespace
+
+int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned) return OTT_ERR_STATE;
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return OTT_ERR_INVALID;
+    return append_impl(c, k, v, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, void *stream) {
+    if (!c) return OTT_ERR_INVALID;
+    if (c->poisoned) return OTT_ERR_STATE;
+    const void *dk = mapped(k), *dv = mapped(v), *dq = mapped(q);
+    void *dout = const_cast<void *>(mapped(out));
+    if (!dk || !dv || !dq || !dout || !aligned16(dk) || !aligned16(dv) || !aligned16(dq) || !aligned16(dout))
+        return OTT_ERR_INVALID;
+    if (out == q || out == k || out == v) return OTT_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int rc = append_impl(c, dk, dv, s, static_cast<const __half *>(dq));
+    if (rc != OTT_OK) return rc;
+    const cudaError_t e = launch_decode(c, c->qdev, static_cast<__half *>(dout), s);
+    if (e != cudaSuccess) return fail_cuda(c, e);
+    c->blocks_settled = 1;
     return OTT_OK;
 }
 

@@ -1051,8 +1051,14 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
         }
     }
     __half *o = a.out + ((size_t)b * a.Hq + hq) * D + lane * CPL;
+    // one vector store per lane (out may be host memory)
+    uint32_t w[CPL / 2];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) o[c] = __float2half_rn(acc[c] / L);
+    for (int c = 0; c < CPL; c += 2) w[c / 2] = h2bits(__floats2half2_rn(acc[c] / L, acc[c + 1] / L));
+    if constexpr (CPL == 4)
+        *reinterpret_cast<uint2 *>(o) = make_uint2(w[0], w[1]);
+    else
+        *reinterpret_cast<uint32_t *>(o) = w[0];
 }
 
 // Launch the combine as a programmatic dependent of the decode grid just

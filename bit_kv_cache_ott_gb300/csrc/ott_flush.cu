@@ -657,19 +657,29 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
 }
 
 // k, v [U][d] -> ring slot `slot` of every unit
+// With qsrc, the step's queries (nq 16-byte vectors) are copied to qdst too
+// (a step fed from host memory: k, v and q are read where they are).
 __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
-                         __half *rv, int U, int d, int ring, int slot) {
+                         __half *rv, int U, int d, int ring, int slot, const uint4 *__restrict__ qsrc,
+                         uint4 *__restrict__ qdst, int nq) {
     // a decode queued next may start now; it waits for this grid before reading the ring
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // launched as a programmatic dependent: the kernel before this one (the
     // previous call's combine, or whatever wrote k and v) completes first
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int vpr = d / 8;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
-        const int u = e / vpr, x = e % vpr;
-        const size_t off = ((size_t)u * ring + slot) * d;
-        reinterpret_cast<uint4 *>(rk + off)[x] = k[e];
-        reinterpret_cast<uint4 *>(rv + off)[x] = v[e];
+    // one 16-byte vector per thread (k and v of one unit, or one of q), so
+    // that every load is in flight at once (they may come from host memory)
+    const int vpr = d / 8, n = U * vpr;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n + nq; e += gridDim.x * blockDim.x) {
+        if (e < n) {
+            const int u = e / vpr, x = e % vpr;
+            const size_t off = ((size_t)u * ring + slot) * d;
+            const uint4 kk = k[e], vv = v[e];
+            reinterpret_cast<uint4 *>(rk + off)[x] = kk;
+            reinterpret_cast<uint4 *>(rv + off)[x] = vv;
+        } else {
+            qdst[e - n] = qsrc[e - n];
+        }
     }
 }
 
@@ -679,15 +689,21 @@ struct SlotTable {
 };
 
 __global__ void k_append_ragged(const uint4 *__restrict__ k, const uint4 *__restrict__ v, __half *rk,
-                                __half *rv, int U, int Hkv, int d, int ring, const __grid_constant__ SlotTable st) {
+                                __half *rv, int U, int Hkv, int d, int ring, const __grid_constant__ SlotTable st,
+                                const uint4 *__restrict__ qsrc, uint4 *__restrict__ qdst, int nq) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int vpr = d / 8;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < U * vpr; e += gridDim.x * blockDim.x) {
-        const int u = e / vpr, x = e % vpr;
-        const size_t off = ((size_t)u * ring + st.slot[u / Hkv]) * d;
-        reinterpret_cast<uint4 *>(rk + off)[x] = k[e];
-        reinterpret_cast<uint4 *>(rv + off)[x] = v[e];
+    const int vpr = d / 8, n = U * vpr;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n + nq; e += gridDim.x * blockDim.x) {
+        if (e < n) {
+            const int u = e / vpr, x = e % vpr;
+            const size_t off = ((size_t)u * ring + st.slot[u / Hkv]) * d;
+            const uint4 kk = k[e], vv = v[e];
+            reinterpret_cast<uint4 *>(rk + off)[x] = kk;
+            reinterpret_cast<uint4 *>(rv + off)[x] = vv;
+        } else {
+            qdst[e - n] = qsrc[e - n];
+        }
     }
 }
 
@@ -836,15 +852,17 @@ void pdl_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
 
 }  // namespace
 
-cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s, const __half *qsrc) {
     const int slot = (int)(c->T % c->ring);
     const int n = c->U * c->d / 8;
-    const int th = 256, bl = (n + th - 1) / th;
+    const int nq = qsrc ? c->B * c->Hq * c->d / 8 : 0;
+    const int th = 256, bl = (n + nq + th - 1) / th;
     cudaLaunchConfig_t cfg = pdl_config(bl, th, s);
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr);
     return cudaLaunchKernelEx(&cfg, k_append, reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
-                              c->rk, c->rv, c->U, c->d, c->ring, slot);
+                              c->rk, c->rv, c->U, c->d, c->ring, slot, reinterpret_cast<const uint4 *>(qsrc),
+                              reinterpret_cast<uint4 *>(c->qdev), nq);
 }
 
 namespace {
@@ -997,16 +1015,19 @@ cudaError_t launch_release(const ott_cache *c, int b, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s) {
+cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s,
+                                 const __half *qsrc) {
+    const int nq = qsrc ? c->B * c->Hq * c->d / 8 : 0;
     SlotTable st;
     for (int b = 0; b < c->B; ++b) st.slot[b] = (int)(c->Tb[b] % c->ring);
     const int n = c->U * c->d / 8;
-    const int th = 256, bl = (n + th - 1) / th;
+    const int th = 256, bl = (n + nq + th - 1) / th;
     cudaLaunchConfig_t cfg = pdl_config(bl, th, s);
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr);
     return cudaLaunchKernelEx(&cfg, k_append_ragged, reinterpret_cast<const uint4 *>(k),
-                              reinterpret_cast<const uint4 *>(v), c->rk, c->rv, c->U, c->Hkv, c->d, c->ring, st);
+                              reinterpret_cast<const uint4 *>(v), c->rk, c->rv, c->U, c->Hkv, c->d, c->ring, st,
+                              reinterpret_cast<const uint4 *>(qsrc), reinterpret_cast<uint4 *>(c->qdev), nq);
 }
 
 cudaError_t launch_copy_tail_units(const ott_cache *c, const __half *K, const __half *V, int u0, int nu,

@@ -149,6 +149,7 @@ struct ott_cache {
     int32_t *pidx;          // [U][P]
     float *part;            // [warps][maxu][2][gq][d+2] split-K partials
     int *ctl;               // [1] status flag set by a bounded wait that timed out
+    __half *qdev;           // [B][Hq][d] the queries of a step fed from host memory
     // sequences of different lengths (ott_create_ragged + ott_prefill_lens)
     int ragged_capable;     // partials sized for ragged decode
     int ragged;             // per-sequence lengths in effect
@@ -198,8 +199,11 @@ struct FlushList {
     int lb[RAGGED_MAX], lj[RAGGED_MAX];
 };
 
-cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s);
-cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s);
+// qsrc (optional): the step's queries, copied to c->qdev by the same kernel
+cudaError_t launch_append(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s,
+                          const __half *qsrc = nullptr);
+cudaError_t launch_append_ragged(const ott_cache *c, const __half *k, const __half *v, cudaStream_t s,
+                                 const __half *qsrc = nullptr);
 cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *srcV,
                          long long src_unit_stride, long long src_mod, long long t0, int j,
                          cudaStream_t s);

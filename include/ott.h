@@ -223,6 +223,25 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream);
 int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
 
 /*
+ * One decode step fed from and answered into pinned host memory: the same
+ * work as copying k, v and q to the device, ott_append(k, v) and
+ * ott_decode_attn(q, out), then copying out back, but the kernels read and
+ * write the host buffers themselves through the device's mapping of pinned
+ * memory, so the step is one chain of kernels on the stream with no copy
+ * between them (each kernel's launch then overlaps the one before it).
+ * k, v: fp16 [B][Hkv][d], q: fp16 [B][Hq][d], out: fp16 [B][Hq][d], all in
+ * pinned (page-locked, mapped) host memory, 16-byte aligned; out may not
+ * alias an input. The queries are copied to the device by the append kernel.
+ * The buffers must stay valid, and the inputs unchanged, until the stream
+ * passes the step; out is complete then. A pointer the device cannot address
+ * (cudaHostGetDevicePointer fails) or that is not 16-byte aligned gives
+ * OTT_ERR_INVALID before anything is queued; the other errors are those of
+ * ott_append and ott_decode_attn. (Where the GPU addresses all host memory,
+ * pageable buffers are accepted too, at lower speed.)
+ */
+int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, void *stream);
+
+/*
  * The same decode as ott_decode_attn, but allocation-free: it calls no
  * cudaMalloc, cudaFree or allocating library routine, and it does not use the
  * split-K scratch that ott_create set aside. Its partial results go to a fixed
