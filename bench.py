@@ -35,6 +35,7 @@ from bit_kv_cache_ott_gb300 import metrics, synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "OTT decode-attn GB/s (% of HBM peak) and decode tokens/s at B=32, 4K ctx"
+E2E_ZERO_COPY_MAX = 512 * 1024   # step inputs at or above this travel by copy, below it by ott_step_host
 DECODE_SRC = os.path.join(ROOT, "bit_kv_cache_ott_gb300", "csrc", "ott_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
@@ -581,11 +582,18 @@ def run_ours(args, w):
     peak, peak_kind = hbm_peak()
 
     # end to end through the public API with host buffers (pinned), per step.
-    # Top-K decode: k, v, q host->device, append, decode, out device->host. Two buffer sets:
+    # Copy path: k, v, q host->device, append, decode, out device->host. Two buffer sets:
     # the copy stream brings in step s+1's inputs and reads back step s's
     # output while step s's kernels run, as a serving loop would drive the API.
     e2e = None
-    if E_steps > 0 and w.topk > 0:
+    # Feeding the kernels from pinned host memory (ott_step_host) keeps the
+    # launch chain but puts host-memory latency on each step's critical path;
+    # it pays for small inputs. Steps with large inputs (and Top-K decode,
+    # which ott_step_host does not run) copy them on a second stream a step
+    # ahead instead.
+    in_step_bytes = sum(t.numel() * t.element_size() for t in host[0])
+    copy_stream_e2e = w.topk > 0 or in_step_bytes >= E2E_ZERO_COPY_MAX
+    if E_steps > 0 and copy_stream_e2e:
         # each step's k, v and q travel in one pinned buffer (one copy per step)
         shapes = [tuple(t.shape) for t in host[0]]
         sizes = [t.numel() for t in host[0]]
@@ -644,7 +652,7 @@ def run_ours(args, w):
     # Full decode: ott_step_host appends k, v and decodes q straight from
     # pinned host memory (the append kernel reads them; the combine writes out
     # back to pinned host memory), so the step stays one chain of kernels.
-    if E_steps > 0 and w.topk == 0:
+    if E_steps > 0 and not copy_stream_e2e:
         shapes = [tuple(t.shape) for t in host[0]]
         sizes = [t.numel() for t in host[0]]
         pin = [torch.cat([t.reshape(-1) for t in x]).pin_memory() for x in host]
