@@ -588,11 +588,10 @@ def run_ours(args, w):
     e2e = None
     # Feeding the kernels from pinned host memory (ott_step_host) keeps the
     # launch chain but puts host-memory latency on each step's critical path;
-    # it pays for small inputs. Steps with large inputs (and Top-K decode,
-    # which ott_step_host does not run) copy them on a second stream a step
-    # ahead instead.
+    # it pays for small inputs. Steps with large inputs copy them on a second
+    # stream a step ahead instead.
     in_step_bytes = sum(t.numel() * t.element_size() for t in host[0])
-    copy_stream_e2e = w.topk > 0 or in_step_bytes >= E2E_ZERO_COPY_MAX
+    copy_stream_e2e = in_step_bytes >= E2E_ZERO_COPY_MAX
     if E_steps > 0 and copy_stream_e2e:
         # each step's k, v and q travel in one pinned buffer (one copy per step)
         shapes = [tuple(t.shape) for t in host[0]]
@@ -649,7 +648,7 @@ def run_ours(args, w):
                "d2h_bytes_per_step": int(out_h[0].numel() * out_h[0].element_size()), "steps": E_steps,
                "copies": "k, v, q in one pinned host buffer per step, double-buffered on a second stream"}
 
-    # Full decode: ott_step_host appends k, v and decodes q straight from
+    # ott_step_host appends k, v and decodes q (full or Top-K) straight from
     # pinned host memory (the append kernel reads them; the combine writes out
     # back to pinned host memory), so the step stays one chain of kernels.
     if E_steps > 0 and not copy_stream_e2e:
@@ -666,7 +665,7 @@ def run_ours(args, w):
         for s in range(E_steps):
             kh, vh, qh = views[(W_steps + K_steps + s) % n_distinct]
             for c in caches:
-                c.step_host(kh, vh, qh, out_h[s % 2], stream)
+                c.step_host(kh, vh, qh, out_h[s % 2], w.topk, stream)
         x1.record(stream)
         torch.cuda.synchronize()
         barrier()

@@ -73,7 +73,7 @@ def load(build_if_missing: bool = False):
     L.ott_prefill.argtypes = [P, P, P, i32, P]
     L.ott_prefill_lens.argtypes = [P, P, P, C.POINTER(i32), i32, P]
     L.ott_append.argtypes = [P, P, P, P]
-    L.ott_step_host.argtypes = [P, P, P, P, P, P]
+    L.ott_step_host.argtypes = [P, P, P, P, P, i32, P]
     L.ott_decode_attn.argtypes = [P, P, P, P]
     L.ott_decode_attn_static.argtypes = [P, P, P, P]
     L.ott_decode_attn_topk.argtypes = [P, P, P, i32, P, P]
@@ -204,10 +204,12 @@ class OTTCache:
         _check(load().ott_append(self._h, _dev_ptr(k, shp, "k"), _dev_ptr(v, shp, "v"),
                                  _stream(stream)), "ott_append")
 
-    def step_host(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out: torch.Tensor, stream=None):
+    def step_host(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out: torch.Tensor, topk: int = 0,
+                  stream=None):
         """One step from pinned host memory: append k, v (fp16 [B][Hkv][d]) and
         decode q (fp16 [B][Hq][d]) into out (fp16 [B][Hq][d]), all pinned CPU
         tensors; the kernels read and write them in place (ott_step_host).
+        topk >= 1 decodes with Top-K sparse access over that many blocks.
         out is complete when the stream has passed the step."""
         for name, t, shp in (("k", k, (self.B, self.Hkv, self.d)), ("v", v, (self.B, self.Hkv, self.d)),
                              ("q", q, (self.B, self.Hq, self.d)), ("out", out, (self.B, self.Hq, self.d))):
@@ -215,7 +217,7 @@ class OTTCache:
                 raise TypeError(f"{name}: expected a pinned CPU float16 tensor")
             if tuple(t.shape) != shp or not t.is_contiguous():
                 raise ValueError(f"{name}: expected contiguous shape {shp}, got {tuple(t.shape)}")
-        _check(load().ott_step_host(self._h, k.data_ptr(), v.data_ptr(), q.data_ptr(), out.data_ptr(),
+        _check(load().ott_step_host(self._h, k.data_ptr(), v.data_ptr(), q.data_ptr(), out.data_ptr(), int(topk),
                                     _stream(stream)), "ott_step_host")
 
     def decode_attn(self, q: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -477,7 +477,7 @@ int ott_append(ott_cache *c, const void *k, const void *v, void *stream) {
     return append_impl(c, k, v, static_cast<cudaStream_t>(stream), nullptr);
 }
 
-int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, void *stream) {
+int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, int topk, void *stream) {
     if (!c) return OTT_ERR_INVALID;
     if (c->poisoned) return OTT_ERR_STATE;
     const void *dk = mapped(k), *dv = mapped(v), *dq = mapped(q);
@@ -485,9 +485,11 @@ int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, voi
     if (!dk || !dv || !dq || !dout || !aligned16(dk) || !aligned16(dv) || !aligned16(dq) || !aligned16(dout))
         return OTT_ERR_INVALID;
     if (out == q || out == k || out == v) return OTT_ERR_INVALID;
+    if (topk > 0 && !c->topk_ok) return OTT_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int rc = append_impl(c, dk, dv, s, static_cast<const __half *>(dq));
     if (rc != OTT_OK) return rc;
+    if (topk > 0) return ott_decode_attn_topk(c, c->qdev, dout, topk, nullptr, stream);
     const cudaError_t e = launch_decode(c, c->qdev, static_cast<__half *>(dout), s);
     if (e != cudaSuccess) return fail_cuda(c, e);
     c->blocks_settled = 1;

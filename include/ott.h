@@ -225,7 +225,8 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
 /*
  * One decode step fed from and answered into pinned host memory: the same
  * work as copying k, v and q to the device, ott_append(k, v) and
- * ott_decode_attn(q, out), then copying out back, but the kernels read and
+ * ott_decode_attn(q, out) (topk >= 1: ott_decode_attn_topk(q, out, topk)),
+ * then copying out back, but the kernels read and
  * write the host buffers themselves through the device's mapping of pinned
  * memory, so the step is one chain of kernels on the stream with no copy
  * between them (each kernel's launch then overlaps the one before it).
@@ -239,7 +240,7 @@ int ott_decode_attn(ott_cache *c, const void *q, void *out, void *stream);
  * ott_append and ott_decode_attn. (Where the GPU addresses all host memory,
  * pageable buffers are accepted too, at lower speed.)
  */
-int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, void *stream);
+int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, void *out, int topk, void *stream);
 
 /*
  * The same decode as ott_decode_attn, but allocation-free: it calls no

@@ -47,7 +47,7 @@ def test_step_host_equals_device_path(ott, B, Hq, Hkv, d, G, R, P, L, steps, rag
         outs = [torch.empty(B, Hq, d, dtype=torch.float16).pin_memory() for _ in range(steps)]
         stream = torch.cuda.current_stream()
         for s in range(steps):
-            a.step_host(kh[s], vh[s], qh[s], outs[s], stream)
+            a.step_host(kh[s], vh[s], qh[s], outs[s], stream=stream)
             b.append(kh[s].to(dev), vh[s].to(dev))
             ref = b.decode_attn(qh[s].to(dev))
             torch.cuda.synchronize()
@@ -73,14 +73,41 @@ def test_step_host_argument_checks(ott):
             c.step_host(k.cuda(), k, q, out)                                           # on the device
         L = ott.load()
         sp = C.c_void_p(torch.cuda.current_stream().cuda_stream)
-        rc = L.ott_step_host(c.handle, k.data_ptr(), k.data_ptr(), q.data_ptr(), q.data_ptr(), sp)
+        rc = L.ott_step_host(c.handle, k.data_ptr(), k.data_ptr(), q.data_ptr(), q.data_ptr(), 0, sp)
         assert rc == ott.OTT_ERR_INVALID                      # out aliases q
-        rc = L.ott_step_host(c.handle, k.data_ptr() + 2, k.data_ptr(), q.data_ptr(), out.data_ptr(), sp)
+        rc = L.ott_step_host(c.handle, k.data_ptr() + 2, k.data_ptr(), q.data_ptr(), out.data_ptr(), 0, sp)
         assert rc == ott.OTT_ERR_INVALID                      # k not 16-byte aligned
-        rc = L.ott_step_host(c.handle, None, k.data_ptr(), q.data_ptr(), out.data_ptr(), sp)
+        rc = L.ott_step_host(c.handle, None, k.data_ptr(), q.data_ptr(), out.data_ptr(), 0, sp)
         assert rc == ott.OTT_ERR_INVALID                      # no k
         assert c.counts()[0] == 0                             # nothing queued
         c.step_host(k, k.clone().pin_memory(), q, out)
         torch.cuda.synchronize()
         assert c.counts()[0] == 1 and torch.isfinite(out.float()).all()
         c.check_device()
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+def test_step_host_topk_equals_device_path(ott, ragged):
+    """Top-K steps from host memory against ott_append + ott_decode_attn_topk
+    on device buffers: every output equal, across a flush."""
+    B, Hq, Hkv, d, G, R, P, L, steps, Kb = 2, 8, 2, 128, 16, 4, 6, 300, 30, 3
+    K, V, Q = _gen(7, B, Hkv, Hq, L + steps, d)
+    dev = torch.device("cuda")
+    kw = dict(max_tokens=L + steps + 1, ragged=ragged)
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, **kw) as a, ott.OTTCache(B, Hq, Hkv, d, G, R, P, **kw) as b:
+        for c in (a, b):
+            if ragged:
+                c.prefill_lens(K[:, :, :L].contiguous().to(dev), V[:, :, :L].contiguous().to(dev), [L, L - 40])
+            else:
+                c.prefill(K[:, :, :L].contiguous().to(dev), V[:, :, :L].contiguous().to(dev))
+        out = torch.empty(B, Hq, d, dtype=torch.float16).pin_memory()
+        for s in range(steps):
+            kh, vh, qh = (K[:, :, L + s].contiguous().pin_memory(), V[:, :, L + s].contiguous().pin_memory(),
+                          Q[L + s].contiguous().pin_memory())
+            a.step_host(kh, vh, qh, out, topk=Kb)
+            b.append(kh.to(dev), vh.to(dev))
+            ref = b.decode_attn_topk(qh.to(dev), Kb)
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref.cpu()), s
+        a.check_device()
+        b.check_device()
