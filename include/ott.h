@@ -34,9 +34,16 @@
  * Variants, each declared below with its own rules: batches whose sequences
  * differ in length (ott_create_ragged), a paged block pool with sequences
  * that finish and are replaced (ott_create_paged, ott_release_seq,
- * ott_prefill_seq), the cold-pool eviction policy (ott_create_cold), Top-K
- * sparse decode (ott_decode_attn_topk) and an allocation-free decode
- * (ott_decode_attn_static).
+ * ott_prefill_seq), the cold-pool eviction policy (ott_create_cold), the
+ * channel-conditioned outlier criterion (ott_create_pct), Top-K sparse
+ * decode (ott_decode_attn_topk), an allocation-free decode
+ * (ott_decode_attn_static), and whole steps fed from pinned host memory
+ * (ott_step_host). Two diagnostics support measurements (ott_hbm_copy,
+ * ott_ex2_probe).
+ *
+ * Kernels of consecutive calls on one stream are chained by programmatic
+ * dependent launches: an append or a decode may start while the kernel
+ * before it finishes, and waits for it before reading its inputs.
  *
  * Conventions for every call:
  *   - Device pointers are CUDA device addresses of fp16 data (IEEE binary16),

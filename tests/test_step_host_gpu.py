@@ -111,3 +111,41 @@ def test_step_host_topk_equals_device_path(ott, ragged):
             assert torch.equal(out, ref.cpu()), s
         a.check_device()
         b.check_device()
+
+
+@pytest.mark.parametrize("kind", ["paged", "pct", "cold"])
+def test_step_host_on_other_caches(ott, kind):
+    """The host-buffer step on a paged, a channel-criterion and a cold-pool
+    cache, against the device path on the same kind of cache; then the
+    allocation-free decode agrees with the last step."""
+    B, Hq, Hkv, d, G, R, P, L, steps = 2, 4, 2, 128, 16, 4, 6, 120, 30
+    K, V, Q = _gen(11, B, Hkv, Hq, L + steps, d)
+    dev = torch.device("cuda")
+    kw = dict(max_tokens=L + steps + 1)
+    if kind == "paged":
+        kw["pool_blocks"] = B * Hkv * 16
+    elif kind == "pct":
+        kw["pct"] = (2500, 4)
+    else:
+        kw["cold"] = 3
+    with ott.OTTCache(B, Hq, Hkv, d, G, R, P, **kw) as a, ott.OTTCache(B, Hq, Hkv, d, G, R, P, **kw) as b:
+        for c in (a, b):
+            c.prefill(K[:, :, :L].contiguous().to(dev), V[:, :, :L].contiguous().to(dev))
+        out = torch.empty(B, Hq, d, dtype=torch.float16).pin_memory()
+        for s in range(steps):
+            kh, vh, qh = (K[:, :, L + s].contiguous().pin_memory(), V[:, :, L + s].contiguous().pin_memory(),
+                          Q[L + s].contiguous().pin_memory())
+            a.step_host(kh, vh, qh, out)
+            b.append(kh.to(dev), vh.to(dev))
+            ref = b.decode_attn(qh.to(dev))
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref.cpu()), (kind, s)
+        st = torch.empty(B, Hq, d, dtype=torch.float16, device=dev)
+        qd = qh.to(dev)
+        L_ = ott.load()
+        assert L_.ott_decode_attn_static(a.handle, qd.data_ptr(), st.data_ptr(),
+                                         C.c_void_p(torch.cuda.current_stream().cuda_stream)) == ott.OTT_OK
+        torch.cuda.synchronize()
+        assert torch.equal(st.cpu(), out)
+        a.check_device()
+        b.check_device()
