@@ -144,6 +144,7 @@ struct DecodeArgs {
     long long W;        // U * Iu
     int NWp;            // warps in the grid
     int MAXU;           // units a warp's range can touch
+    int NSM;            // SMs of the device (the combine's CTA count is sized to them)
     float sl2;          // softmax scale 1/sqrt(d) times log2(e)
     int B;              // sequences (the ragged table's length)
     // cold-pool policy: data-dependent block sizes and a fourth, fp16 store
@@ -953,12 +954,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
 constexpr int COMB_MAXW = 32;
 constexpr int COMB_GRP = 8;     // candidate segments a warp loads at a time
 
-template <int D, int GQ, bool RG>
+// CS > 1: the channels of a head are split over CS CTAs (each merges every
+// partial's max and sum, and its own D/CS channels), so that a batch with
+// few query heads still spreads its partials' loads over many SMs.
+template <int D, int GQ, bool RG, int CS>
 __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const __grid_constant__ TableT<RG> st) {
-    constexpr int CPL = D / 32, GRP = COMB_GRP;
-    __shared__ float red[COMB_MAXW][D + 2];
+    constexpr int DC = D / CS, CPL = DC / 32, GRP = COMB_GRP;
+    static_assert(CPL >= 1, "at least one channel per lane");
+    __shared__ float red[COMB_MAXW][DC + 2];
     const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
+    const int bh = blockIdx.x / CS, cs = blockIdx.x % CS;
+    const int b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
+    const int ch0 = cs * DC + lane * CPL;   // this lane's first channel
     // The unit's items are [ub, ub + Sf) fp16 then [ub + Sf, ue) quantized; the
     // decode warps holding them are contiguous ranges [f0, f1] and [q0, q1].
     // Only the first of them can have started in an earlier unit.
@@ -1007,7 +1014,7 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
                 ms[g] = p[0];
                 ls[g] = p[1];
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) vs[g][c] = p[2 + lane * CPL + c];
+                for (int c = 0; c < CPL; ++c) vs[g][c] = p[2 + ch0 + c];
             }
         }
         float mn = M;
@@ -1050,15 +1057,19 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
             for (int c = 0; c < CPL; ++c) acc[c] = fmaf(sx, red[x][2 + lane * CPL + c], acc[c]);
         }
     }
-    __half *o = a.out + ((size_t)b * a.Hq + hq) * D + lane * CPL;
+    __half *o = a.out + ((size_t)b * a.Hq + hq) * D + ch0;
     // one vector store per lane (out may be host memory)
-    uint32_t w[CPL / 2];
+    if constexpr (CPL == 1) {
+        *o = __float2half_rn(acc[0] / L);
+    } else {
+        uint32_t w[CPL / 2];
 #pragma unroll
-    for (int c = 0; c < CPL; c += 2) w[c / 2] = h2bits(__floats2half2_rn(acc[c] / L, acc[c + 1] / L));
-    if constexpr (CPL == 4)
-        *reinterpret_cast<uint2 *>(o) = make_uint2(w[0], w[1]);
-    else
-        *reinterpret_cast<uint32_t *>(o) = w[0];
+        for (int c = 0; c < CPL; c += 2) w[c / 2] = h2bits(__floats2half2_rn(acc[c] / L, acc[c + 1] / L));
+        if constexpr (CPL == 4)
+            *reinterpret_cast<uint2 *>(o) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t *>(o) = w[0];
+    }
 }
 
 // Launch the combine as a programmatic dependent of the decode grid just
@@ -1070,8 +1081,12 @@ cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cud
     const long long per_unit_warps = (a.NWp + U - 1) / U + 1;
     int cw = (int)((2 * per_unit_warps + 2 * COMB_GRP - 1) / (2 * COMB_GRP));   // about two rounds per warp
     cw = cw < 1 ? 1 : (cw > COMB_MAXW ? COMB_MAXW : cw);
+    // few heads: split their channels so that the CTAs cover the SMs
+    const long long heads = (long long)B * a.Hq;
+    int cs = 1;
+    while (cs < 4 && cs * 2 <= D / 32 && heads * cs * 2 <= 2LL * a.NSM) cs *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * a.Hq));
+    cfg.gridDim = dim3((unsigned)(heads * cs));
     cfg.blockDim = dim3((unsigned)(32 * cw));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -1080,7 +1095,9 @@ cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ, RG>, a, st);
+    if (cs == 4) return cudaLaunchKernelEx(&cfg, k_combine<D, GQ, RG, (D / 32 >= 4 ? 4 : 1)>, a, st);
+    if (cs == 2) return cudaLaunchKernelEx(&cfg, k_combine<D, GQ, RG, 2>, a, st);
+    return cudaLaunchKernelEx(&cfg, k_combine<D, GQ, RG, 1>, a, st);
 }
 
 // One sequence's counts after T tokens and nf flushes.
@@ -1172,6 +1189,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     // never more active warps than items: every active warp owns >= 1 item
     a.NWp = (int)(a.W < (long long)c->sm_count * DEC_WARPS ? a.W : (long long)c->sm_count * DEC_WARPS);
     a.sl2 = (float)(1.4426950408889634 / sqrt((double)D));
+    a.NSM = c->sm_count;
     // CTAs only as wide as the active warps need: with few items, the SMs keep
     // room for the combine's CTAs, which then start while the decode drains
     const int wpc = (int)(((long long)a.NWp + c->sm_count - 1) / c->sm_count);
