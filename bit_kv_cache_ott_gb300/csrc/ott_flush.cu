@@ -60,6 +60,19 @@ __device__ __forceinline__ uint32_t qcode(float x, const float4 &r) {
     return (uint32_t)(a > r.y) + (uint32_t)(a >= r.z) + (uint32_t)(a > r.w);
 }
 
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
+}
+// 16 bytes, cached in L2 only (each row is read once)
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
 // Position of channel ch within staged row r: the row's 16-byte chunks are
 // permuted by XOR with r mod 8.
 __device__ __forceinline__ int SWZ(int r, int ch) { return (((ch >> 3) ^ (r & 7)) << 3) | (ch & 7); }
@@ -195,9 +208,13 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             sk = a.srcK + off;
             sv = a.srcV + off;
         }
-        reinterpret_cast<uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)] = reinterpret_cast<const uint4 *>(sk)[v8];
-        reinterpret_cast<uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)] = reinterpret_cast<const uint4 *>(sv)[v8];
+        // asynchronous 16-byte copies: every thread's loads are in flight at once
+        cp_async16(reinterpret_cast<uint4 *>(ck + (size_t)row * RS) + RL::chunk(row, v8),
+                   reinterpret_cast<const uint4 *>(sk) + v8);
+        cp_async16(reinterpret_cast<uint4 *>(cv + (size_t)row * RS) + RL::chunk(row, v8),
+                   reinterpret_cast<const uint4 *>(sv) + v8);
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // 2. keys: (fp32 squared norm bits, token index); norms >= +0 order as bits
@@ -554,13 +571,6 @@ __global__ void __launch_bounds__(PF_THREADS) k_pf_group(const __half *__restric
     }
 }
 
-__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n"
-                 :: "r"((uint32_t)__cvta_generic_to_shared(smem_dst)), "l"(gsrc) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-}
 
 // Output k (0-based) of the merge of the ascending lists A (na keys) and B
 // (nb keys), all keys distinct, k < na + nb: a binary search on the merge
