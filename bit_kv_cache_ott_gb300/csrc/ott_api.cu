@@ -153,8 +153,11 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     if (B < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || G < 1 || R < 0 || P < 0 || max_tokens < 0)
         return OTT_ERR_INVALID;
     const int gq = Hq / Hkv;
-    if (!decode_supported(d, gq)) return OTT_ERR_INVALID;
-    if ((long long)B * Hkv > INT_MAX / 64 || (long long)G + R + P > (1 << 20)) return OTT_ERR_INVALID;
+    if (!decode_supported(d)) return OTT_ERR_INVALID;
+    // query heads per decode pass, and passes (slices) per kv head
+    const int gs = slice_heads(gq), S = (gq + gs - 1) / gs;
+    if ((long long)B * Hkv * S > INT_MAX / 64 || (long long)B * Hq > INT_MAX / 4 || (long long)G + R + P > (1 << 20))
+        return OTT_ERR_INVALID;
 
     int dev = 0, sms = 0, smem_optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -162,7 +165,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return OTT_ERR_CUDA;
     const int fsmem = flush_smem_bytes(d, G, P);
-    if (fsmem > smem_optin || decode_smem_bytes(d, gq) > smem_optin) return OTT_ERR_INVALID;
+    if (fsmem > smem_optin || decode_smem_bytes(d, gs) > smem_optin) return OTT_ERR_INVALID;
 
     ott_cache *c = new (std::nothrow) ott_cache();
     if (!c) return OTT_ERR_OOM;
@@ -170,6 +173,8 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->max_tokens = max_tokens;
     c->U = B * Hkv;
     c->gq = gq;
+    c->gs = gs;
+    c->S = S;
     c->ring = G + R;
     c->NB = max_tokens >= G + R ? (max_tokens - R) / G : 0;
     c->ntile = ntiles_of(G);
@@ -178,9 +183,9 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->sm_count = sms;
     c->flush_smem = fsmem;
     // the decode grid's warps split the work items evenly; a warp's range
-    // (at most W/NW + 1 items) touches at most U/NW + 2 units
+    // (at most W/NW + 1 items) touches at most U*S/NW + 2 units (kv-head slices)
     const int nwarps = sms * DEC_WARPS;
-    c->maxu = (int)((long long)B * Hkv / nwarps) + 2;
+    c->maxu = (int)((long long)B * Hkv * S / nwarps) + 2;
     // ragged batches: units differ in length, so a range of L items can touch
     // up to L units; L <= ceil(W_max / warps) with at most NB blocks of
     // chunks_per_block(G) items and ceil((G + R + P) / FP16_CHUNK) fp16 items
@@ -190,7 +195,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->maxu_r = 0;
     if (ragged) {
         const long long iu_max = (G + R + P + FP16_CHUNK - 1) / FP16_CHUNK + (long long)c->NB * chunks_per_block(G);
-        const long long w_max = (long long)B * Hkv * iu_max;
+        const long long w_max = (long long)B * Hkv * S * iu_max;
         c->maxu_r = (int)((w_max + nwarps - 1) / nwarps) + 2;
         c->Tb.assign(B, 0);
         c->nfb.assign(B, 0);
@@ -207,7 +212,7 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     const size_t sz_ring = U * c->ring * (size_t)d * 2;
     const size_t sz_pool = U * (size_t)P * d * 2;
     const size_t sz_pn = U * (size_t)P * 4;
-    const size_t sz_part = (size_t)nwarps * maxu_alloc * 2 * gq * (d + 2) * 4;
+    const size_t sz_part = (size_t)nwarps * maxu_alloc * 2 * gs * (d + 2) * 4;
     c->cold = cold;
     c->pct = pct;
     c->n_oc = n_oc;
@@ -276,10 +281,10 @@ int create_cache(int B, int Hq, int Hkv, int d, int G, int R, int P, int max_tok
     c->fstack = sz_fs ? reinterpret_cast<int32_t *>(base + o_fs) : nullptr;
     c->ftop = reinterpret_cast<int *>(base + o_ft);
     c->bound = reinterpret_cast<float *>(base + o_bnd);
-    c->topk_ok = topk_smem_bytes(d, gq, c->NB) <= smem_optin - 2048;
+    c->topk_ok = topk_smem_bytes(d, gs, c->NB) <= smem_optin - 2048;
     e = cudaMemset(mem, 0, c->mem_bytes);
-    if (e == cudaSuccess) e = set_kernel_attributes(d, gq, smem_optin);
-    if (e == cudaSuccess) e = set_topk_attributes(d, gq, smem_optin);
+    if (e == cudaSuccess) e = set_kernel_attributes(d, gs, smem_optin);
+    if (e == cudaSuccess) e = set_topk_attributes(d, gs, smem_optin);
     if (e == cudaSuccess && c->paged) {
         // every pool slot free
         std::vector<int32_t> slots((size_t)pool_blocks);

@@ -134,6 +134,9 @@ struct DecodeArgs {
     float *part;
     int *ctl;
     int Hq, Hkv, G;
+    // a kv head's g = Hq/Hkv query heads are served in S passes of GQ heads
+    // (slices); work units are (sequence, kv head, slice), u = (b*Hkv + hkv)*S + s
+    int g, S;
     int nf, jfull;      // blocks; blocks j >= jfull hold G tokens
     int ring_start;     // first residual token's ring slot
     int ntail, npool;
@@ -235,7 +238,7 @@ __device__ __forceinline__ UnitInfo unit_at(const DecodeArgs &a, const TableT<RG
         }
         const SeqEntry &e = st.e[lo];
         const int h = (int)((unsigned)(x - e.base) / (unsigned)e.Iu);
-        r.u = lo * a.Hkv + h;
+        r.u = lo * a.Hkv * a.S + h;
         r.ub = e.base + (long long)h * e.Iu;
         r.ntail = e.ntail;
         r.npool = e.npool;
@@ -265,16 +268,27 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[NW]) {
     }
 }
 
+// The GQ query heads of work unit u (a kv-head slice); heads of a padded
+// last slice repeat the kv head's last query head (their results are unused).
 template <int D, int GQ>
 __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
-    const int b = u / a.Hkv, hkv = u % a.Hkv;
-    const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + hkv * GQ) * D);
-    for (int e = lane; e < GQ * D / 2; e += 32) reinterpret_cast<__half2 *>(qsm)[e] = qp[e];
+    if (a.S == 1 && a.g == GQ) {
+        const int b = u / a.Hkv, hkv = u % a.Hkv;
+        const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + hkv * GQ) * D);
+        for (int e = lane; e < GQ * D / 2; e += 32) reinterpret_cast<__half2 *>(qsm)[e] = qp[e];
+    } else {
+        const int Hv = a.Hkv * a.S, b = u / Hv, hv = u % Hv, hkv = hv / a.S, h0 = (hv % a.S) * GQ;
+        const __half2 *qp = reinterpret_cast<const __half2 *>(a.q + ((size_t)b * a.Hq + (size_t)hkv * a.g) * D);
+        for (int e = lane; e < GQ * D / 2; e += 32) {
+            const int h = min(h0 + e / (D / 2), a.g - 1);
+            reinterpret_cast<__half2 *>(qsm)[e] = qp[h * (D / 2) + e % (D / 2)];
+        }
+    }
     __syncwarp();
 }
 
 // ---------------------------------------------------------------- quantized segment
-// Quantized work items [q0, q1) of unit u: item q is the block at position
+// Quantized work items [q0, q1) of kv unit u (queries of work unit uq): item q is the block at position
 // q / IPB (Top-K: the block listed there in the unit's selection), whole
 // (IPB = 1) or its chunk q % IPB (IPB = CPB: chunks of up to CHUNK_TILES
 // tiles); the partial goes to part[slot]. Chunks past a short block's tokens
@@ -287,7 +301,7 @@ __device__ void load_queries(const DecodeArgs &a, int u, float *qsm, int lane) {
 // G tokens) runs a body without any masking; the ragged last chunk of a short
 // block takes the masked body.
 template <int D, int GQ, bool CO, bool TK, bool RG>
-__device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, int q1, uint8_t *stg0,
+__device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int uq, int q0, int q1, uint8_t *stg0,
                               uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, __half *qhl,
                               int lane) {
     using C = Cfg<D, GQ>;
@@ -367,7 +381,7 @@ __device__ bool quant_segment(const DecodeArgs &a, size_t slot, int u, int q0, i
         advance(ic);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    load_queries<D, GQ>(a, u, qsm, lane);
+    load_queries<D, GQ>(a, uq, qsm, lane);
 
     // Cooperative per-block constants: lane L handles channel pairs
     // (2L + 64m, 2L + 64m + 1); the channels' class scales stay in registers
@@ -743,7 +757,7 @@ __device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1,
 // (token f >= ntail + npool: its (f - ntail - npool)-th oldest entry); its
 // size is read on the device, and the host sizes the items for C entries.
 template <int D, int GQ, bool CO>
-__device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slot, int u, int c0, int c1,
+__device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slot, int u, int uq, int c0, int c1,
                              uint8_t *stg0, uint8_t *stg1, uint64_t *bars, uint32_t &phase, float *qsm, int lane) {
     constexpr int NKT = D / 16;
     constexpr int RS = D + 8;                 // padded row stride (halves)
@@ -797,7 +811,7 @@ __device__ bool fp16_segment(const DecodeArgs &a, const UnitInfo &ui, size_t slo
         issue(k, st_issue);
         st_issue ^= 1;
     }
-    load_queries<D, GQ>(a, u, qsm, lane);
+    load_queries<D, GQ>(a, uq, qsm, lane);
     // score B operand: column r = (head r/2, piece r&1); q is exact in fp16
     const int hB = r >> 1;
     uint32_t Bq[NKT][2];
@@ -923,19 +937,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_decode(DecodeArgs a, cons
     const int u_first = unit_at<RG>(a, st, x).u;
     while (x < x1) {
         const UnitInfo ui = unit_at<RG>(a, st, x);
-        const int u = ui.u;
+        const int u = ui.u;                           // work unit (kv-head slice)
+        const int ud = a.S == 1 ? u : u / a.S;        // its kv unit: the cache data
         const long long ubase = ui.ub;
         const int off = (int)(x - ubase);
         if (off < ui.Sf) {
             const int end = (int)min(x1 - ubase, (long long)ui.Sf);
-            if (!fp16_segment<D, GQ, CO>(a, ui, part_slot(a, gw, u - u_first, 0), u, off, end, stg0, stg1, bars,
+            if (!fp16_segment<D, GQ, CO>(a, ui, part_slot(a, gw, u - u_first, 0), ud, u, off, end, stg0, stg1, bars,
                                      phase, qsm, lane))
                 return;
             x = ubase + end;
         } else {
             const int end = (int)min(x1 - ubase, (long long)ui.Iu);
-            if (!quant_segment<D, GQ, CO, TK, RG>(a, part_slot(a, gw, u - u_first, 1), u, off - ui.Sf, end - ui.Sf, stg0,
-                                      stg1, bars, phase, qsm, qhl, lane))
+            if (!quant_segment<D, GQ, CO, TK, RG>(a, part_slot(a, gw, u - u_first, 1), ud, u, off - ui.Sf, end - ui.Sf,
+                                      stg0, stg1, bars, phase, qsm, qhl, lane))
                 return;
             x = ubase + end;
         }
@@ -964,7 +979,9 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
     __shared__ float red[COMB_MAXW][DC + 2];
     const int cw = blockDim.x >> 5, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x / CS, cs = blockIdx.x % CS;
-    const int b = bh / a.Hq, hq = bh % a.Hq, u = b * a.Hkv + hq / GQ, h = hq % GQ;
+    // work unit of query head hq: kv head hq / g, slice (hq mod g) / GQ
+    const int b = bh / a.Hq, hq = bh % a.Hq, hkv = hq / a.g, hs = hq % a.g, h = hs % GQ;
+    const int uv = hkv * a.S + hs / GQ, u = b * a.Hkv * a.S + uv;
     const int ch0 = cs * DC + lane * CPL;   // this lane's first channel
     // The unit's items are [ub, ub + Sf) fp16 then [ub + Sf, ue) quantized; the
     // decode warps holding them are contiguous ranges [f0, f1] and [q0, q1].
@@ -973,7 +990,7 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
     int Iu, Sf;
     if constexpr (RG) {
         const SeqEntry &e = st.e[b];
-        ub = e.base + (long long)(hq / GQ) * e.Iu;
+        ub = e.base + (long long)uv * e.Iu;
         Iu = e.Iu;
         Sf = e.Sf;
     } else {
@@ -1077,7 +1094,7 @@ __global__ void __launch_bounds__(COMB_MAXW * 32) k_combine(DecodeArgs a, const 
 template <int D, int GQ, bool RG>
 cudaError_t launch_combine(const DecodeArgs &a, const TableT<RG> &st, int B, cudaStream_t s) {
     // candidate segments per unit: about 2 * (decode warps covering a unit)
-    const long long U = (long long)B * a.Hkv;
+    const long long U = (long long)B * a.Hkv * a.S;
     const long long per_unit_warps = (a.NWp + U - 1) / U + 1;
     int cw = (int)((2 * per_unit_warps + 2 * COMB_GRP - 1) / (2 * COMB_GRP));   // about two rounds per warp
     cw = cw < 1 ? 1 : (cw > COMB_MAXW ? COMB_MAXW : cw);
@@ -1144,6 +1161,8 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     a.ctl = c->ctl;
     a.Hq = c->Hq;
     a.Hkv = c->Hkv;
+    a.g = c->gq;
+    a.S = c->S;
     a.G = c->G;
     a.B = c->B;
     a.jfull = (c->P + c->G - 1) / c->G;   // from this block on, the pool is full
@@ -1156,9 +1175,9 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
     long long nblk = 0;
     if constexpr (RG) {
         for (int b = 0; b < c->B; ++b)
-            nblk += (long long)c->Hkv * (TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b]);
+            nblk += (long long)c->Hkv * c->S * (TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b]);
     } else {
-        nblk = (long long)c->U * (TK ? (c->nf < Kc ? c->nf : Kc) : c->nf);
+        nblk = (long long)c->U * c->S * (TK ? (c->nf < Kc ? c->nf : Kc) : c->nf);
     }
     const long long nwarps = (long long)c->sm_count * DEC_WARPS;
     a.IPB = nblk >= nwarps ? a.CPB : 1;
@@ -1168,7 +1187,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
         for (int b = 0; b < c->B; ++b) {
             st.e[b] = seq_entry(c, c->Tb[b], c->nfb[b], TK ? (c->nfb[b] < Kc ? c->nfb[b] : Kc) : c->nfb[b], a.IPB);
             st.e[b].base = base;
-            base += (long long)c->Hkv * st.e[b].Iu;
+            base += (long long)c->Hkv * c->S * st.e[b].Iu;
         }
         st.e[c->B] = SeqEntry{};
         st.e[c->B].base = base;
@@ -1183,7 +1202,7 @@ cudaError_t launch_decode_t(const ott_cache *c, const __half *q, __half *out, fl
         a.npool = e.npool;
         a.Sf = e.Sf;
         a.Iu = e.Iu;
-        a.W = (long long)c->U * a.Iu;
+        a.W = (long long)c->U * c->S * a.Iu;
         a.MAXU = c->maxu;
     }
     // never more active warps than items: every active warp owns >= 1 item
@@ -1263,13 +1282,11 @@ cudaError_t launch_decode_topk_t(const ott_cache *c, const __half *q, __half *ou
 
 }  // namespace
 
-bool decode_supported(int d, int gq) {
-    return (d == 64 || d == 128) && (gq == 1 || gq == 2 || gq == 4);
-}
+bool decode_supported(int d) { return d == 64 || d == 128; }
 
-int decode_smem_bytes(int d, int gq) {
+int decode_smem_bytes(int d, int gs) {
 #define OTT_SM(D_, G_) \
-    if (d == D_ && gq == G_) return Cfg<D_, G_>::WARP_SMEM * DEC_WARPS;
+    if (d == D_ && gs == G_) return Cfg<D_, G_>::WARP_SMEM * DEC_WARPS;
     OTT_SM(128, 1) OTT_SM(128, 2) OTT_SM(128, 4) OTT_SM(64, 1) OTT_SM(64, 2) OTT_SM(64, 4)
 #undef OTT_SM
     return 1 << 30;
@@ -1277,11 +1294,11 @@ int decode_smem_bytes(int d, int gq) {
 
 // Both kernels may use up to smem_max bytes of dynamic shared memory (the
 // device's opt-in limit), so caches of different shapes never conflict.
-cudaError_t set_kernel_attributes(int d, int gq, int smem_max) {
+cudaError_t set_kernel_attributes(int d, int gs, int smem_max) {
     cudaError_t e = set_flush_attributes(d, smem_max);
     if (e != cudaSuccess) return e;
 #define OTT_ATTR(D_, G_) \
-    if (d == D_ && gq == G_) return set_decode_attr<D_, G_>(smem_max);
+    if (d == D_ && gs == G_) return set_decode_attr<D_, G_>(smem_max);
     OTT_ATTR(128, 1) OTT_ATTR(128, 2) OTT_ATTR(128, 4) OTT_ATTR(64, 1) OTT_ATTR(64, 2) OTT_ATTR(64, 4)
 #undef OTT_ATTR
     return cudaErrorInvalidValue;
@@ -1289,7 +1306,7 @@ cudaError_t set_kernel_attributes(int d, int gq, int smem_max) {
 
 cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s) {
 #define OTT_DECK(D_, G_) \
-    if (c->d == D_ && c->gq == G_) return launch_decode_topk_t<D_, G_>(c, q, out, Kc, s);
+    if (c->d == D_ && c->gs == G_) return launch_decode_topk_t<D_, G_>(c, q, out, Kc, s);
     OTT_DECK(128, 1) OTT_DECK(128, 2) OTT_DECK(128, 4) OTT_DECK(64, 1) OTT_DECK(64, 2) OTT_DECK(64, 4)
 #undef OTT_DECK
     return cudaErrorInvalidValue;
@@ -1297,7 +1314,7 @@ cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out,
 
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s) {
 #define OTT_DEC(D_, G_) \
-    if (c->d == D_ && c->gq == G_) return launch_decode_any<D_, G_>(c, q, out, c->part, s);
+    if (c->d == D_ && c->gs == G_) return launch_decode_any<D_, G_>(c, q, out, c->part, s);
     OTT_DEC(128, 1) OTT_DEC(128, 2) OTT_DEC(128, 4) OTT_DEC(64, 1) OTT_DEC(64, 2) OTT_DEC(64, 4)
 #undef OTT_DEC
     return cudaErrorInvalidValue;
@@ -1420,7 +1437,7 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
     if (cudaGetDevice(&dev) != cudaSuccess) return OTT_ERR_CUDA;
     if (dev != c->device) return OTT_ERR_STATE;   // the cache's device must be current
     const int maxu = c->ragged ? c->maxu_r : c->maxu;
-    const size_t need = (size_t)c->sm_count * DEC_WARPS * maxu * 2 * c->gq * (c->d + 2);
+    const size_t need = (size_t)c->sm_count * DEC_WARPS * maxu * 2 * c->gs * (c->d + 2);
     if (need > kStaticScratchFloats) return OTT_ERR_CAPACITY;
     float *scratch = nullptr;
     if (static_scratch_address(dev, &scratch) != cudaSuccess) return OTT_ERR_CUDA;
@@ -1429,7 +1446,7 @@ extern "C" int ott_decode_attn_static(ott_cache *c, const void *q, void *out, vo
     const __half *qh = static_cast<const __half *>(q);
     __half *oh = static_cast<__half *>(out);
 #define OTT_DEC_S(D_, G_) \
-    if (c->d == D_ && c->gq == G_) e = launch_decode_any<D_, G_>(c, qh, oh, scratch, s);
+    if (c->d == D_ && c->gs == G_) e = launch_decode_any<D_, G_>(c, qh, oh, scratch, s);
     OTT_DEC_S(128, 1) OTT_DEC_S(128, 2) OTT_DEC_S(128, 4) OTT_DEC_S(64, 1) OTT_DEC_S(64, 2) OTT_DEC_S(64, 4)
 #undef OTT_DEC_S
     if (e != cudaSuccess) {

@@ -127,6 +127,10 @@ __host__ __device__ inline int vsz_index(int t, int gamma) {
 struct ott_cache {
     int B, Hq, Hkv, d, G, R, P, max_tokens;
     int U, gq, ring, NB, ntile;
+    // The decode kernels serve gs query heads of a kv head per pass (1, 2 or
+    // 4); a kv head with gq = Hq / Hkv heads is read in S = ceil(gq / gs)
+    // passes ("slices"), the last one padded with copies of its last head.
+    int gs, S;
     long long blk_bytes;
     long long T;
     int nf;
@@ -137,7 +141,7 @@ struct ott_cache {
     int device;
     int sm_count;
     int flush_smem;
-    int maxu;               // units one decode warp's item range can touch
+    int maxu;               // units (kv-head slices) one decode warp's item range can touch
     // device memory (one allocation)
     void *mem;
     size_t mem_bytes;
@@ -147,7 +151,7 @@ struct ott_cache {
     __half *pk, *pv;        // [U][P][d]
     float *pnorm;           // [U][P]
     int32_t *pidx;          // [U][P]
-    float *part;            // [warps][maxu][2][gq][d+2] split-K partials
+    float *part;            // [warps][maxu][2][gs][d+2] split-K partials
     int *ctl;               // [1] status flag set by a bounded wait that timed out
     __half *qdev;           // [B][Hq][d] the queries of a step fed from host memory
     // sequences of different lengths (ott_create_ragged + ott_prefill_lens)
@@ -230,14 +234,16 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
 cudaError_t launch_decode(const ott_cache *c, const __half *q, __half *out, cudaStream_t s);
 cudaError_t launch_decode_topk(const ott_cache *c, const __half *q, __half *out, int Kc, cudaStream_t s);
 cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int Kc, cudaStream_t s);
-int topk_smem_bytes(int d, int gq, int nf);
-cudaError_t set_topk_attributes(int d, int gq, int smem_max);
+int topk_smem_bytes(int d, int gs, int nf);
+cudaError_t set_topk_attributes(int d, int gs, int smem_max);
 cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *stage, cudaStream_t s);
 size_t export_stage_bytes(const ott_cache *c, int nu, int nf);
 int flush_smem_bytes(int d, int G, int P);
-int decode_smem_bytes(int d, int gq);
-cudaError_t set_kernel_attributes(int d, int gq, int smem_max);
+int decode_smem_bytes(int d, int gs);
+cudaError_t set_kernel_attributes(int d, int gs, int smem_max);
 cudaError_t set_flush_attributes(int d, int smem);
-bool decode_supported(int d, int gq);
+bool decode_supported(int d);
+// query heads per decode pass for gq query heads per kv head
+inline int slice_heads(int gq) { return (gq == 1 || gq == 2 || gq == 4) ? gq : 4; }
 
 }  // namespace ott

@@ -43,6 +43,7 @@ struct TopkArgs {
     const int32_t *bcnt;     // block sizes under the cold-pool policy, else null
     const __half *q;         // [B][Hq][d]
     int Hq, Hkv;
+    int g;                   // query heads per kv head (taken GQ at a time)
     int K;                   // blocks to keep
     int Kc;                  // slots per unit in sel: min(K, nf)
     float *bound;            // [U][NB] scratch: block bounds
@@ -77,8 +78,12 @@ __global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a, const _
     if (j0 >= nf_u) return;   // the whole CTA: this unit has fewer blocks
     const int nb = min(BND_BLOCKS, nf_u - j0);
     const int b = u / a.Hkv, hk = u % a.Hkv;
-    const __half *qp = a.q + ((size_t)b * a.Hq + hk * GQ) * D;
-    for (int e = tid; e < GQ * D; e += nth) qs[e] = __half2float(qp[e]);
+    const __half *qp = a.q + ((size_t)b * a.Hq + (size_t)hk * a.g) * D;
+    // the first GQ query heads (a kv head with fewer repeats its last one)
+    auto load_q = [&](int s0) {
+        for (int e = tid; e < GQ * D; e += nth) qs[e] = __half2float(qp[(size_t)min(s0 + e / D, a.g - 1) * D + e % D]);
+    };
+    load_q(0);
     uint4 buf[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -100,32 +105,40 @@ __global__ void __launch_bounds__(BND_THREADS) k_topk_bounds(TopkArgs a, const _
             dst[3] = buf[i].w;
         }
     }
-    __syncthreads();
     const int r = tid % BND_BLOCKS, h = tid / BND_BLOCKS;
-    if (h < GQ && r < nb) {
-        float acc = 0.0f;
-        const uint32_t *row = hdr + r * RW;
-        const float *qh = qs + h * D;
-#pragma unroll 8
-        for (int c = 0; c < D; ++c) {
-            const uint32_t w = row[c];
-            const float s = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
-            const float z = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
-            const float top = __fadd_rn(z, __fmul_rn(3.0f, s));
-            const float lo = __fmul_rn(qh[c], z), hi = __fmul_rn(qh[c], top);
-            acc = __fadd_rn(acc, hi > lo ? hi : lo);
+    float best = -CUDART_INF_F;   // thread tid < nb: block j0 + tid, over the heads so far
+    // the kv head's g query heads, GQ per round (a short last round repeats
+    // its last head, which leaves the maximum unchanged)
+    for (int s0 = 0; s0 < a.g; s0 += GQ) {
+        if (s0 > 0) {
+            __syncthreads();   // the previous round's heads and bounds are read
+            load_q(s0);
         }
-        part[h][r] = acc;
+        __syncthreads();
+        if (h < GQ && r < nb) {
+            float acc = 0.0f;
+            const uint32_t *row = hdr + r * RW;
+            const float *qh = qs + h * D;
+#pragma unroll 8
+            for (int c = 0; c < D; ++c) {
+                const uint32_t w = row[c];
+                const float s = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+                const float z = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+                const float top = __fadd_rn(z, __fmul_rn(3.0f, s));
+                const float lo = __fmul_rn(qh[c], z), hi = __fmul_rn(qh[c], top);
+                acc = __fadd_rn(acc, hi > lo ? hi : lo);
+            }
+            part[h][r] = acc;
+        }
+        __syncthreads();
+        if (tid < nb)
+#pragma unroll
+            for (int x = 0; x < GQ; ++x) best = part[x][tid] > best ? part[x][tid] : best;
     }
-    __syncthreads();
     if (tid < nb) {
         const int j = j0 + tid;
         const int cnt = a.bcnt ? a.bcnt[(size_t)u * a.NB + j] : (j >= a.jfull ? a.G : block_count(a.P, a.G, j));
-        float best = -CUDART_INF_F;
-        if (cnt > 0)
-#pragma unroll
-            for (int x = 0; x < GQ; ++x) best = part[x][tid] > best ? part[x][tid] : best;
-        a.bound[(size_t)u * a.NB + j] = best;
+        a.bound[(size_t)u * a.NB + j] = cnt > 0 ? best : -CUDART_INF_F;
     }
 }
 
@@ -265,9 +278,9 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_pick(TopkArgs a, const __
 
 }  // namespace
 
-int topk_smem_bytes(int d, int gq, int nf) {
+int topk_smem_bytes(int d, int gs, int nf) {
     (void)d;
-    (void)gq;
+    (void)gs;
     return (nf > 1 ? nf : 1) * 4;
 }
 
@@ -295,6 +308,7 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     a.q = q;
     a.Hq = c->Hq;
     a.Hkv = c->Hkv;
+    a.g = c->gq;
     a.K = K;
     a.Kc = Kc;
     a.bound = c->bound;
@@ -302,7 +316,7 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     const dim3 grid((unsigned)((nf_max + BND_BLOCKS - 1) / BND_BLOCKS), (unsigned)c->U);
     bool found = false;
 #define OTT_BND(D_, G_)                                                       \
-    if (c->d == D_ && c->gq == G_) {                                          \
+    if (c->d == D_ && c->gs == G_) {                                          \
         k_topk_bounds<D_, G_><<<grid, BND_THREADS, 0, s>>>(a, nt);            \
         found = true;                                                         \
     }
@@ -327,9 +341,9 @@ cudaError_t launch_topk_select(const ott_cache *c, const __half *q, int K, int K
     return cudaLaunchKernelEx(&cfg, k_topk_pick, a, nt);
 }
 
-cudaError_t set_topk_attributes(int d, int gq, int smem_max) {
+cudaError_t set_topk_attributes(int d, int gs, int smem_max) {
     (void)d;
-    (void)gq;
+    (void)gs;
     return cudaFuncSetAttribute(k_topk_pick, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max - 2048);
 }
 

@@ -87,9 +87,13 @@ enum {
  * G=128, R=32, P=32). max_tokens bounds T; all device memory is allocated
  * here (blocks, residual ring, pool, split-K scratch) and nothing is
  * allocated by the other calls except ott_export_state's staging buffer.
- * Supported: d in {64, 128}; Hq % Hkv == 0 with Hq/Hkv in {1, 2, 4};
- * G >= 1; R >= 0; P >= 0; (P + G) * (d + 8) * 4 bytes of flush staging must
- * fit in one CTA's shared memory. Uses the current CUDA device.
+ * Supported: d in {64, 128}; Hq % Hkv == 0 (any ratio g = Hq/Hkv); G >= 1;
+ * R >= 0; P >= 0; (P + G) * (d + 8) * 4 bytes of flush staging must fit in
+ * one CTA's shared memory. Uses the current CUDA device.
+ * The decode serves up to 4 query heads of a kv head per read of its blocks:
+ * g in {1, 2, 4} reads each block once per call, any other g reads it
+ * ceil(g / 4) times (the kv head's query heads in slices of 4, the last
+ * slice padded with copies of its last head, whose results are dropped).
  * Returns OTT_OK and *out, or an error with *out = NULL.
  */
 int ott_create(int B, int Hq, int Hkv, int d, int G, int R, int P,
@@ -268,8 +272,9 @@ int ott_step_host(ott_cache *c, const void *k, const void *v, const void *q, voi
  *     Nothing in it needs clearing between calls.
  * Errors: as ott_decode_attn, plus OTT_ERR_STATE if the cache's device is not
  * the current device, and OTT_ERR_CAPACITY if this shape's partials
- * (SMs x 16 warps x (units/warps + 2) x 2 x Hq/Hkv x (d+2) floats) exceed
- * the array.
+ * (SMs x 16 warps x (units/warps + 2) x 2 x gs x (d+2) floats, where
+ * gs = g for g in {1, 2, 4}, else 4, and units = B x Hkv x ceil(g / gs))
+ * exceed the array.
  */
 int ott_decode_attn_static(ott_cache *c, const void *q, void *out, void *stream);
 

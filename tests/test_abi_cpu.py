@@ -56,7 +56,7 @@ def test_status_strings_and_null_handles(libott):
     out = C.c_void_p(123)
     assert libott.ott_create(1, 1, 1, 128, 128, 32, 32, 100, None) == -1
     # unsupported shapes are rejected before any device call
-    assert libott.ott_create(1, 3, 1, 128, 128, 32, 32, 100, C.byref(out)) == -1   # Hq/Hkv = 3
+    assert libott.ott_create(1, 3, 2, 128, 128, 32, 32, 100, C.byref(out)) == -1   # Hq % Hkv != 0
     assert out.value is None
     assert libott.ott_create(1, 1, 1, 96, 128, 32, 32, 100, C.byref(out)) == -1    # d = 96
     assert libott.ott_create(1, 2, 4, 128, 128, 32, 32, 100, C.byref(out)) == -1   # Hq < Hkv

@@ -81,6 +81,7 @@ def _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, Cc, L, steps, seed, every=1):
     (3, 3, 3, 128, 20, 5, 9, 0, 200, 30),        # C = 0: displaced tokens are discarded
     (2, 2, 2, 128, 16, 3, 0, 4, 120, 30),        # P = 0: nothing is ever displaced
     (1, 4, 1, 128, 8, 2, 20, 6, 180, 30),        # P > G: several flushes before the pool is full
+    (2, 12, 2, 128, 16, 4, 6, 5, 260, 40),       # GQA 6: slices of 4 and 2 (padded)
 ])
 def test_cold_every_step(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, Cc, L, steps):
     ev = _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, Cc, L, steps, seed=L + G + Cc)

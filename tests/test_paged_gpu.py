@@ -74,6 +74,7 @@ def _serve(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, lens, steps, events, seed, p
     (4, 4, 2, 128, 16, 3, 5, [40, 97, 18, 130], 30, {6: [(1, 50)], 17: [(0, 3), (3, 77)]}),
     (3, 8, 2, 64, 32, 0, 7, [150, 5, 66], 40, {10: [(0, 200)], 25: [(2, 1)]}),     # GQA 4, d=64, R=0
     (6, 6, 6, 128, 128, 32, 32, [300, 161, 160, 159, 33, 1], 30, {12: [(4, 400)]}),   # the pages' G, R, P
+    (3, 16, 2, 64, 32, 0, 7, [150, 5, 66], 40, {10: [(0, 200)], 25: [(2, 1)]}),   # GQA 8: two slices
 ])
 def test_paged_serving(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, lens, steps, events):
     # a pool just large enough for the run

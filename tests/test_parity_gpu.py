@@ -58,6 +58,10 @@ def _run_small(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps, seed, dup=Fals
     (3, 3, 3, 64, 20, 5, 0, 90, 30),          # G not a multiple of 16, P=0
     (1, 4, 1, 128, 48, 4, 60, 200, 30),       # P > G (empty first blocks), GQA 4
     (2, 2, 2, 128, 4, 1, 2, 60, 20),          # tiny G
+    (2, 6, 2, 128, 16, 3, 5, 100, 30),        # GQA 3: one slice of four, padded
+    (1, 16, 2, 64, 32, 0, 7, 150, 40),        # GQA 8: two slices, d=64, R=0
+    (2, 5, 1, 128, 20, 5, 40, 120, 30),       # GQA 5: slices of 4 and 1, P > G
+    (1, 32, 1, 128, 16, 4, 8, 90, 20),        # multi-query (GQA 32): eight slices
 ])
 def test_small_shapes_every_step(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps):
     _run_small(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps, seed=L * 7 + G)

@@ -66,6 +66,7 @@ def _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps, seed, eve
     (3, 3, 3, 128, 20, 5, 10, 100, 1, 200, 25),       # 1%: one outlier per flush; G not a multiple of 16
     (1, 4, 1, 128, 16, 2, 40, 3000, 128, 150, 40),    # GQA 4, P above the fixed point, every channel
     (1, 2, 1, 128, 8, 2, 3, 0, 2, 40, 30),            # p = 0: no pool; the first flushes during the steps
+    (2, 16, 2, 64, 16, 0, 7, 5000, 3, 260, 40),       # GQA 8 (two slices), d = 64
 ])
 def test_pct_small(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps):
     T, nf, tail, npool = _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, pct, n_oc, L, steps, seed=B + G + pct)

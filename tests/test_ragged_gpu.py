@@ -73,6 +73,7 @@ def _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, lens, steps, seed, every=1):
     (5, 2, 1, 128, 20, 4, 0, [19, 20, 23, 24, 60], 30),   # G not a multiple of 16, P=0, lengths around G+R
     (2, 4, 1, 128, 48, 4, 60, [200, 7], 30),              # P > G (empty first blocks), GQA 4
     (6, 6, 6, 128, 128, 32, 32, [300, 161, 160, 159, 33, 1], 40),   # the pages' G, R, P
+    (3, 15, 3, 128, 32, 0, 7, [150, 5, 66], 50),          # GQA 5: slices of 4 and 1 per kv head
 ])
 def test_ragged_every_step(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, lens, steps):
     _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, lens, steps, seed=sum(lens) + G)

@@ -29,6 +29,7 @@ def _gen(seed, B, Hkv, Hq, T, d):
     (2, 8, 2, 128, 16, 4, 8, 130, 40, False),     # GQA 4
     (1, 4, 2, 64, 32, 8, 6, 60, 50, False),       # d = 64, GQA 2, the first flush during the steps
     (3, 4, 4, 128, 16, 4, 5, 90, 30, True),       # ragged batch
+    (2, 12, 2, 128, 16, 4, 8, 130, 40, False),    # GQA 6: slices of 4 and 2
 ])
 def test_step_host_equals_device_path(ott, B, Hq, Hkv, d, G, R, P, L, steps, ragged):
     K, V, Q = _gen(B + G, B, Hkv, Hq, L + steps, d)

@@ -71,6 +71,8 @@ def _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps, Ks, seed, cold=None,
     (2, 4, 2, 64, 16, 0, 7, 260, 30, (2, 5)),           # GQA 2, d = 64, R = 0
     (3, 3, 3, 128, 20, 5, 0, 200, 25, (1, 6)),          # G not a multiple of 16, P = 0
     (1, 1, 1, 128, 8, 2, 3, 40, 30, (1, 2)),            # the first flushes happen during the steps
+    (1, 16, 2, 128, 32, 8, 40, 700, 40, (1, 3, 7)),     # GQA 8: bounds over both slices' heads
+    (2, 6, 2, 64, 16, 0, 7, 260, 30, (2, 5)),           # GQA 3 (a padded slice), d = 64
 ])
 def test_topk_every_step(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps, Ks):
     _run(oracle_mod, ott, B, Hq, Hkv, d, G, R, P, L, steps, Ks, seed=L + G)

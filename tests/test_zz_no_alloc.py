@@ -32,6 +32,8 @@ def _static_decode(ott, cache, q, out):
     (4, 8, 8, 128, 128, 32, 32, 700),     # MHA, several flushes
     (2, 8, 2, 128, 32, 4, 6, 300),        # GQA 4
     (3, 2, 1, 64, 16, 3, 5, 120),         # d = 64, GQA 2
+    (2, 16, 2, 128, 32, 4, 6, 300),       # GQA 8: two slices
+    (3, 3, 1, 64, 16, 3, 5, 120),         # GQA 3: a padded slice
 ])
 def test_static_decode_matches_decode_twice(ott, B, Hq, Hkv, d, G, R, P, L):
     g = torch.Generator().manual_seed(L + G)
