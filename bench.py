@@ -35,6 +35,8 @@ from bit_kv_cache_ott_gb300 import metrics, synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "OTT decode-attn GB/s (% of HBM peak) and decode tokens/s at B=32, 4K ctx"
+E2E_START = ("caches rebuilt from the same prompts and advanced by the same warm-up steps: the e2e steps take "
+             "the device-timed steps' inputs at the same context lengths")
 E2E_ZERO_COPY_MAX = 512 * 1024   # step inputs at or above this travel by copy, below it by ott_step_host
 DECODE_SRC = os.path.join(ROOT, "bit_kv_cache_ott_gb300", "csrc", "ott_decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
@@ -419,24 +421,32 @@ def run_ours(args, w):
 
     # weak scaling: rank r holds its own shard of B sequences
     wr = shard(w, rank, ws)
-    K_steps, W_steps, E_steps = args.steps, args.warmup, args.e2e_steps
-    total_steps = W_steps + K_steps + E_steps + w.G + 2   # + the flush probe
-    caches = []
+    K_steps, W_steps = args.steps, args.warmup
+    # e2e: by default the same steps as the timed region, on caches rebuilt
+    # from the same prompts (so at the same context lengths)
+    E_steps = K_steps if args.e2e_steps < 0 else args.e2e_steps
+    total_steps = W_steps + max(K_steps, E_steps) + w.G + 2   # + the flush probe
     lens = synth.seq_lens(wr)
-    for layer in range(w.layers):
-        pool = None
-        if w.paged:   # the blocks the run fills, from one pool
-            pool = sum(metrics.flush_count(t + total_steps, w.G, w.R) for t in lens) * w.Hkv + 1
-        c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged,
-                         cold=cold_of(w), pool_blocks=pool)
-        K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
-        if w.ragged:
-            c.prefill_lens(K, V, lens)
-        else:
-            c.prefill(K, V)
-        del K, V
-        caches.append(c)
-    torch.cuda.synchronize()
+
+    def build_caches():
+        cs = []
+        for layer in range(w.layers):
+            pool = None
+            if w.paged:   # the blocks the run fills, from one pool
+                pool = sum(metrics.flush_count(t + total_steps, w.G, w.R) for t in lens) * w.Hkv + 1
+            c = ott.OTTCache(w.B, w.Hq, w.Hkv, w.d, w.G, w.R, w.P, max_tokens=w.L + total_steps, ragged=w.ragged,
+                             cold=cold_of(w), pool_blocks=pool)
+            K, V = synth.prefill_kv(wr, layer=layer, device=str(dev))
+            if w.ragged:
+                c.prefill_lens(K, V, lens)
+            else:
+                c.prefill(K, V)
+            del K, V
+            cs.append(c)
+        torch.cuda.synchronize()
+        return cs
+
+    caches = build_caches()
 
     # step inputs (drawn on the host with the CPU generator, staged on the device)
     n_distinct = min(total_steps, 64)
@@ -580,6 +590,7 @@ def run_ours(args, w):
 
     for c in caches:
         c.check_device()
+    cache_bytes = caches[0].device_bytes() * w.layers
 
     value = job_tokens_per_s(w.B, K_steps, ws, ms_amortized)
     n_launch = n_dec * w.layers
@@ -591,12 +602,24 @@ def run_ours(args, w):
     # the copy stream brings in step s+1's inputs and reads back step s's
     # output while step s's kernels run, as a serving loop would drive the API.
     e2e = None
+    if E_steps > 0:
+        # the e2e run starts from the prompts again and takes the same warm-up
+        # steps (device-resident inputs, untimed): its timed steps then see the
+        # same inputs, context lengths and flushes as the device-timed region
+        for c in caches:
+            c.close()
+        caches = build_caches()
+        for s in range(W_steps):
+            step(s)
+        torch.cuda.synchronize()
     # Feeding the kernels from pinned host memory (ott_step_host) keeps the
     # launch chain but puts host-memory latency on each step's critical path;
     # it pays for small inputs. Steps with large inputs copy them on a second
     # stream a step ahead instead.
     in_step_bytes = sum(t.numel() * t.element_size() for t in host[0])
-    copy_stream_e2e = in_step_bytes >= E2E_ZERO_COPY_MAX
+    # (caches that fit in L2 are timed step by step with L2 flushed in between,
+    # which a copy stream running a step ahead cannot be)
+    copy_stream_e2e = in_step_bytes >= E2E_ZERO_COPY_MAX and not l2_flush
     if E_steps > 0 and copy_stream_e2e:
         # each step's k, v and q travel in one pinned buffer (one copy per step)
         shapes = [tuple(t.shape) for t in host[0]]
@@ -618,7 +641,7 @@ def run_ours(args, w):
             with torch.cuda.stream(cstream):
                 if s >= nb:
                     cstream.wait_event(computed[b])
-                flat[b].copy_(pin[(W_steps + K_steps + s) % n_distinct], non_blocking=True)
+                flat[b].copy_(pin[(W_steps + s) % n_distinct], non_blocking=True)
                 copied[b].record(cstream)
 
         torch.cuda.synchronize()
@@ -651,7 +674,8 @@ def run_ours(args, w):
         e2e = {"value": job_tokens_per_s(w.B, E_steps, ws, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(pin[0].numel() * pin[0].element_size()),
                "d2h_bytes_per_step": int(out_h[0].numel() * out_h[0].element_size()), "steps": E_steps,
-               "copies": "k, v, q in one pinned host buffer per step, double-buffered on a second stream"}
+               "copies": "k, v, q in one pinned host buffer per step, double-buffered on a second stream",
+               "start": E2E_START}
 
     # ott_step_host appends k, v and decodes q (full or Top-K) straight from
     # pinned host memory (the append kernel reads them; the combine writes out
@@ -663,25 +687,36 @@ def run_ours(args, w):
         offs = (0, sizes[0], sizes[0] + sizes[1])
         views = [tuple(p_.narrow(0, o, n).view(sh) for o, n, sh in zip(offs, sizes, shapes)) for p_ in pin]
         out_h = [torch.empty(w.B, w.Hq, w.d, dtype=torch.float16).pin_memory() for _ in range(2)]
+        # with an L2 flush, each step has its own events and the flush falls outside
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(E_steps if l2_flush else 1)]
         torch.cuda.synchronize()
         barrier()
-        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        x0.record(stream)
+        if not l2_flush:
+            ev[0][0].record(stream)
         for s in range(E_steps):
-            kh, vh, qh = views[(W_steps + K_steps + s) % n_distinct]
+            kh, vh, qh = views[(W_steps + s) % n_distinct]
+            if l2_flush:
+                flush_l2(s)
+                ev[s][0].record(stream)
             for c in caches:
                 c.step_host(kh, vh, qh, out_h[s % 2], w.topk, stream)
-        x1.record(stream)
+            if l2_flush:
+                ev[s][1].record(stream)
+        if not l2_flush:
+            ev[0][1].record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = max_over_ranks(x0.elapsed_time(x1), dev)
+        ems = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in ev), dev)
         in_bytes = int(pin[0].numel() * pin[0].element_size())
         out_bytes = int(out_h[0].numel() * out_h[0].element_size())
         e2e = {"value": job_tokens_per_s(w.B, E_steps, ws, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": in_bytes * w.layers, "d2h_bytes_per_step": out_bytes * w.layers,
                "steps": E_steps,
                "copies": "ott_step_host per layer: k, v and q read by the append kernel from one pinned host "
-                         "buffer per step, out written by the combine into pinned host memory (two, alternating)"}
+                         "buffer per step, out written by the combine into pinned host memory (two, alternating)",
+               "start": E2E_START,
+               "l2": "flushed between steps (each step timed on its own)" if l2_flush else "no flush needed"}
 
     # the prefill of one layer's cache (the parallel pass), timed on its own
     pf = None
@@ -713,7 +748,6 @@ def run_ours(args, w):
                "one_core": {"value": rate1, "cores": 1, "sample": sample1, "seconds": round(dt1, 2)}}
 
     if rank == 0:
-        cache_bytes = caches[0].device_bytes() * w.layers
         fp16_bytes = sum(metrics.fp16_cache_bytes(t, 1, w.Hkv, w.d) for t in synth.seq_lens(wr)) * w.layers
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K_steps,
@@ -778,7 +812,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=-1, help="steps of the e2e run (default: --steps)")
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-units", type=int, default=64)
