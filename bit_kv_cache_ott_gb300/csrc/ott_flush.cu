@@ -72,6 +72,12 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// wait until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 // Position of channel ch within staged row r: the row's 16-byte chunks are
 // permuted by XOR with r mod 8.
@@ -189,30 +195,39 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
     float *kz = ks + D;
     const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
 
-    // 1. stage the candidates: old pool rows, then the group's rows
-    for (int e = tid; e < nc * VPR; e += nth) {
-        const int row = e / VPR, v8 = e % VPR;
-        const __half *sk, *sv;
-        if (row < np0 && ph) {
-            const long long t = (long long)(uint32_t)ph[row];
-            const size_t off = (size_t)(u - a.src_u0) * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
-            sk = a.srcK + off;
-            sv = a.srcV + off;
-        } else if (row < np0) {
-            const size_t off = ((size_t)u * P + row) * D;
-            sk = a.pk + off;
-            sv = a.pv + off;
-        } else {
-            const long long t = t0 + (row - np0);
-            const size_t off = (size_t)(u - a.src_u0) * a.src_unit_stride + (size_t)(t % a.src_mod) * D;
-            sk = a.srcK + off;
-            sv = a.srcV + off;
+    // 1. stage the candidates: old pool rows, then the group's rows, by
+    // asynchronous 16-byte copies (every thread's loads in flight at once).
+    // Source slots: token t sits at t mod src_mod (the ring wraps; a prompt
+    // does not). The group's tokens are consecutive, so their slots follow
+    // from the first one with at most one wrap (G <= the ring).
+    {
+        const size_t uoff = (size_t)(u - a.src_u0) * a.src_unit_stride;
+        const __half *srcK = a.srcK + uoff, *srcV = a.srcV + uoff;
+        const long long s0 = t0 % a.src_mod;
+        for (int e = tid; e < nc * VPR; e += nth) {
+            const int row = e / VPR, v8 = e % VPR;
+            const __half *sk, *sv;
+            if (row < np0 && !ph) {
+                const size_t off = ((size_t)u * P + row) * D;
+                sk = a.pk + off;
+                sv = a.pv + off;
+            } else {
+                long long slot;
+                if (row < np0) {
+                    slot = (long long)(uint32_t)ph[row];
+                    if (slot >= a.src_mod) slot %= a.src_mod;
+                } else {
+                    slot = s0 + (row - np0);
+                    if (slot >= a.src_mod) slot -= a.src_mod;
+                }
+                sk = srcK + (size_t)slot * D;
+                sv = srcV + (size_t)slot * D;
+            }
+            cp_async16(reinterpret_cast<uint4 *>(ck + (size_t)row * RS) + RL::chunk(row, v8),
+                       reinterpret_cast<const uint4 *>(sk) + v8);
+            cp_async16(reinterpret_cast<uint4 *>(cv + (size_t)row * RS) + RL::chunk(row, v8),
+                       reinterpret_cast<const uint4 *>(sv) + v8);
         }
-        // asynchronous 16-byte copies: every thread's loads are in flight at once
-        cp_async16(reinterpret_cast<uint4 *>(ck + (size_t)row * RS) + RL::chunk(row, v8),
-                   reinterpret_cast<const uint4 *>(sk) + v8);
-        cp_async16(reinterpret_cast<uint4 *>(cv + (size_t)row * RS) + RL::chunk(row, v8),
-                   reinterpret_cast<const uint4 *>(sv) + v8);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -354,12 +369,15 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
     // 5. the new pool (old pool rows are already staged in shared memory);
     // a parallel prefill keeps only the last group's
     const bool write_pool = !a.phist || jj == a.pf_nf - 1;
-    for (int e = tid; write_pool && e < nc * VPR; e += nth) {
-        const int row = e / VPR, v8 = e % VPR, rk = rank[row];
-        if (rk < keep) {
-            const size_t off = ((size_t)u * P + rk) * D;
-            reinterpret_cast<uint4 *>(a.pk + off)[v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)];
-            reinterpret_cast<uint4 *>(a.pv + off)[v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)];
+    {
+        uint4 *pk_u = reinterpret_cast<uint4 *>(a.pk + (size_t)u * P * D);
+        uint4 *pv_u = reinterpret_cast<uint4 *>(a.pv + (size_t)u * P * D);
+        for (int e = tid; write_pool && e < nc * VPR; e += nth) {
+            const int row = e / VPR, v8 = e % VPR, rk = rank[row];
+            if (rk < keep) {
+                pk_u[rk * VPR + v8] = reinterpret_cast<const uint4 *>(ck + (size_t)row * RS)[RL::chunk(row, v8)];
+                pv_u[rk * VPR + v8] = reinterpret_cast<const uint4 *>(cv + (size_t)row * RS)[RL::chunk(row, v8)];
+            }
         }
     }
     for (int row = tid; write_pool && row < nc; row += nth) {
