@@ -55,9 +55,28 @@ __device__ __forceinline__ float4 code_rule(float s, float z) {
     return make_float4(z, t1, t2, t3);
 }
 
-__device__ __forceinline__ uint32_t qcode(float x, const float4 &r) {
-    const float a = __fsub_rn(x, r.x);
+// fl32(x - z) for the fp16 value in the low (hi = 0) or high half of w: the
+// mixed-precision subtraction converts x exactly and rounds once
+__device__ __forceinline__ float sub_h(uint32_t w, bool hi, float z) {
+    float d;
+    if (hi)
+        asm("{ .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n sub.rn.f32.f16 %0, h, %2; }" : "=f"(d) : "r"(w), "f"(z));
+    else
+        asm("{ .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n sub.rn.f32.f16 %0, l, %2; }" : "=f"(d) : "r"(w), "f"(z));
+    return d;
+}
+// the code of a = fl32(x - z) under the rule r = (z, t1, t2, t3)
+__device__ __forceinline__ uint32_t qcode_a(float a, const float4 &r) {
     return (uint32_t)(a > r.y) + (uint32_t)(a >= r.z) + (uint32_t)(a > r.w);
+}
+// s + x*x for the fp16 value in half `hi` of w, one rounding (x*x is exact in fp32)
+__device__ __forceinline__ float sq_acc(uint32_t w, bool hi, float s) {
+    float d;
+    if (hi)
+        asm("{ .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n fma.rn.f32.f16 %0, h, h, %2; }" : "=f"(d) : "r"(w), "f"(s));
+    else
+        asm("{ .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n fma.rn.f32.f16 %0, l, l, %2; }" : "=f"(d) : "r"(w), "f"(s));
+    return d;
 }
 
 __device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
@@ -250,12 +269,11 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
                 float s = 0.0f;
                 for (int v8 = 0; v8 < VPR; ++v8) {   // channels 8 v8 .. 8 v8 + 7, in order
                     const uint4 x = kr[RL::chunk(row, v8)];
-                    const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+                    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h[e]);
-                        s = __fadd_rn(s, __fmul_rn(f.x, f.x));
-                        s = __fadd_rn(s, __fmul_rn(f.y, f.y));
+                        s = sq_acc(w4[e], false, s);
+                        s = sq_acc(w4[e], true, s);
                     }
                 }
                 nrm = s;
@@ -516,9 +534,10 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
             for (int p = 0; p < 8; ++p) {
                 // K word: channels 16kt + 2i + 8o (+1) of token tk
                 const int q = 8 * wp + p, o = q / NKT, kt = q % NKT, ch = 16 * kt + 2 * i + 8 * o;
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(krow + RL::pos(rk_, ch)));
-                kw |= qcode(f.x, krule[ch + (ch >> 3)]) << (2 * p);
-                kw |= qcode(f.y, krule[ch + 1 + ((ch + 1) >> 3)]) << (16 + 2 * p);
+                const uint32_t x2 = *reinterpret_cast<const uint32_t *>(krow + RL::pos(rk_, ch));
+                const float4 r0 = krule[ch + (ch >> 3)], r1 = krule[ch + 1 + ((ch + 1) >> 3)];
+                kw |= qcode_a(sub_h(x2, false, r0.x), r0) << (2 * p);
+                kw |= qcode_a(sub_h(x2, true, r1.x), r1) << (16 + 2 * p);
             }
         }
         // V word: channel 16mt + r + 8rowhalf of token slots 16tau + 2i + 8hi (+1)
@@ -532,7 +551,9 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const int q = 8 * wp + p, rowhalf = q / NKT, mt = q % NKT, vch = 16 * mt + r + 8 * rowhalf;
-                    vw |= qcode(__half2float(vrow[RL::pos(rv_, vch)]), vr[(vch / 32) * VS]) << (16 * h + 2 * p);
+                    const float4 rr = vr[(vch / 32) * VS];
+                    const uint32_t x1 = __half_as_ushort(vrow[RL::pos(rv_, vch)]);
+                    vw |= qcode_a(sub_h(x1, false, rr.x), rr) << (16 * h + 2 * p);
                 }
             }
         }
@@ -568,12 +589,11 @@ __global__ void __launch_bounds__(PF_THREADS) k_pf_group(const __half *__restric
 #pragma unroll 4
         for (int v8 = 0; v8 < D / 8; ++v8) {
             const uint4 x = __ldg(row + v8);
-            const __half2 *h = reinterpret_cast<const __half2 *>(&x);
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {   // channels 8 v8 + 2e, 8 v8 + 2e + 1
-                const float2 f = __half22float2(h[e]);
-                s = __fadd_rn(s, __fmul_rn(f.x, f.x));
-                s = __fadd_rn(s, __fmul_rn(f.y, f.y));
+                s = sq_acc(w4[e], false, s);
+                s = sq_acc(w4[e], true, s);
             }
         }
         gkey[t] = ((uint64_t)__float_as_uint(s) << 32) | (uint32_t)(t0 + t);
