@@ -8,6 +8,7 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -72,14 +73,52 @@ void to_per_sequence(ott_cache *c) {
 // needs the flushes one after another, when the call flushes enough units
 // (units_flushing) for group-by-group launches to fill the GPU, or when no
 // scratch could be had: the caller then flushes group by group.
+// The parallel prefill's scratch comes from a stream-ordered pool that the
+// library creates once per device and that keeps up to kScratchKeep bytes
+// between calls: with the default pool's threshold of zero, every prefill
+// after a synchronization would map its scratch afresh (about 0.1 ms of host
+// time before the first kernel). If this pool cannot be had or used (for
+// example after a device reset), the device's default pool serves.
+constexpr uint64_t kScratchKeep = 1ull << 30;
+constexpr int kMaxDevices = 64;
+
+cudaMemPool_t scratch_pool(int dev) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = kScratchKeep;
+        if (cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) cudaGetLastError();
+        pools[dev] = p;
+    }
+    return pools[dev];
+}
+
 bool try_prefill_parallel(const ott_cache *c, const __half *K, const __half *V, long long unit_stride, int src_u0,
                           int u0, int nu, int nf, int units_flushing, cudaStream_t s, cudaError_t &err) {
     err = cudaSuccess;
     if (!prefill_parallel_ok(c, nf, units_flushing)) return false;
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, prefill_scratch_bytes(c, nu, nf), s) != cudaSuccess) {
+    const size_t bytes = prefill_scratch_bytes(c, nu, nf);
+    const cudaMemPool_t pool = scratch_pool(c->device);
+    if (!pool || cudaMallocFromPoolAsync(&scratch, bytes, pool, s) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        scratch = nullptr;
+        if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
     }
     err = launch_prefill_parallel(c, K, V, unit_stride, src_u0, u0, nu, nf, static_cast<uint64_t *>(scratch), s);
     const cudaError_t e2 = cudaFreeAsync(scratch, s);

@@ -610,22 +610,35 @@ __global__ void __launch_bounds__(PF_THREADS) k_pf_group(const __half *__restric
 }
 
 
-// Output k (0-based) of the merge of the ascending lists A (na keys) and B
-// (nb keys), all keys distinct, k < na + nb: a binary search on the merge
-// path for the number of A's keys among the first k + 1.
-__device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int na, const uint64_t *B, int nb, int k) {
-    int lo = max(0, k + 1 - nb), hi = min(k + 1, na);
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (A[mid] < B[k - mid]) lo = mid + 1;
-        else hi = mid;
+// Outputs [k0, k1) (0-based, k1 <= na + nb) of the merge of the ascending
+// lists A (na keys) and B (nb keys), all keys distinct, through emit(k, key):
+// a binary search on the merge path finds how many of A's keys precede
+// output k0, then each output takes the smaller head.
+template <typename Emit>
+__device__ __forceinline__ void merge_range(const uint64_t *A, int na, const uint64_t *B, int nb, int k0, int k1,
+                                            Emit emit) {
+    if (k0 >= k1) return;
+    int ia = 0;   // A's keys among the first k0 outputs
+    if (k0 > 0) {
+        int lo = max(0, k0 - nb), hi = min(k0, na);
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (A[mid] < B[k0 - 1 - mid]) lo = mid + 1;
+            else hi = mid;
+        }
+        ia = lo;
     }
-    uint64_t x = lo > 0 ? A[lo - 1] : 0ull;
-    if (k - lo >= 0) {
-        const uint64_t y = B[k - lo];
-        x = y > x ? y : x;
+    for (int k = k0; k < k1; ++k) {
+        const int ib = k - ia;
+        if (ia < na && (ib >= nb || A[ia] < B[ib])) emit(k, A[ia++]);
+        else emit(k, B[ib]);
     }
-    return x;
+}
+// this lane's share of m outputs: a contiguous range
+__device__ __forceinline__ void lane_range(int m, int lane, int &k0, int &k1) {
+    const int per = (m + 31) >> 5;
+    k0 = min(m, lane * per);
+    k1 = min(m, k0 + per);
 }
 
 // Pass 2, one CTA per unit: the pool after flush j (ascending keys) is the
@@ -633,75 +646,104 @@ __device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int na, const ui
 // smallest of a union is associative, so it runs as a two-level scan:
 //   1. warp c scans its chunk of groups [j0, j1) alone: the local prefix
 //      after group j (the smallest of groups j0..j), written to the history;
-//   2. warp 0 carries across the chunks: the smallest of groups 0..j0 - 1
-//      for every chunk;
+//   2. the chunks' totals are scanned across the warps (log2(warps) rounds
+//      of merges, all warps at once): the carry of chunk c is the smallest
+//      of groups 0..j0(c) - 1;
 //   3. warp c merges its chunk's carry into each local prefix.
-// The dependent merges per unit drop from nf to about 3 nf / warps + warps.
-// Lanes find their outputs by merge_at; the next group's keys arrive by
-// cp.async during a merge.
+// The dependent merges per unit drop from nf to about 2 nf / warps +
+// log2(warps). Each lane takes a contiguous range of a merge's outputs
+// (merge_range). The lists a warp merges
+// next arrive by cp.async, SCAN_AHEAD of them in flight.
 constexpr int SCAN_WARPS = 32;
+constexpr int SCAN_AHEAD = 4;
+
+// Shared memory of k_pf_scan for sw warps: per warp the running list, its
+// successor and SCAN_AHEAD incoming lists; two lists per warp for the scan of
+// the chunk totals, and their lengths.
+inline size_t scan_smem_bytes(int sw, int P) {
+    return (size_t)sw * P * (2 + SCAN_AHEAD + 2) * 8 + (size_t)sw * 2 * 4;
+}
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__restrict__ gtop,
                                                              uint64_t *__restrict__ phist, int nf, int G, int P) {
-    extern __shared__ uint64_t scan_sm[];   // per warp 4 lists; then chunk totals and carries
+    extern __shared__ uint64_t scan_sm[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int uu = blockIdx.x;
-    uint64_t *A = scan_sm + (size_t)w * 4 * P, *Cn = A + P, *Bc = Cn + P, *Bn = Bc + P;
-    uint64_t *tot = scan_sm + (size_t)nw * 4 * P, *car = tot + (size_t)nw * P;
+    uint64_t *A = scan_sm + (size_t)w * (2 + SCAN_AHEAD) * P, *Cn = A + P, *ring = Cn + P;
+    uint64_t *Sa = scan_sm + (size_t)nw * (2 + SCAN_AHEAD) * P, *Sb = Sa + (size_t)nw * P;
+    int *na_ = reinterpret_cast<int *>(Sb + (size_t)nw * P), *nb_ = na_ + nw;
     const int nb = min(P, G);
     const uint64_t *gt = gtop + (size_t)uu * nf * P;
     uint64_t *ph = phist + (size_t)uu * nf * P;
-    const int j0 = (int)((long long)nf * w / nw), j1 = (int)((long long)nf * (w + 1) / nw);
+    const int j0 = (int)((long long)nf * w / nw), j1 = (int)((long long)nf * (w + 1) / nw);   // j0 < j1: nw <= nf
+    // list q of the ring <- n keys from src; always one commit group (possibly
+    // empty), so that the list of step j is the one SCAN_AHEAD - 1 commits back
+    auto fetch = [&](int q, const uint64_t *src, int n) {
+        for (int k = lane; k < n; k += 32) cp_async8(ring + (size_t)q * P + k, src + k);
+        cp_async_commit();
+    };
     // 1. local prefixes of this warp's chunk
-    if (j0 < j1) {
-        for (int k = lane; k < nb; k += 32) Bc[k] = gt[(size_t)j0 * P + k];
+    for (int q = 0; q < SCAN_AHEAD; ++q) fetch(q, gt + (size_t)(j0 + q) * P, j0 + q < j1 ? nb : 0);
+    int na = 0;
+    for (int j = j0; j < j1; ++j) {
+        const int q = (j - j0) % SCAN_AHEAD;
+        cp_async_wait_group<SCAN_AHEAD - 1>();
         __syncwarp();
-        int na = 0;
-        for (int j = j0; j < j1; ++j) {
-            if (j + 1 < j1)
-                for (int k = lane; k < nb; k += 32) cp_async8(Bn + k, gt + (size_t)(j + 1) * P + k);
-            const int m = (int)min((long long)P, (long long)na + G);
-            for (int k = lane; k < m; k += 32) {
-                const uint64_t x = merge_at(A, na, Bc, nb, k);
-                Cn[k] = x;
-                ph[(size_t)j * P + k] = x;
-            }
-            cp_async_wait_all();
-            __syncwarp();
-            uint64_t *t = A; A = Cn; Cn = t;
-            t = Bc; Bc = Bn; Bn = t;
-            na = m;
-        }
-        for (int k = lane; k < na; k += 32) tot[(size_t)w * P + k] = A[k];
+        const uint64_t *Bc = ring + (size_t)q * P;
+        const int m = (int)min((long long)P, (long long)na + G);
+        int k0, k1;
+        lane_range(m, lane, k0, k1);
+        merge_range(A, na, Bc, nb, k0, k1, [&](int k, uint64_t x) {
+            Cn[k] = x;
+            ph[(size_t)j * P + k] = x;
+        });
+        __syncwarp();
+        fetch(q, gt + (size_t)(j + SCAN_AHEAD) * P, j + SCAN_AHEAD < j1 ? nb : 0);
+        uint64_t *t = A; A = Cn; Cn = t;
+        na = m;
     }
+    for (int k = lane; k < na; k += 32) Sa[(size_t)w * P + k] = A[k];
+    if (lane == 0) na_[w] = na;
     __syncthreads();
-    // 2. carries: car[c] = the smallest min(P, j0(c) G) keys of groups before chunk c
-    if (w == 0) {
-        int nc = 0;
-        for (int c = 1; c < nw; ++c) {
-            const int pj0 = (int)((long long)nf * (c - 1) / nw), pj1 = (int)((long long)nf * c / nw);
-            const int nt = (int)min((long long)P, (long long)(pj1 - pj0) * G);
-            const int m = (int)min((long long)P, (long long)pj1 * G);
-            for (int k = lane; k < m; k += 32)
-                car[(size_t)c * P + k] = merge_at(car + (size_t)(c - 1) * P, nc, tot + (size_t)(c - 1) * P, nt, k);
-            __syncwarp();
-            nc = m;
+    // 2. inclusive scan of the chunk totals (Hillis-Steele): after it Sa[c] is
+    // the smallest of chunks 0..c
+    for (int dd = 1; dd < nw; dd <<= 1) {
+        const uint64_t *x = Sa + (size_t)w * P;
+        uint64_t *y = Sb + (size_t)w * P;
+        if (w >= dd) {
+            const int nx = na_[w - dd], ny = na_[w], m = min(P, nx + ny);
+            int k0, k1;
+            lane_range(m, lane, k0, k1);
+            merge_range(Sa + (size_t)(w - dd) * P, nx, x, ny, k0, k1, [&](int k, uint64_t v) { y[k] = v; });
+            if (lane == 0) nb_[w] = m;
+        } else {
+            for (int k = lane; k < na_[w]; k += 32) y[k] = x[k];
+            if (lane == 0) nb_[w] = na_[w];
         }
+        __syncthreads();
+        uint64_t *t = Sa; Sa = Sb; Sb = t;
+        int *ti = na_; na_ = nb_; nb_ = ti;
     }
-    __syncthreads();
-    // 3. the pool after group j: the carry merged with the local prefix
-    if (w > 0 && j0 < j1) {
-        const int ncar = (int)min((long long)P, (long long)j0 * G);
-        const uint64_t *cw = car + (size_t)w * P;
+    // 3. the pool after group j: the carry (chunks before this one) merged
+    // with the local prefix
+    if (w > 0) {
+        const uint64_t *cw = Sa + (size_t)(w - 1) * P;
+        const int ncar = na_[w - 1];
+        auto nl_of = [&](int j) { return (int)min((long long)P, (long long)(j - j0 + 1) * G); };
+        for (int q = 0; q < SCAN_AHEAD; ++q) fetch(q, ph + (size_t)(j0 + q) * P, j0 + q < j1 ? nl_of(j0 + q) : 0);
         for (int j = j0; j < j1; ++j) {
-            const int nl = (int)min((long long)P, (long long)(j - j0 + 1) * G);
-            const int m = (int)min((long long)P, (long long)(j + 1) * G);
-            for (int k = lane; k < nl; k += 32) Bc[k] = ph[(size_t)j * P + k];
+            const int q = (j - j0) % SCAN_AHEAD;
+            cp_async_wait_group<SCAN_AHEAD - 1>();
             __syncwarp();
-            for (int k = lane; k < m; k += 32) ph[(size_t)j * P + k] = merge_at(cw, ncar, Bc, nl, k);
+            const int nl = nl_of(j), m = (int)min((long long)P, (long long)(j + 1) * G);
+            int k0, k1;
+            lane_range(m, lane, k0, k1);
+            merge_range(cw, ncar, ring + (size_t)q * P, nl, k0, k1, [&](int k, uint64_t v) { ph[(size_t)j * P + k] = v; });
             __syncwarp();
+            fetch(q, ph + (size_t)(j + SCAN_AHEAD) * P, j + SCAN_AHEAD < j1 ? nl_of(j + SCAN_AHEAD) : 0);
         }
     }
+    cp_async_wait_group<0>();
 }
 
 // k, v [U][d] -> ring slot `slot` of every unit
@@ -1010,8 +1052,8 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     if (e != cudaSuccess) return e;
     int sw = nf < SCAN_WARPS ? nf : SCAN_WARPS;
-    while (sw > 1 && (long long)sw * P * 6 * 8 > optin) --sw;
-    k_pf_scan<<<nu, 32 * sw, (size_t)sw * P * 6 * 8, s>>>(gtop, phist, nf, G, P);
+    while (sw > 1 && scan_smem_bytes(sw, P) > (size_t)optin) --sw;
+    k_pf_scan<<<nu, 32 * sw, scan_smem_bytes(sw, P), s>>>(gtop, phist, nf, G, P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     }
