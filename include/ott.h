@@ -85,8 +85,9 @@ enum {
  * Create an empty cache for B sequences, Hq query heads, Hkv kv heads, head
  * dim d, group G, residual window R, pool capacity P (the pages' defaults are
  * G=128, R=32, P=32). max_tokens bounds T; all device memory is allocated
- * here (blocks, residual ring, pool, split-K scratch) and nothing is
- * allocated by the other calls except ott_export_state's staging buffer.
+ * here (blocks, residual ring, pool, split-K scratch). The other calls
+ * allocate nothing, except ott_export_state's staging buffer and the
+ * parallel prefill's stream-ordered scratch (see ott_prefill).
  * Supported: d in {64, 128}; Hq % Hkv == 0 (any ratio g = Hq/Hkv); G >= 1;
  * R >= 0; P >= 0; (P + G) * (d + 8) * 4 bytes of flush staging must fit in
  * one CTA's shared memory. Uses the current CUDA device.
@@ -198,6 +199,12 @@ int ott_destroy(ott_cache *c);
  * Equivalent to L appends in token order (the flush runs for every group of
  * G that leaves the residual window). L may be 0. Errors: OTT_ERR_STATE if
  * T > 0, OTT_ERR_CAPACITY if L > max_tokens.
+ * With fewer (sequence, kv head) units than SMs, the flushes run as one
+ * parallel pass (the pool after every group found by a scan first), with
+ * 16 * P bytes of scratch per (unit, group) allocated on the stream from a
+ * pool the library keeps per device (it holds up to 1 GiB between calls);
+ * the same applies to ott_prefill_lens and ott_prefill_seq. If no scratch
+ * can be had, the flushes run group by group instead.
  */
 int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream);
 
