@@ -570,6 +570,8 @@ __global__ void __launch_bounds__(FLUSH_THREADS, 2) k_flush(FlushArgs a, const _
 // each group's own smallest keys, pass 2 merges them unit by unit into the
 // pool history, pass 3 (k_flush with the history) builds every block.
 constexpr int PF_THREADS = 128;
+// shared memory of k_pf_group: G staged key rows of d + 8 halves, G keys
+inline size_t pf_group_smem_bytes(int d, int G) { return (size_t)G * (d + 8) * 2 + (size_t)G * 8; }
 
 // Pass 1, one CTA per group j of unit u0 + i: the G keys' squared norms,
 // summed in fp32 in channel order exactly as k_flush sums them, and the
@@ -579,16 +581,28 @@ template <int D>
 __global__ void __launch_bounds__(PF_THREADS) k_pf_group(const __half *__restrict__ srcK, long long src_unit_stride,
                                                          int src_u0, int u0, int nf, int G, int P,
                                                          uint64_t *__restrict__ gtop) {
-    extern __shared__ uint64_t gkey[];   // [G]
+    // the group's keys, staged by coalesced asynchronous copies into rows
+    // padded to D + 8 halves (each thread then reads its own row without
+    // bank conflicts), and the group's (norm, index) keys
+    constexpr int RS = D + 8, VPR = D / 8;
+    extern __shared__ __align__(16) uint8_t pf_sm[];
+    __half *rows = reinterpret_cast<__half *>(pf_sm);
+    uint64_t *gkey = reinterpret_cast<uint64_t *>(pf_sm + (size_t)G * RS * 2);   // [G]
     const int uu = blockIdx.x / nf, j = blockIdx.x % nf, u = u0 + uu;
     const long long t0 = (long long)j * G;
-    const __half *base = srcK + (size_t)(u - src_u0) * src_unit_stride;
+    const __half *base = srcK + (size_t)(u - src_u0) * src_unit_stride + (size_t)t0 * D;
+    for (int e = threadIdx.x; e < G * VPR; e += blockDim.x) {
+        const int r = e / VPR, v8 = e % VPR;
+        cp_async16(rows + (size_t)r * RS + 8 * v8, base + (size_t)r * D + 8 * v8);
+    }
+    cp_async_wait_all();
+    __syncthreads();
     for (int t = threadIdx.x; t < G; t += blockDim.x) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(base + (size_t)(t0 + t) * D);
+        const uint4 *row = reinterpret_cast<const uint4 *>(rows + (size_t)t * RS);
         float s = 0.0f;
 #pragma unroll 4
-        for (int v8 = 0; v8 < D / 8; ++v8) {
-            const uint4 x = __ldg(row + v8);
+        for (int v8 = 0; v8 < VPR; ++v8) {
+            const uint4 x = row[v8];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {   // channels 8 v8 + 2e, 8 v8 + 2e + 1
@@ -1040,11 +1054,11 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
     cudaError_t e = cudaSuccess;
     if (P > 0) {   // with no pool every block is its own group: pass 3 alone
     if (c->d == 128)
-        k_pf_group<128><<<(int)groups, PF_THREADS, (size_t)G * 8, s>>>(srcK, src_unit_stride, src_u0, u0, nf, G, P,
-                                                                      gtop);
+        k_pf_group<128><<<(int)groups, PF_THREADS, pf_group_smem_bytes(128, G), s>>>(
+            srcK, src_unit_stride, src_u0, u0, nf, G, P, gtop);
     else
-        k_pf_group<64><<<(int)groups, PF_THREADS, (size_t)G * 8, s>>>(srcK, src_unit_stride, src_u0, u0, nf, G, P,
-                                                                     gtop);
+        k_pf_group<64><<<(int)groups, PF_THREADS, pf_group_smem_bytes(64, G), s>>>(
+            srcK, src_unit_stride, src_u0, u0, nf, G, P, gtop);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // as many warps as groups, at most SCAN_WARPS, within the shared memory
@@ -1171,7 +1185,9 @@ cudaError_t set_flush_attributes(int d, int smem) {
     const void *fns[] = {reinterpret_cast<const void *>(k_flush<128, true>),
                          reinterpret_cast<const void *>(k_flush<128, false>),
                          reinterpret_cast<const void *>(k_flush<64, true>),
-                         reinterpret_cast<const void *>(k_flush<64, false>)};
+                         reinterpret_cast<const void *>(k_flush<64, false>),
+                         reinterpret_cast<const void *>(k_pf_group<128>),
+                         reinterpret_cast<const void *>(k_pf_group<64>)};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
