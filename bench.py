@@ -346,19 +346,20 @@ def copy_peak(ott, dev, stream, gib: int = 2, reps: int = 10):
 
 
 def prefill_launches(w, lens, sm_count: int) -> int:
-    """Kernel launches of one layer's prefill, as the library issues them:
-    when fewer (sequence, kv head) units flush than the GPU has SMs, a prompt
-    of two or more groups takes the parallel pass (group keys, pool scan,
-    every block at once; with P = 0 the blocks alone); otherwise, and under
-    the cold-pool policy, the flushes run group by group (one launch per
-    group for all units that have it). Then the residual tokens are copied
-    (one launch, or one per sequence of a ragged batch)."""
+    """Kernel launches of one layer's prefill, as the library issues them: a
+    prompt of two or more groups takes the parallel pass (group keys, pool
+    scan, every block at once; with P = 0 the blocks alone), except under the
+    cold-pool policy, and in a ragged batch (one pass per sequence) only when
+    fewer (sequence, kv head) units flush than the GPU has SMs; otherwise the
+    flushes run group by group (one launch per group for all units that have
+    it). Then the residual tokens are copied (one launch, or one per sequence
+    of a ragged batch)."""
     nfs = [metrics.flush_count(L, w.G, w.R) for L in lens]
     par_cost = 3 if w.P > 0 else 1
     few = w.B * w.Hkv < sm_count
     if not w.ragged:
         nf = nfs[0]
-        return (par_cost if (nf >= 2 and w.cold < 0 and few) else nf) + 1
+        return (par_cost if (nf >= 2 and w.cold < 0) else nf) + 1
     par = [nf >= 2 and w.cold < 0 and few for nf in nfs]
     serial = max([nf for nf, p in zip(nfs, par) if not p], default=0)
     return par_cost * sum(par) + serial + len(lens)

@@ -70,9 +70,10 @@ void to_per_sequence(ott_cache *c) {
 
 // Every flush of units [u0, u0 + nu), nf each, in one parallel pass (the
 // source holds unit u at (u - src_u0) * unit_stride). False when the policy
-// needs the flushes one after another, when the call flushes enough units
-// (units_flushing) for group-by-group launches to fill the GPU, or when no
-// scratch could be had: the caller then flushes group by group.
+// needs the flushes one after another, when the call runs one pass per
+// sequence and its group-by-group launches would carry enough units
+// (shared_units; 0 for a call with a single pass) to fill the GPU, or when
+// no scratch could be had: the caller then flushes group by group.
 // The parallel prefill's scratch comes from a stream-ordered pool that the
 // library creates once per device and that keeps up to kScratchKeep bytes
 // between calls: with the default pool's threshold of zero, every prefill
@@ -106,9 +107,9 @@ cudaMemPool_t scratch_pool(int dev) {
 }
 
 bool try_prefill_parallel(const ott_cache *c, const __half *K, const __half *V, long long unit_stride, int src_u0,
-                          int u0, int nu, int nf, int units_flushing, cudaStream_t s, cudaError_t &err) {
+                          int u0, int nu, int nf, int shared_units, cudaStream_t s, cudaError_t &err) {
     err = cudaSuccess;
-    if (!prefill_parallel_ok(c, nf, units_flushing)) return false;
+    if (!prefill_parallel_ok(c, nf, shared_units)) return false;
     void *scratch = nullptr;
     const size_t bytes = prefill_scratch_bytes(c, nu, nf);
     const cudaMemPool_t pool = scratch_pool(c->device);
@@ -371,7 +372,7 @@ int ott_prefill(ott_cache *c, const void *K, const void *V, int L, void *stream)
     c->free_blocks -= blocks_needed(c, (long long)nf * c->U);
     c->blocks_settled = 0;
     cudaError_t e = cudaSuccess;
-    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, c->U, s, e)) {
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, 0, 0, c->U, nf, 0, s, e)) {
         for (int j = 0; j < nf && e == cudaSuccess; ++j)
             e = launch_flush(c, Kh, Vh, (long long)L * c->d, LLONG_MAX, (long long)j * c->G, j, s);
     }
@@ -602,7 +603,7 @@ int ott_prefill_seq(ott_cache *c, int b, const void *K, const void *V, int L, vo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const __half *Kh = static_cast<const __half *>(K), *Vh = static_cast<const __half *>(V);
     cudaError_t e = cudaSuccess;
-    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, b * c->Hkv, b * c->Hkv, c->Hkv, nf, c->Hkv, s, e)) {
+    if (!try_prefill_parallel(c, Kh, Vh, (long long)L * c->d, b * c->Hkv, b * c->Hkv, c->Hkv, nf, 0, s, e)) {
         for (int j = 0; j < nf && e == cudaSuccess; ++j) {
             FlushList fl;
             fl.n = 1;

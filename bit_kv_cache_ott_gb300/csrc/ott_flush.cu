@@ -1033,14 +1033,17 @@ cudaError_t launch_flush(const ott_cache *c, const __half *srcK, const __half *s
     return run_flush(c, flush_args(c, srcK, srcV, src_unit_stride, src_mod, t0, j), none, c->U, s);
 }
 
-bool prefill_parallel_ok(const ott_cache *c, int nf, int units_flushing) {
+bool prefill_parallel_ok(const ott_cache *c, int nf, int shared_units) {
     // The cold pool and the channel criterion carry state that a flush needs
-    // from the one before it. The parallel pass pays off when the flushes
-    // flushed group by group would leave the GPU idle: fewer flushing units
-    // than SMs (measured: 32 units x 31 groups 0.21 ms parallel against 0.46
-    // ms group by group; 256 units 0.73 against 0.67; 1024 units 2.3 against
-    // 1.9, where the extra norm pass outweighs the idle tails).
-    return c->cold < 0 && c->pct < 0 && nf >= 2 && units_flushing < c->sm_count;
+    // from the one before it. A call that covers all its units in one pass
+    // (shared_units = 0) always takes it: its one launch of every block has
+    // no idle tails and no sequential launches (measured, 4,096-token
+    // prompts: 1,024 units 1.72 ms against 1.76 ms group by group, 512 units
+    // 0.89 against 1.05, 256 units 0.47 against 0.61). A ragged batch runs
+    // one pass per sequence, one after another; there the group-by-group
+    // launches, shared by every sequence, win once the shared_units they
+    // carry fill the GPU.
+    return c->cold < 0 && c->pct < 0 && nf >= 2 && shared_units < c->sm_count;
 }
 
 cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, const __half *srcV,

@@ -226,7 +226,7 @@ cudaError_t launch_release(const ott_cache *c, int b, cudaStream_t s);
 // Parallel prefill of units [u0, u0 + nu), nf flushes each, from a source
 // holding unit u at (u - src_u0) * src_unit_stride; scratch of
 // prefill_scratch_bytes(c, nu, nf) bytes on the device.
-bool prefill_parallel_ok(const ott_cache *c, int nf, int units_flushing);
+bool prefill_parallel_ok(const ott_cache *c, int nf, int shared_units);
 size_t prefill_scratch_bytes(const ott_cache *c, int nu, int nf);
 cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, const __half *srcV,
                                     long long src_unit_stride, int src_u0, int u0, int nu, int nf,
