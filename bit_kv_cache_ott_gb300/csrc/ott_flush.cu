@@ -25,6 +25,7 @@
 // the per-block count array.
 #include <math_constants.h>
 
+#include <algorithm>
 #include <climits>
 
 #include "ott_internal.cuh"
@@ -655,17 +656,20 @@ __device__ __forceinline__ void lane_range(int m, int lane, int &k0, int &k1) {
     k1 = min(m, k0 + per);
 }
 
-// Pass 2, one CTA per unit: the pool after flush j (ascending keys) is the
-// smallest min(P, (j + 1) G) of groups 0..j's smallest keys. Keeping the
-// smallest of a union is associative, so it runs as a two-level scan:
+// Pass 2: the pool after flush j (ascending keys) is the smallest
+// min(P, (j + 1) G) of groups 0..j's smallest keys. Keeping the smallest of
+// a union is associative, so a unit's groups are cut into C chunks of cg
+// groups, one CTA each (C > 1 when few units would leave SMs idle), and each
+// CTA scans its chunk in two levels:
 //   1. warp c scans its chunk of groups [j0, j1) alone: the local prefix
 //      after group j (the smallest of groups j0..j), written to the history;
 //   2. the chunks' totals are scanned across the warps (log2(warps) rounds
 //      of merges, all warps at once): the carry of chunk c is the smallest
 //      of groups 0..j0(c) - 1;
 //   3. warp c merges its chunk's carry into each local prefix.
-// The dependent merges per unit drop from nf to about 2 nf / warps +
-// log2(warps). Each lane takes a contiguous range of a merge's outputs
+// The dependent merges per chunk are about 2 cg / warps + log2(warps).
+// With C > 1 each CTA leaves its chunk's total in gtot, and k_pf_carry then
+// merges the totals of the chunks before each chunk into its prefixes. Each lane takes a contiguous range of a merge's outputs
 // (merge_range). The lists a warp merges
 // next arrive by cp.async, SCAN_AHEAD of them in flight.
 constexpr int SCAN_WARPS = 32;
@@ -679,17 +683,21 @@ inline size_t scan_smem_bytes(int sw, int P) {
 }
 
 __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__restrict__ gtop,
-                                                             uint64_t *__restrict__ phist, int nf, int G, int P) {
+                                                             uint64_t *__restrict__ phist, int nf_unit, int G, int P,
+                                                             int cg, int C, uint64_t *__restrict__ gtot) {
     extern __shared__ uint64_t scan_sm[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int uu = blockIdx.x;
+    const int uu = blockIdx.x / C, cc = blockIdx.x % C;
     uint64_t *A = scan_sm + (size_t)w * (2 + SCAN_AHEAD) * P, *Cn = A + P, *ring = Cn + P;
     uint64_t *Sa = scan_sm + (size_t)nw * (2 + SCAN_AHEAD) * P, *Sb = Sa + (size_t)nw * P;
     int *na_ = reinterpret_cast<int *>(Sb + (size_t)nw * P), *nb_ = na_ + nw;
     const int nb = min(P, G);
-    const uint64_t *gt = gtop + (size_t)uu * nf * P;
-    uint64_t *ph = phist + (size_t)uu * nf * P;
-    const int j0 = (int)((long long)nf * w / nw), j1 = (int)((long long)nf * (w + 1) / nw);   // j0 < j1: nw <= nf
+    // this CTA's chunk: groups [J0, J0 + nf) of the unit, scanned as if alone
+    const int J0 = cc * cg, nf = min(nf_unit - J0, cg);
+    const uint64_t *gt = gtop + ((size_t)uu * nf_unit + J0) * P;
+    uint64_t *ph = phist + ((size_t)uu * nf_unit + J0) * P;
+    // a warp's range may be empty (a short last chunk)
+    const int j0 = (int)((long long)nf * w / nw), j1 = (int)((long long)nf * (w + 1) / nw);
     // list q of the ring <- n keys from src; always one commit group (possibly
     // empty), so that the list of step j is the one SCAN_AHEAD - 1 commits back
     auto fetch = [&](int q, const uint64_t *src, int n) {
@@ -738,6 +746,11 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
         uint64_t *t = Sa; Sa = Sb; Sb = t;
         int *ti = na_; na_ = nb_; nb_ = ti;
     }
+    // the chunk's total (the smallest of all its groups) for the carries
+    if (C > 1 && w == nw - 1) {
+        uint64_t *dst = gtot + ((size_t)uu * C + cc) * P;
+        for (int k = lane; k < na_[nw - 1]; k += 32) dst[k] = Sa[(size_t)(nw - 1) * P + k];
+    }
     // 3. the pool after group j: the carry (chunks before this one) merged
     // with the local prefix
     if (w > 0) {
@@ -758,6 +771,67 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
         }
     }
     cp_async_wait_group<0>();
+}
+
+// Pass 2b (C > 1), one CTA per unit and chunk c >= 1: the carry of chunk c,
+// the smallest of chunks 0..c-1 (their totals reduced pairwise in
+// ceil(log2 c) rounds), merged into each of its groups' prefixes.
+constexpr int CARRY_MAX_CHUNKS = 32;
+
+inline size_t carry_smem_bytes(int C, int nw, int P) { return ((size_t)2 * C + nw) * P * 8; }
+
+__global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_carry(uint64_t *__restrict__ phist,
+                                                              const uint64_t *__restrict__ gtot, int nf, int G,
+                                                              int P, int cg, int C) {
+    extern __shared__ uint64_t car_sm[];
+    __shared__ int cnt[2][CARRY_MAX_CHUNKS];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int uu = blockIdx.x / (C - 1), c = blockIdx.x % (C - 1) + 1;
+    uint64_t *La = car_sm, *Lb = car_sm + (size_t)C * P, *Bw = car_sm + (size_t)2 * C * P + (size_t)w * P;
+    int *ca = cnt[0], *cb = cnt[1];
+    // the totals of chunks 0..c-1 (chunk x holds min(P, its groups x G) keys)
+    for (int x = threadIdx.x; x < c; x += blockDim.x)
+        ca[x] = (int)min((long long)P, (long long)min(cg, nf - x * cg) * G);
+    __syncthreads();
+    for (int e = threadIdx.x; e < c * P; e += blockDim.x) {
+        const int x = e / P, k = e % P;
+        if (k < ca[x]) La[e] = gtot[((size_t)uu * C + x) * P + k];
+    }
+    __syncthreads();
+    for (int n = c; n > 1;) {
+        const int half = (n + 1) / 2;
+        for (int pi = w; pi < half; pi += nw) {
+            const int x = 2 * pi;
+            uint64_t *y = Lb + (size_t)pi * P;
+            if (x + 1 < n) {
+                const int m = min(P, ca[x] + ca[x + 1]);
+                int k0, k1;
+                lane_range(m, lane, k0, k1);
+                merge_range(La + (size_t)x * P, ca[x], La + (size_t)(x + 1) * P, ca[x + 1], k0, k1,
+                            [&](int k, uint64_t v) { y[k] = v; });
+                if (lane == 0) cb[pi] = m;
+            } else {
+                for (int k = lane; k < ca[x]; k += 32) y[k] = La[(size_t)x * P + k];
+                if (lane == 0) cb[pi] = ca[x];
+            }
+        }
+        __syncthreads();
+        uint64_t *t = La; La = Lb; Lb = t;
+        int *ti = ca; ca = cb; cb = ti;
+        n = half;
+    }
+    const int ncar = ca[0];
+    const int J0 = c * cg, J1 = min(nf, J0 + cg);
+    for (int j = J0 + w; j < J1; j += nw) {
+        const int nl = (int)min((long long)P, (long long)(j - J0 + 1) * G), m = (int)min((long long)P, (long long)(j + 1) * G);
+        uint64_t *pj = phist + ((size_t)uu * nf + j) * P;
+        for (int k = lane; k < nl; k += 32) Bw[k] = pj[k];
+        __syncwarp();
+        int k0, k1;
+        lane_range(m, lane, k0, k1);
+        merge_range(La, ncar, Bw, nl, k0, k1, [&](int k, uint64_t v) { pj[k] = v; });
+        __syncwarp();
+    }
 }
 
 // k, v [U][d] -> ring slot `slot` of every unit
@@ -1046,6 +1120,14 @@ bool prefill_parallel_ok(const ott_cache *c, int nf, int shared_units) {
     return c->cold < 0 && c->pct < 0 && nf >= 2 && shared_units < c->sm_count;
 }
 
+// Chunks per unit of the pool scan: enough CTAs to cover the SMs twice, at
+// most CARRY_MAX_CHUNKS, and chunks of at least SCAN_WARPS groups.
+static int scan_chunks(const ott_cache *c, int nu, int nf) {
+    long long C = std::min<long long>(CARRY_MAX_CHUNKS, (nf + SCAN_WARPS - 1) / SCAN_WARPS);
+    C = std::min<long long>(C, (2LL * c->sm_count + nu - 1) / nu);
+    return C < 1 ? 1 : (int)C;
+}
+
 cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, const __half *srcV,
                                     long long src_unit_stride, int src_u0, int u0, int nu, int nf,
                                     uint64_t *scratch, cudaStream_t s) {
@@ -1064,15 +1146,27 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
             srcK, src_unit_stride, src_u0, u0, nf, G, P, gtop);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // as many warps as groups, at most SCAN_WARPS, within the shared memory
+    // C chunks per unit, one CTA each; as many warps as a chunk has groups,
+    // at most SCAN_WARPS, within the shared memory
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     if (e != cudaSuccess) return e;
-    int sw = nf < SCAN_WARPS ? nf : SCAN_WARPS;
+    const int C = scan_chunks(c, nu, nf), cg = (nf + C - 1) / C;
+    uint64_t *gtot = C > 1 ? phist + (size_t)nu * nf * P : nullptr;
+    int sw = cg < SCAN_WARPS ? cg : SCAN_WARPS;
     while (sw > 1 && scan_smem_bytes(sw, P) > (size_t)optin) --sw;
-    k_pf_scan<<<nu, 32 * sw, scan_smem_bytes(sw, P), s>>>(gtop, phist, nf, G, P);
+    k_pf_scan<<<nu * C, 32 * sw, scan_smem_bytes(sw, P), s>>>(gtop, phist, nf, G, P, cg, C, gtot);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (C > 1) {
+        int cw = cg < SCAN_WARPS ? cg : SCAN_WARPS;
+        const size_t room = (size_t)optin - sizeof(int) * 2 * CARRY_MAX_CHUNKS;   // after the static counts
+        while (cw > 1 && carry_smem_bytes(C, cw, P) > room) --cw;
+        if (carry_smem_bytes(C, cw, P) > room) return cudaErrorInvalidValue;
+        k_pf_carry<<<nu * (C - 1), 32 * cw, carry_smem_bytes(C, cw, P), s>>>(phist, gtot, nf, G, P, cg, C);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     }
     FlushArgs a = flush_args(c, srcK, srcV, src_unit_stride, LLONG_MAX, 0, 0);
     a.src_u0 = src_u0;
@@ -1084,7 +1178,10 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
     return run_flush(c, a, none, (int)groups, s);
 }
 
-size_t prefill_scratch_bytes(const ott_cache *c, int nu, int nf) { return (size_t)2 * nu * nf * c->P * 8 + 16; }
+size_t prefill_scratch_bytes(const ott_cache *c, int nu, int nf) {
+    const int C = scan_chunks(c, nu, nf);
+    return (size_t)2 * nu * nf * c->P * 8 + (C > 1 ? (size_t)nu * C * c->P * 8 : 0) + 16;
+}
 
 cudaError_t launch_flush_list(const ott_cache *c, const __half *srcK, const __half *srcV,
                               long long src_unit_stride, long long src_mod, const FlushList &fl,
@@ -1184,6 +1281,9 @@ cudaError_t launch_export(const ott_cache *c, int u0, int nu, int nf, uint8_t *s
 
 cudaError_t set_flush_attributes(int d, int smem) {
     cudaError_t e = cudaFuncSetAttribute(k_pf_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_pf_carry, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem - (int)sizeof(int) * 2 * CARRY_MAX_CHUNKS);
     if (e != cudaSuccess) return e;
     const void *fns[] = {reinterpret_cast<const void *>(k_flush<128, true>),
                          reinterpret_cast<const void *>(k_flush<128, false>),
