@@ -119,7 +119,11 @@ struct Rows {
 // on the order the values come in): a negative value keeps its sign bit and
 // has its magnitude bits flipped. The map is its own inverse.
 __device__ __forceinline__ uint32_t okey2(uint32_t h2) {
-    return h2 ^ (((h2 >> 15) & 0x00010001u) * 0x7fffu);
+    // 0xffff in each 16-bit lane whose sign bit is set (byte permute with
+    // sign replication of bytes 1 and 3)
+    uint32_t m;
+    asm("prmt.b32 %0, %1, %2, 0xBB99;" : "=r"(m) : "r"(h2), "r"(0u));
+    return h2 ^ (m & 0x7fff7fffu);
 }
 // the fp16 value of the key in the low 16-bit lane
 __device__ __forceinline__ float okey_lo(uint32_t k2) {
