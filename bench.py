@@ -355,14 +355,22 @@ def prefill_launches(w, lens, sm_count: int) -> int:
     it). Then the residual tokens are copied (one launch, or one per sequence
     of a ragged batch)."""
     nfs = [metrics.flush_count(L, w.G, w.R) for L in lens]
-    par_cost = 3 if w.P > 0 else 1
     few = w.B * w.Hkv < sm_count
+
+    def par_cost(nu, nf):
+        # group keys, pool scan (plus its carry pass when the scan is cut
+        # into chunks), every block; with P = 0 the blocks alone
+        if w.P == 0:
+            return 1
+        chunks = max(1, min(32, -(-nf // 32), -(-2 * sm_count // nu)))
+        return 3 + (chunks > 1)
+
     if not w.ragged:
         nf = nfs[0]
-        return (par_cost if (nf >= 2 and w.cold < 0) else nf) + 1
+        return (par_cost(w.B * w.Hkv, nf) if (nf >= 2 and w.cold < 0) else nf) + 1
     par = [nf >= 2 and w.cold < 0 and few for nf in nfs]
     serial = max([nf for nf, p in zip(nfs, par) if not p], default=0)
-    return par_cost * sum(par) + serial + len(lens)
+    return sum(par_cost(w.Hkv, nf) for nf, p in zip(nfs, par) if p) + serial + len(lens)
 
 
 def measure_prefill(ott, w, wr, dev, stream, reps: int = 3):
