@@ -42,6 +42,11 @@ def _appended(ott, K, V, args, kw, L):
     (2, 4, 1, 64, 32, 8, 7, 400),        # d = 64, GQA 4
     (3, 3, 3, 128, 20, 5, 0, 210),       # P = 0, G not a multiple of 16
     (1, 1, 1, 128, 128, 32, 32, 1200),   # the pages' G, R, P
+    # enough groups on few units that the pool scan is cut into chunks with
+    # a carry pass (3, 9 and 6 chunks per unit)
+    (1, 4, 2, 128, 16, 4, 40, 1400),     # P > G
+    (2, 2, 2, 64, 8, 2, 5, 2100),        # d = 64, P < G
+    (1, 8, 1, 128, 16, 0, 64, 3000),     # P = 4 G, R = 0, GQA 8
 ])
 def test_prefill_equals_appends(ott, B, Hq, Hkv, d, G, R, P, L):
     K, V = _gen(B + G + P, B, Hkv, L, d)
