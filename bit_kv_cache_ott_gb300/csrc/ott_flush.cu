@@ -1150,14 +1150,16 @@ cudaError_t launch_prefill_parallel(const ott_cache *c, const __half *srcK, cons
             srcK, src_unit_stride, src_u0, u0, nf, G, P, gtop);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // C chunks per unit, one CTA each; as many warps as a chunk has groups,
-    // at most SCAN_WARPS, within the shared memory
+    // C chunks per unit, one CTA each; a warp per 4 groups of a chunk (fewer,
+    // smaller CTAs cover the SMs in one wave), at most SCAN_WARPS, within
+    // the shared memory
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     if (e != cudaSuccess) return e;
     const int C = scan_chunks(c, nu, nf), cg = (nf + C - 1) / C;
     uint64_t *gtot = C > 1 ? phist + (size_t)nu * nf * P : nullptr;
-    int sw = cg < SCAN_WARPS ? cg : SCAN_WARPS;
+    int sw = (cg + 4 - 1) / 4;
+    sw = sw < 1 ? 1 : (sw > SCAN_WARPS ? SCAN_WARPS : sw);
     while (sw > 1 && scan_smem_bytes(sw, P) > (size_t)optin) --sw;
     k_pf_scan<<<nu * C, 32 * sw, scan_smem_bytes(sw, P), s>>>(gtop, phist, nf, G, P, cg, C, gtot);
     e = cudaGetLastError();
