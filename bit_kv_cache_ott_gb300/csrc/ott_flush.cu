@@ -662,20 +662,21 @@ __device__ __forceinline__ void lane_range(int m, int lane, int &k0, int &k1) {
 
 // Pass 2: the pool after flush j (ascending keys) is the smallest
 // min(P, (j + 1) G) of groups 0..j's smallest keys. Keeping the smallest of
-// a union is associative, so a unit's groups are cut into C chunks of cg
-// groups, one CTA each (C > 1 when few units would leave SMs idle), and each
-// CTA scans its chunk in two levels:
-//   1. warp c scans its chunk of groups [j0, j1) alone: the local prefix
-//      after group j (the smallest of groups j0..j), written to the history;
-//   2. the chunks' totals are scanned across the warps (log2(warps) rounds
-//      of merges, all warps at once): the carry of chunk c is the smallest
-//      of groups 0..j0(c) - 1;
-//   3. warp c merges its chunk's carry into each local prefix.
-// The dependent merges per chunk are about 2 cg / warps + log2(warps).
-// With C > 1 each CTA leaves its chunk's total in gtot, and k_pf_carry then
-// merges the totals of the chunks before each chunk into its prefixes. Each lane takes a contiguous range of a merge's outputs
-// (merge_range). The lists a warp merges
-// next arrive by cp.async, SCAN_AHEAD of them in flight.
+// a union is associative, so the pools are found by a scan. A unit's groups
+// are cut into C chunks of cg groups, one CTA each (C > 1 when few units
+// would leave SMs idle), and each CTA scans its chunk in two levels:
+//   1. warp w scans its own range of the chunk's groups [j0, j1) alone: the
+//      local prefix after group j (the smallest of groups j0..j), written to
+//      the history;
+//   2. the warps' totals are scanned across the warps (log2(warps) rounds of
+//      merges, all warps at once): warp w's carry is the smallest of the
+//      chunk's groups before j0;
+//   3. warp w merges its carry into each of its local prefixes.
+// The dependent merges per chunk are about 2 cg / warps + log2(warps). With
+// C > 1 each CTA leaves its chunk's total in gtot, and k_pf_carry then merges
+// the totals of the chunks before each chunk into that chunk's prefixes.
+// Each lane takes a contiguous range of a merge's outputs (merge_range). The
+// lists a warp merges next arrive by cp.async, SCAN_AHEAD of them in flight.
 constexpr int SCAN_WARPS = 32;
 constexpr int SCAN_AHEAD = 4;
 
@@ -708,7 +709,7 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
         for (int k = lane; k < n; k += 32) cp_async8(ring + (size_t)q * P + k, src + k);
         cp_async_commit();
     };
-    // 1. local prefixes of this warp's chunk
+    // 1. local prefixes of this warp's range
     for (int q = 0; q < SCAN_AHEAD; ++q) fetch(q, gt + (size_t)(j0 + q) * P, j0 + q < j1 ? nb : 0);
     int na = 0;
     for (int j = j0; j < j1; ++j) {
@@ -731,8 +732,8 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
     for (int k = lane; k < na; k += 32) Sa[(size_t)w * P + k] = A[k];
     if (lane == 0) na_[w] = na;
     __syncthreads();
-    // 2. inclusive scan of the chunk totals (Hillis-Steele): after it Sa[c] is
-    // the smallest of chunks 0..c
+    // 2. inclusive scan of the warps' totals (Hillis-Steele): after it Sa[w]
+    // is the smallest of warp ranges 0..w
     for (int dd = 1; dd < nw; dd <<= 1) {
         const uint64_t *x = Sa + (size_t)w * P;
         uint64_t *y = Sb + (size_t)w * P;
@@ -755,8 +756,8 @@ __global__ void __launch_bounds__(SCAN_WARPS * 32) k_pf_scan(const uint64_t *__r
         uint64_t *dst = gtot + ((size_t)uu * C + cc) * P;
         for (int k = lane; k < na_[nw - 1]; k += 32) dst[k] = Sa[(size_t)(nw - 1) * P + k];
     }
-    // 3. the pool after group j: the carry (chunks before this one) merged
-    // with the local prefix
+    // 3. the pool after group j: the carry (the warp ranges before this one)
+    // merged with the local prefix
     if (w > 0) {
         const uint64_t *cw = Sa + (size_t)(w - 1) * P;
         const int ncar = na_[w - 1];
